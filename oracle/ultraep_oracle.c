@@ -1,0 +1,281 @@
+/*
+ * ultraep_oracle.c -- the CPU oracle of the UltraEP balancing hot path.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or
+ * load this file: only the tests, the smoke check and the benchmark's CPU
+ * baseline leg use it.  It shares no code, header, table or helper with the
+ * CUDA library; it is a plain, slow, single-threaded restatement of what each
+ * step computes, written so that it can be checked against its sources by eye.
+ *
+ * Sources (the web pages this method is described on):
+ *   [A] UltraEP article (m.youleyou.com), section "关键设计：让最优负载均衡走进生产"
+ *       (key design): the reserved-slot paragraph, the forward-pass paragraph
+ *       (global load after the gate -> replication planning -> reroute) and the
+ *       control-plane paragraph (solve the quota each expert instance receives;
+ *       each exploration step may instantiate a replica or move load).
+ *   [B] "UltraEP brings real-time MoE balancing to Xiaohongshu's rack-scale
+ *       inference stack", section "What UltraEP does".
+ *   [C] EPLB tutorial, section "EPLB 和 DeepEP 怎么协同？" (dispatch looks up the
+ *       physical replica of each top-k logical id; combine gathers results back
+ *       to their logical owner).
+ *
+ * The pages give no formula; where they are silent this file takes the
+ * plainest reading, and every such reading is marked READING below.
+ *
+ * Integer-only: no floating point appears anywhere in this file.
+ *
+ * Domain: R ranks, E logical experts, H = E/R home experts per rank, S spare
+ * (redundant) slots per rank, P = R*(H+S) physical instances numbered
+ * rank-major: p = r*(H+S) + j.  For j < H, p is the home instance of expert
+ * r*H + j (READING: contiguous home placement); for H <= j < H+S it is spare
+ * slot j-H of rank r.
+ */
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORACLE_OK 0
+#define ORACLE_ITER_LIMIT 2
+
+/* ------------------------------------------------------------------------ */
+/* Step 1: exact per-expert load ("global load after the gate", [A] forward-
+ * pass paragraph; [B] "reads the actual token load after the gate").
+ *
+ * counts[e]        = #{ slots i = t*k + j : ids[i] == e }
+ * counts_src[r][e] = the same, restricted to tokens of source rank r, where
+ *                    READING: rank r owns tokens [r*Tr, (r+1)*Tr), Tr = ceil(T/R).
+ * One (token, k) slot is one unit of load (READING).  Ids outside [0, E) are
+ * skipped; the return value is how many were skipped.                        */
+int64_t oracle_count(const int32_t *ids, int64_t T, int32_t k, int32_t R, int32_t E,
+                     int32_t *counts, int32_t *counts_src)
+{
+    int64_t Tr = (T + R - 1) / R;
+    int64_t invalid = 0;
+    for (int32_t e = 0; e < E; e++) counts[e] = 0;
+    for (int64_t x = 0; x < (int64_t)R * E; x++) counts_src[x] = 0;
+    for (int64_t t = 0; t < T; t++) {
+        int64_t r = t / Tr;
+        for (int32_t j = 0; j < k; j++) {
+            int32_t e = ids[t * k + j];
+            if (e < 0 || e >= E) { invalid++; continue; }
+            counts[e] += 1;
+            counts_src[r * E + e] += 1;
+        }
+    }
+    return invalid;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 2: the coupled replica-placement + quota solve ([A] control-plane
+ * paragraph: solve how much load each expert instance finally receives; one
+ * exploration step either instantiates a new replica or shifts load; [A]
+ * reserved-slot paragraph: a fixed set of spare slots per rank, no allocation).
+ *
+ * The pages do not give the rule.  This is the fixed deterministic reading:
+ *   start: each home instance carries its expert's whole count, spare slots
+ *          are empty, L[r] = sum of the quotas of the instances on rank r;
+ *   repeat:
+ *     1. hot  = argmax_r L[r]                      (ties: lowest r)
+ *     2. on hot, the instance with the largest quota (ties: lowest expert id);
+ *        call its expert e
+ *     3. eligible = ranks c != hot that hold e (home or spare slot) or that
+ *        still have a free spare slot; none -> stop (slots ran out)
+ *     4. cold = argmin over eligible of L[c]       (ties: lowest c)
+ *     5. q = min(quota of the hot instance, floor((L[hot] - L[cold]) / 2));
+ *        q == 0 -> stop
+ *     6. if max_iters moves were made already -> stop with ITER_LIMIT, state
+ *        left as it is
+ *     7. move q from the hot instance to cold's instance of e; if cold does
+ *        not hold e, its lowest-index free slot receives e first (quota 0)
+ *   READING: stopping is global (the rule never retries another instance or
+ *   rank); slots are never released inside one plan; a replica whose quota
+ *   falls to 0 still holds its expert.
+ *
+ * Outputs: quota[P], slot_expert[R*S] (-1 = empty), rank_load[R], and the
+ * logical->physical table as CSR ([C]: per logical expert, its physical
+ * copies): inst_ptr[E+1]; for expert e the entries inst_ptr[e] ..
+ * inst_ptr[e+1]-1 list the home instance first, then the replicas in
+ * ascending p (READING), with inst_cum the inclusive running sum of their
+ * quotas.  Returns ORACLE_OK or ORACLE_ITER_LIMIT; *n_iter = moves made.     */
+int oracle_plan(const int32_t *counts, int32_t R, int32_t E, int32_t S, int32_t max_iters,
+                int32_t *quota, int32_t *slot_expert, int32_t *rank_load,
+                int32_t *inst_ptr, int32_t *inst_id, int32_t *inst_cum, int32_t *n_iter)
+{
+    int32_t H = E / R;
+    int32_t W = H + S;               /* instances per rank */
+    int32_t P = R * W;
+    int64_t *L = (int64_t *)calloc((size_t)R, sizeof(int64_t));
+    int status = ORACLE_OK;
+    int32_t moves = 0;
+
+    for (int32_t p = 0; p < P; p++) quota[p] = 0;
+    for (int32_t x = 0; x < R * S; x++) slot_expert[x] = -1;
+    for (int32_t e = 0; e < E; e++) {
+        int32_t home = e / H;
+        quota[home * W + (e % H)] = counts[e];
+        L[home] += counts[e];
+    }
+
+    for (;;) {
+        /* 1. hottest rank, lowest index on ties */
+        int32_t hot = 0;
+        for (int32_t r = 1; r < R; r++)
+            if (L[r] > L[hot]) hot = r;
+
+        /* 2. its largest-quota instance, lowest expert id on ties */
+        int32_t src_p = -1, src_e = -1;
+        for (int32_t j = 0; j < W; j++) {
+            int32_t p = hot * W + j;
+            int32_t e = (j < H) ? hot * H + j : slot_expert[hot * S + (j - H)];
+            if (e < 0) continue;
+            if (src_p < 0 || quota[p] > quota[src_p] || (quota[p] == quota[src_p] && e < src_e)) {
+                src_p = p;
+                src_e = e;
+            }
+        }
+
+        /* 3-4. coldest eligible rank, lowest index on ties */
+        int32_t cold = -1;
+        for (int32_t c = 0; c < R; c++) {
+            if (c == hot) continue;
+            int holds = (src_e / H == c);
+            int has_free = 0;
+            for (int32_t j = 0; j < S; j++) {
+                if (slot_expert[c * S + j] == src_e) holds = 1;
+                if (slot_expert[c * S + j] < 0) has_free = 1;
+            }
+            if (!(holds || has_free)) continue;
+            if (cold < 0 || L[c] < L[cold]) cold = c;
+        }
+        if (cold < 0) break;                          /* slots ran out */
+
+        /* 5. amount to move */
+        int64_t half = (L[hot] - L[cold]) / 2;
+        int64_t q = quota[src_p] < half ? quota[src_p] : half;
+        if (q <= 0) break;
+
+        /* 6. safety cap */
+        if (moves == max_iters) { status = ORACLE_ITER_LIMIT; break; }
+
+        /* 7. cold's instance of src_e, creating a replica if needed */
+        int32_t dst_p = -1;
+        if (src_e / H == cold) dst_p = cold * W + (src_e % H);
+        for (int32_t j = 0; j < S && dst_p < 0; j++)
+            if (slot_expert[cold * S + j] == src_e) dst_p = cold * W + H + j;
+        for (int32_t j = 0; j < S && dst_p < 0; j++)
+            if (slot_expert[cold * S + j] < 0) {
+                slot_expert[cold * S + j] = src_e;
+                dst_p = cold * W + H + j;
+            }
+
+        quota[src_p] -= (int32_t)q;
+        quota[dst_p] += (int32_t)q;
+        L[hot] -= q;
+        L[cold] += q;
+        moves++;
+    }
+
+    for (int32_t r = 0; r < R; r++) rank_load[r] = (int32_t)L[r];
+
+    /* logical -> physical table: home first, then replicas by ascending p */
+    int32_t m = 0;
+    for (int32_t e = 0; e < E; e++) {
+        int32_t cum = 0;
+        inst_ptr[e] = m;
+        int32_t home_p = (e / H) * W + (e % H);
+        cum += quota[home_p];
+        inst_id[m] = home_p;
+        inst_cum[m] = cum;
+        m++;
+        for (int32_t p = 0; p < P; p++) {
+            int32_t j = p % W;
+            if (j < H) continue;
+            if (slot_expert[(p / W) * S + (j - H)] != e) continue;
+            cum += quota[p];
+            inst_id[m] = p;
+            inst_cum[m] = cum;
+            m++;
+        }
+    }
+    inst_ptr[E] = m;
+
+    *n_iter = moves;
+    free(L);
+    return status;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 3: reroute ([A] forward-pass paragraph: reroute splits the tokens of
+ * one logical expert among its copies; [C]: dispatch maps every top-k
+ * logical id to one physical copy).
+ *
+ * Slots are visited in ascending i = t*k + j.  The slots of expert e, in that
+ * order, get within-expert ranks 0, 1, 2, ...; a slot of rank r goes to the
+ * first instance in e's list whose inclusive cumulative quota exceeds r
+ * (quota prefix rule).  Rows are grouped by instance p ascending and, inside
+ * an instance, by slot i ascending:
+ *   inst_offset[p] = sum of quota[p'] for p' < p   (inst_offset[P] = total)
+ *   dst_row[i]     = inst_offset[p] + (slots already placed in p)
+ *   src_slot[row]  = the slot placed at that row.
+ * Slots with an id outside [0, E), or beyond the quotas of their expert, get
+ * dst_row = -1 and no row.                                                  */
+void oracle_reroute(const int32_t *ids, int64_t T, int32_t k, int32_t R, int32_t E, int32_t S,
+                    const int32_t *quota, const int32_t *inst_ptr, const int32_t *inst_id,
+                    const int32_t *inst_cum, int32_t *dst_row, int32_t *src_slot,
+                    int32_t *inst_offset)
+{
+    int32_t P = R * (E / R + S);
+    int64_t N = T * k;
+    int64_t *seen = (int64_t *)calloc((size_t)E, sizeof(int64_t));
+    int64_t *fill = (int64_t *)calloc((size_t)P, sizeof(int64_t));
+
+    inst_offset[0] = 0;
+    for (int32_t p = 0; p < P; p++) inst_offset[p + 1] = inst_offset[p] + quota[p];
+
+    for (int64_t i = 0; i < N; i++) {
+        int32_t e = ids[i];
+        dst_row[i] = -1;
+        if (e < 0 || e >= E) continue;
+        int64_t r = seen[e]++;
+        int32_t p = -1;
+        for (int32_t m = inst_ptr[e]; m < inst_ptr[e + 1]; m++)
+            if (inst_cum[m] > r) { p = inst_id[m]; break; }
+        if (p < 0) continue;
+        int64_t row = inst_offset[p] + fill[p]++;
+        dst_row[i] = (int32_t)row;
+        src_slot[row] = (int32_t)i;
+    }
+    free(seen);
+    free(fill);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 4: permute -- the local half of dispatch ([C]): each grouped row is the
+ * hidden row of the token its slot came from,
+ *   out[row][:] = hidden[src_slot[row] / k][:]   for row in [0, n_rows),
+ * copied as raw 16-bit words (READING: bit copy, never through float, so
+ * NaN payloads and -0 survive).                                             */
+void oracle_permute(const uint16_t *hidden, int32_t k, int32_t Hd,
+                    const int32_t *src_slot, int64_t n_rows, uint16_t *out)
+{
+    for (int64_t row = 0; row < n_rows; row++) {
+        int64_t t = src_slot[row] / k;
+        for (int32_t h = 0; h < Hd; h++)
+            out[row * Hd + h] = hidden[t * Hd + h];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 5: unpermute -- the local half of combine ([C]: results on physical
+ * copies are gathered back to their logical owner), with no gate weighting:
+ *   y[t][j][:] = grouped[dst_row[t*k + j]][:]
+ * READING: a slot with no row (dst_row < 0) gets a zero row.                */
+void oracle_unpermute(const uint16_t *grouped, int64_t T, int32_t k, int32_t Hd,
+                      const int32_t *dst_row, uint16_t *y)
+{
+    for (int64_t i = 0; i < T * k; i++) {
+        int64_t row = dst_row[i];
+        for (int32_t h = 0; h < Hd; h++)
+            y[i * Hd + h] = (row < 0) ? 0 : grouped[row * Hd + h];
+    }
+}
