@@ -1,0 +1,463 @@
+"""Benchmark of the UltraEP balancing hot path on B300.
+
+One step = one microbatch of the Qwen3-235B-like workload (R=64 ranks, E=128
+experts, S=1 spare slot per rank, top-8, T=131072 tokens, 94 MoE layers,
+hidden 4096 bf16) through all 94 layers; every layer runs
+ep_count -> ep_plan -> ep_reroute -> ep_permute through the C ABI, in that
+order, on one stream.  The metric is microseconds per MoE layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ultraep|reference]
+
+--impl reference times the CPU oracle (the plain C definition of the same
+steps) on the host cores, on a bounded sample of the same workload.
+With N > 1 (torchrun) every rank runs an independent replica on its own GPU
+and microbatch; there is no collective on the data path.
+"""
+import argparse
+import dataclasses
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_expert_load_id_b300 import workload as W  # noqa: E402
+from moe_expert_load_id_b300 import quality as Q  # noqa: E402
+
+WORKLOAD = "qwen3-235b"
+METRIC = "µs per MoE layer (count+plan+reroute+permute) at EP64"
+UNIT = "us/layer"
+N_HIDDEN_BUFS = 2  # distinct hidden inputs, alternating by layer (each 1.07 GB > L2)
+
+# DRAM traffic of one ep_permute launch on this workload, from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum), valid for the permute source
+# with this SHA-256; reported as null once the kernel source changes.
+NCU_PERMUTE = {"source_sha256": None, "bytes_per_launch": None, "capture": None}
+
+
+def _sha(path):
+    with open(path, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()
+
+
+def permute_traffic():
+    src = os.path.join(ROOT, "moe_expert_load_id_b300", "csrc", "permute.cu")
+    if NCU_PERMUTE["source_sha256"] and _sha(src) == NCU_PERMUTE["source_sha256"]:
+        return NCU_PERMUTE["bytes_per_launch"]
+    return None
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return 6400.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of this process's GPU during the timed region."""
+    FIELDS = ("index,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.proc = None
+        self.file = tempfile.NamedTemporaryFile(mode="w+", suffix=".csv", delete=False)
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.uuid = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.seek(0)
+        rows = [r.split(", ") for r in self.file.read().strip().splitlines() if r.strip()]
+        os.unlink(self.file.name)
+        mine = [r for r in rows if len(r) >= 10 and self.uuid and
+                (r[1].strip().lower().endswith(self.uuid.lower().replace("gpu-", "")))]
+        if not mine:
+            mine = [r for r in rows if len(r) >= 10 and r[0].strip() == os.environ.get(
+                "CUDA_VISIBLE_DEVICES", "0").split(",")[0]] or [r for r in rows if len(r) >= 10]
+        if not mine:
+            return None
+        sm = [float(r[2]) for r in mine if r[2].strip().replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in mine if r[3].strip().replace(".", "").isdigit()]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in mine for n, v in zip(names, r[6:10]) if v.strip() == "Active"})
+        loaded = [s for s in sm if mx and s > 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(mine)}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ the CUDA path
+class LayerPipeline:
+    """Per-layer launches of the path for L layers of one microbatch (device buffers)."""
+
+    def __init__(self, U, w, device):
+        self.U, self.w, self.dev = U, w, device
+        i32 = dict(dtype=torch.int32, device=device)
+        L, dom = w.layers, U.Domain(w.R, w.E, w.S, w.k)
+        self.dom = dom
+        self.counts = torch.empty((L, w.E), **i32)
+        self.counts_src = torch.empty((L, w.R, w.E), **i32)
+        self.quota = torch.empty((L, dom.P), **i32)
+        self.slot_expert = torch.empty((L, w.R, w.S), **i32)
+        self.rank_load = torch.empty((L, w.R), **i32)
+        self.inst_ptr = torch.empty((L, w.E + 1), **i32)
+        self.inst_id = torch.empty((L, w.E + w.R * w.S), **i32)
+        self.inst_cum = torch.empty((L, w.E + w.R * w.S), **i32)
+        self.n_iter = torch.empty((L,), **i32)
+        self.inst_status = torch.empty((L,), **i32)
+        self.dev_status = torch.zeros((1,), **i32)
+        self.workspace = torch.zeros((U.ep_count_workspace_bytes(dom, w.T, 1) // 4,), **i32)
+        self.dst_row = torch.empty((1, w.N), **i32)
+        self.inst_offset = torch.empty((1, dom.P + 1), **i32)
+        self.grouped = torch.empty((1, w.N, w.Hd), dtype=torch.bfloat16, device=device)
+
+    def layer(self, l, ids_l, hidden_l, stream, ev=None):
+        U, d = self.U, self.dom
+        s = slice(l, l + 1)
+        if ev is not None:
+            ev[0].record(stream)
+        U.ep_count(d, ids_l, self.counts[s], self.counts_src[s], self.dev_status, self.workspace,
+                   stream)
+        if ev is not None:
+            ev[1].record(stream)
+        U.ep_plan(d, self.counts[s], self.quota[s], self.slot_expert[s], self.rank_load[s],
+                  self.inst_ptr[s], self.inst_id[s], self.inst_cum[s], self.n_iter[s],
+                  self.inst_status[s], 0, stream)
+        if ev is not None:
+            ev[2].record(stream)
+        U.ep_reroute(d, ids_l, self.counts_src[s], self.quota[s], self.inst_ptr[s],
+                     self.inst_id[s], self.inst_cum[s], self.dst_row, None, self.inst_offset,
+                     self.dev_status, stream)
+        if ev is not None:
+            ev[3].record(stream)
+        U.ep_permute(hidden_l, d.k, self.dst_row, self.grouped, self.dev_status, stream)
+        if ev is not None:
+            ev[4].record(stream)
+
+    def step(self, ids, hiddens, stream, events=None):
+        for l in range(self.w.layers):
+            self.layer(l, ids[l:l + 1], hiddens[l % len(hiddens)][None], stream,
+                       None if events is None else events[l])
+
+    def results(self):
+        """The step's result the host reads back: per-layer plan outcome."""
+        return (self.rank_load, self.n_iter, self.inst_status, self.dev_status)
+
+
+def make_inputs(w, microbatch, device):
+    ids = torch.stack([W.topk_ids(w, l, microbatch, device=device) for l in range(w.layers)])
+    hiddens = [W.hidden(w.T, w.Hd, w.seed(1000 + b, microbatch), device=device)
+               for b in range(N_HIDDEN_BUFS)]
+    return ids, hiddens
+
+
+def quality_report(U, w, ids, pipe, microbatch, device):
+    """max/mean rank load over the 94 layers: before, after (GPU plan), lower bound,
+    and an EPLB-style placement built from the previous microbatches' loads."""
+    counts = pipe.counts.cpu().numpy().astype(np.int64)
+    after = pipe.rank_load.cpu().numpy()
+    dom = pipe.dom
+    hist = []
+    hb = U.Buffers(dom, w.T, w.layers, device=device)
+    for m in range(max(0, microbatch - 3), microbatch):      # up to 3 earlier microbatches
+        hids = torch.stack([W.topk_ids(w, l, m, device=device) for l in range(w.layers)])
+        hb.count(hids)
+        hist.append(hb.counts.cpu().numpy().astype(np.float64))
+    before_r, after_r, lb_r, e1_r, ea_r = [], [], [], [], []
+    for l in range(w.layers):
+        c = counts[l]
+        mean = c.sum() / w.R
+        before_r.append(Q.imbalance(Q.home_load(c, w.R)))
+        after_r.append(Q.imbalance(after[l]))
+        lb_r.append(Q.lower_bound(c, w.R, w.S) / mean)
+        if hist:
+            e1 = Q.eval_placement(Q.eplb_global(hist[-1][l], w.R, w.H + w.S), c)
+            ea = Q.eval_placement(Q.eplb_global(np.mean([h[l] for h in hist], 0), w.R,
+                                                w.H + w.S), c)
+            e1_r.append(Q.imbalance(e1))
+            ea_r.append(Q.imbalance(ea))
+    rep = {"metric": "max/mean rank load over the layers of the timed microbatch",
+           "before": Q.summarize(before_r), "ultraep_rule": Q.summarize(after_r),
+           "lower_bound": Q.summarize(lb_r),
+           "plan_n_iter": Q.summarize(pipe.n_iter.cpu().numpy())}
+    if hist:
+        rep["eplb_style_history_W1"] = Q.summarize(e1_r)
+        rep[f"eplb_style_history_W{len(hist)}"] = Q.summarize(ea_r)
+    return rep
+
+
+def run_ultraep(args, rank, world, local):
+    from moe_expert_load_id_b300 import ultraep as U
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    w = args.w
+    microbatch = 3 + rank                 # ranks process different microbatches
+    ids, hiddens = make_inputs(w, microbatch, device)
+    pipe = LayerPipeline(U, w, device)
+    stream = torch.cuda.current_stream(device)
+
+    for _ in range(args.warmup):
+        pipe.step(ids, hiddens, stream)
+    torch.cuda.synchronize(device)
+
+    # ---- timed region: K steps, device events per step and per launch
+    L = w.layers
+    step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
+    kern_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(L)]
+               for _ in range(args.steps)]
+    clocks = ClockSampler(device)
+    barrier(world)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    step_ev[0].record(stream)
+    for k in range(args.steps):
+        pipe.step(ids, hiddens, stream, kern_ev[k])
+        step_ev[k + 1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(world)
+    clock_rep = clocks.stop()
+    total_ms = step_ev[0].elapsed_time(step_ev[-1])
+    total_ms = max_over_ranks(total_ms, world, device)
+    ms_per_step = total_ms / args.steps
+    value = total_ms * 1000.0 / (args.steps * L * world)
+
+    names = ("count", "plan", "reroute", "permute")
+    per = {n: [] for n in names}
+    for k in range(args.steps):
+        for l in range(L):
+            e = kern_ev[k][l]
+            for i, n in enumerate(names):
+                per[n].append(e[i].elapsed_time(e[i + 1]) * 1000.0)
+    avg = {n: float(np.mean(v)) for n, v in per.items()}
+
+    status = int(pipe.dev_status.item())
+    plan_status = pipe.inst_status.cpu().numpy()
+    if status != 0 or (plan_status != 0).any():
+        raise RuntimeError(f"device status {status}, plan status {plan_status.tolist()}")
+
+    # ---- roofline of the dominant kernel (permute) and the bandwidth kernels
+    peak, peak_kind = measured_peaks()
+    perm_bytes = w.T * (2 * w.Hd + 4 * w.k + 2 * w.Hd * w.k)   # read row + k dst + k rows
+    count_bytes = 4 * w.N + 4 * w.E * (w.R + 1)
+    reroute_bytes = 12 * w.N
+    gbs = lambda b, us: b / (us * 1e-6) / 1e9
+    roofline = {"kernel": "ep_permute", "bound": "hbm",
+                "achieved": round(gbs(perm_bytes, avg["permute"]), 1), "peak": peak,
+                "unit": "GB/s", "frac": round(gbs(perm_bytes, avg["permute"]) / peak, 4),
+                "traffic": permute_traffic(), "algorithmic_bytes": perm_bytes,
+                "peak_source": f"{peak_kind} hbm_gbs"}
+    kernels = {n: {"us_per_launch": round(avg[n], 2)} for n in names}
+    kernels["count"].update(gbs=round(gbs(count_bytes, avg["count"]), 1),
+                            frac=round(gbs(count_bytes, avg["count"]) / peak, 4))
+    kernels["reroute"].update(gbs=round(gbs(reroute_bytes, avg["reroute"]), 1),
+                              frac=round(gbs(reroute_bytes, avg["reroute"]) / peak, 4))
+    kernels["permute"].update(gbs=roofline["achieved"], frac=roofline["frac"])
+    kernels["plan"].update(n_iter_mean=float(pipe.n_iter.float().mean().item()))
+
+    # ---- end to end: host (pinned) inputs -> device -> path -> host results
+    e2e = None
+    if args.e2e_steps > 0:
+        ids_h = ids.cpu().pin_memory()
+        hid_h = [h.cpu().pin_memory() for h in hiddens]
+        ids_d = torch.empty_like(ids)
+        hid_d = [torch.empty_like(h) for h in hiddens]
+        res_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in pipe.results()]
+        h2d = ids_h.numel() * 4 + sum(h.numel() * 2 for h in hid_h)
+        d2h = sum(t.numel() * t.element_size() for t in res_h)
+
+        def e2e_step():
+            ids_d.copy_(ids_h, non_blocking=True)
+            for d_, h_ in zip(hid_d, hid_h):
+                d_.copy_(h_, non_blocking=True)
+            pipe.step(ids_d, hid_d, stream)
+            for h_, d_ in zip(res_h, pipe.results()):
+                h_.copy_(d_, non_blocking=True)
+
+        e2e_step()
+        torch.cuda.synchronize(device)
+        barrier(world)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+        e2e = {"value": round(e2e_ms * 1000.0 / (args.e2e_steps * L * world), 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "steps": args.e2e_steps}
+
+    quality = quality_report(U, w, ids, pipe, microbatch, device) if rank == 0 else None
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        cpu = cpu_baseline_sample(w, ids[:args.cpu_layers].cpu().numpy(),
+                                  W.bf16_bits(hiddens[0]))
+
+    line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "int32", "payload": "bf16", "data": "synthetic",
+            "config": {"workload": f"{args.workload}-like: R={w.R} E={w.E} S={w.S} k={w.k} "
+                                   f"T={w.T} layers={w.layers} hidden={w.Hd} bf16, "
+                                   f"Zipf(s={w.s}) popularity re-drawn per microbatch",
+                       "step": "one microbatch through all layers, per layer "
+                               "ep_count -> ep_plan -> ep_reroute -> ep_permute",
+                       "l2": "inputs larger than L2 (1.07 GB hidden per layer, 8.6 GB "
+                             "permute output per layer)",
+                       "parallelism": f"replicas x{world}"},
+            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": 4 * L * args.steps, "clocks": clock_rep, "quality": quality,
+            "pages_context": {"critical_path_overhead_us": "< 300 (per rank, hardware not "
+                                                           "disclosed)",
+                              "planning_us_at_ep64": "< 100",
+                              "imbalance": "1.30-4.01 -> 1.01-1.04"}}
+    return line
+
+
+# ------------------------------------------------------------------ the CPU oracle
+def cpu_baseline_sample(w, ids_layers, hidden_bits, perm_fraction=8):
+    """Time the oracle as it stands (single thread) on a bounded sample: for each
+    sampled layer, count + plan + reroute on the whole layer and permute on the
+    first 1/perm_fraction of the rows (its time scaled up by perm_fraction)."""
+    import oracle
+    oracle.lib()
+    per_layer = []
+    for ids in ids_layers:
+        t0 = time.perf_counter()
+        c, _, _ = oracle.count(ids, w.R, w.E)
+        pl = oracle.plan(c, w.R, w.E, w.S)
+        dst, src, off = oracle.reroute(ids, w.R, w.E, w.S, pl)
+        t1 = time.perf_counter()
+        n = int(off[-1]) // perm_fraction
+        oracle.permute(hidden_bits, w.k, src[:n], n)
+        t2 = time.perf_counter()
+        per_layer.append((t1 - t0) + (t2 - t1) * perm_fraction)
+    value = float(np.mean(per_layer)) * 1e6
+    return {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{len(ids_layers)} layer(s) of the same workload: count+plan+reroute on "
+                      f"the whole layer, permute on 1/{perm_fraction} of the rows scaled "
+                      f"x{perm_fraction}; single-threaded C"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    w = args.w
+    ids = [W.topk_ids(w, l, 3).numpy() for l in range(2)]
+    hid = W.bf16_bits(W.hidden(w.T, w.Hd, w.seed(1000, 3)))
+    times = []
+    for k in range(args.warmup + args.steps):
+        r = cpu_baseline_sample(w, [ids[k % 2]], hid)
+        if k >= args.warmup:
+            times.append(r["value"])
+    value = float(np.mean(times))
+    cpu = {"value": round(value, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": "each step one layer: count+plan+reroute on the whole layer, permute on "
+                     "1/8 of the rows scaled x8; single-threaded C"}
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(value / 1000.0, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "int32", "payload": "bf16",
+            "data": "synthetic",
+            "config": {"workload": f"{args.workload}-like: R={w.R} E={w.E} S={w.S} k={w.k} "
+                                   f"T={w.T} layers={w.layers} hidden={w.Hd} bf16",
+                       "parallelism": "host cores, 1 thread"},
+            "cpu_baseline": cpu,
+            "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ultraep", "reference"), default="ultraep")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(W.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="override T (small cases for profiler captures)")
+    ap.add_argument("--layers", type=int, default=0, help="override the number of layers")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-layers", type=int, default=2)
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    w = W.WORKLOADS[args.workload]
+    if args.tokens or args.layers:
+        w = dataclasses.replace(w, T=args.tokens or w.T, layers=args.layers or w.layers)
+    args.w = w
+    rank, world, local = dist_init()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_ultraep(args, rank, world, local)
+    if rank == 0 and line is not None:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

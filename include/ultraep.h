@@ -1,0 +1,212 @@
+/*
+ * ultraep.h -- C ABI of the UltraEP per-microbatch, per-layer balancing hot path
+ * (hand-written CUDA for sm_103a, library libultraep_b300.so).
+ *
+ * The path, per (layer, microbatch) "instance":
+ *     ep_count -> ep_plan -> ep_reroute -> ep_permute  [-> experts ->]  ep_unpermute
+ *
+ * Sources: UltraEP article (m.youleyou.com), section "key design"
+ * (关键设计：让最优负载均衡走进生产); "UltraEP brings real-time MoE balancing to
+ * Xiaohongshu's rack-scale inference stack", section "What UltraEP does";
+ * EPLB tutorial, section "EPLB 和 DeepEP 怎么协同？" (dispatch / combine).
+ *
+ * Simulated EP domain (one GPU holds all of it): R ranks, E logical experts,
+ * H = E/R home experts per rank, S spare ("redundant") slots per rank, top-k k.
+ * Physical instances are numbered rank-major, P = R*(H+S):
+ *     p = r*(H+S) + j;  j < H: home instance of expert r*H + j;
+ *                       H <= j < H+S: spare slot j-H of rank r.
+ * A token-slot is one (token t, choice j) pair, slot index i = t*k + j; one
+ * slot is one unit of load.  Source rank of token t: t / ceil(T/R).
+ *
+ * Conventions shared by every entry point
+ *  - Every pointer argument is a DEVICE pointer owned by the caller.  The
+ *    library never allocates or frees memory and never synchronises with the
+ *    host: every call only enqueues work on `stream` (a cudaStream_t; NULL is
+ *    the legacy default stream) and returns.
+ *  - Batching: n_inst independent instances are laid out back to back along the
+ *    leading dimension of every array (e.g. topk_ids is [n_inst][T][k]).
+ *  - Pointers must be 4-byte aligned (int32 arrays) and 16-byte aligned
+ *    (bf16 row arrays); bf16 rows must be a multiple of 16 bytes (Hd % 8 == 0).
+ *  - The return value reports only errors the host can see before launching:
+ *    EP_ERR_INVAL (bad shape, null or misaligned pointer, limit exceeded),
+ *    EP_ERR_WORKSPACE (workspace too small) and EP_ERR_CUDA (a launch failed).
+ *    On any error nothing is enqueued (EP_ERR_CUDA: the launch that failed
+ *    may have been partially enqueued).
+ *  - Errors that depend on the data are reported on the device: `dev_status`
+ *    (an int32 the caller zeroes; calls OR EP_DEV_* bits into it) and the
+ *    per-instance `inst_status` of ep_plan.  Kernels never trap.
+ *  - Limits: 1 <= R <= 64, E % R == 0, 1 <= E <= 1024, 0 <= S, H + S <= 32,
+ *    1 <= k <= 32, k <= E, 0 <= T, T*k < 2^31, n_inst >= 0.
+ */
+#ifndef ULTRAEP_H
+#define ULTRAEP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct {
+    int32_t R; /* ranks */
+    int32_t E; /* logical experts; H = E / R must be an integer */
+    int32_t S; /* spare slots per rank */
+    int32_t k; /* top-k */
+} ep_domain_t;
+
+typedef enum {
+    EP_OK = 0,
+    EP_ERR_INVAL = 1,
+    EP_ERR_ITER_LIMIT = 2, /* per-instance status of ep_plan */
+    EP_ERR_BAD_ID = 3,     /* reserved for callers mapping EP_DEV_BAD_ID */
+    EP_ERR_WORKSPACE = 4,
+    EP_ERR_CUDA = 5
+} ep_status_t;
+
+/* bits OR-ed into *dev_status by the kernels */
+#define EP_DEV_BAD_ID 1         /* an expert id outside [0, E) was seen and skipped */
+#define EP_DEV_QUOTA_OVERFLOW 2 /* a slot's within-expert rank exceeded its expert's quotas */
+#define EP_DEV_ROW_RANGE 4      /* a dst_row entry was >= T*k; that row was skipped */
+
+#define EP_PLAN_MAX_ITERS (1 << 16)
+#define EP_MAX_R 64
+#define EP_MAX_E 1024
+#define EP_MAX_K 32
+#define EP_MAX_INSTANCES_PER_RANK 32
+
+/* Bytes of workspace ep_count needs for this shape.  Returns 0 for invalid
+ * arguments. */
+size_t ep_count_workspace_bytes(const ep_domain_t *dom, int64_t T, int32_t n_inst);
+
+/*
+ * ep_count -- exact global load after the gate (UltraEP article, "key design",
+ * forward-pass paragraph: the global load is obtained after gating, before
+ * replication planning; rack-scale summary, "What UltraEP does": the actual
+ * token load is read after the gate and before dispatch).
+ *
+ *   topk_ids   [n_inst][T][k] int32   the gate's top-k logical expert ids
+ *   counts     [n_inst][E]    int32   out: counts[e] = #{slots with id e}
+ *   counts_src [n_inst][R][E] int32   out: the same per source rank
+ *                                     (tokens [r*ceil(T/R), (r+1)*ceil(T/R)))
+ *   dev_status int32                  out: |= EP_DEV_BAD_ID if an id was
+ *                                     outside [0, E) (it is skipped)
+ *   workspace  ep_count_workspace_bytes() bytes, caller-owned, 16-byte
+ *              aligned.  Its first 4*n_inst*(R+1) bytes are tickets that find
+ *              the last block of each source rank and instance: they must be
+ *              zero before the first call, and every call resets them to zero
+ *              on completion, so the workspace can be reused by later calls on
+ *              the same stream without clearing.  The rest is scratch for
+ *              per-chunk partial histograms.  Calls that share a workspace must
+ *              not overlap on the GPU.
+ */
+ep_status_t ep_count(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T, int32_t n_inst,
+                     int32_t *counts, int32_t *counts_src, int32_t *dev_status,
+                     void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * ep_plan -- the coupled replica-placement + quota solve (UltraEP article,
+ * "key design", control-plane paragraph: solve how much load each expert
+ * instance finally receives, each step either instantiating a replica or
+ * shifting load, warp-level parallel; reserved-slot paragraph: a fixed set of
+ * spare slots per rank).  One warp solves each instance.
+ *
+ * The pages do not state the rule; this library fixes one deterministic rule:
+ *   start: home instances carry their expert's count, spare slots are empty,
+ *          L[r] = load of rank r;
+ *   repeat: hot = argmax L (lowest r on ties); e = expert of hot's
+ *     largest-quota instance (lowest expert id on ties); eligible = ranks
+ *     c != hot that hold e or have a free spare slot (none: stop);
+ *     cold = argmin L over eligible (lowest c on ties);
+ *     q = min(that instance's quota, floor((L[hot] - L[cold]) / 2)) (0: stop);
+ *     after max_iters moves, if another move is due: stop with
+ *     EP_ERR_ITER_LIMIT, leaving the state as it is;
+ *     move q to cold's instance of e, first filling cold's lowest free slot
+ *     with e if cold does not hold e.  Slots are never released.
+ *
+ *   counts      [n_inst][E]       int32 in
+ *   max_iters   cap on the moves of one instance; <= 0 means EP_PLAN_MAX_ITERS
+ *   quota       [n_inst][P]       int32 out: load of every physical instance
+ *   slot_expert [n_inst][R][S]    int32 out: expert in each spare slot, -1 empty
+ *   rank_load   [n_inst][R]       int32 out
+ *   inst_ptr    [n_inst][E+1]     int32 out: CSR row pointers of the
+ *   inst_id     [n_inst][E+R*S]   int32 out:   logical -> physical table; for
+ *   inst_cum    [n_inst][E+R*S]   int32 out:   expert e, entries inst_ptr[e] ..
+ *               inst_ptr[e+1]-1 list its home instance first and then its
+ *               replicas by ascending p, with inst_cum the inclusive running
+ *               sum of their quotas.  Entries past inst_ptr[E] are not written.
+ *   n_iter      [n_inst]          int32 out: moves made
+ *   inst_status [n_inst]          int32 out: EP_OK, EP_ERR_ITER_LIMIT, or
+ *               EP_ERR_INVAL when a count is negative or the counts sum to
+ *               2^31 or more (no move is made; outputs show home placement)
+ */
+ep_status_t ep_plan(const ep_domain_t *dom, const int32_t *counts, int32_t n_inst,
+                    int32_t max_iters, int32_t *quota, int32_t *slot_expert, int32_t *rank_load,
+                    int32_t *inst_ptr, int32_t *inst_id, int32_t *inst_cum,
+                    int32_t *n_iter, int32_t *inst_status, void *stream);
+
+/*
+ * ep_reroute -- split every logical expert's slots among its instances
+ * (UltraEP article, "key design", forward-pass paragraph: reroute divides the
+ * tokens of one logical expert among its replicas; EPLB tutorial, dispatch:
+ * every top-k logical id is mapped to one physical copy).
+ *
+ * Quota-prefix rule: the slots of expert e, in ascending slot index, get
+ * within-expert ranks 0, 1, ...; a slot of rank r goes to the first entry of
+ * e's instance list whose inst_cum exceeds r.  Rows are grouped by instance p
+ * ascending and, inside an instance, by slot index ascending.
+ *
+ *   topk_ids    [n_inst][T][k]   int32 in
+ *   counts_src  [n_inst][R][E]   int32 in  (from ep_count on the same ids)
+ *   quota, inst_ptr, inst_id, inst_cum   in (from ep_plan)
+ *   dst_row     [n_inst][T*k]    int32 out: row of each slot; -1 for a slot
+ *                                with an invalid id or beyond its quotas
+ *   src_slot    [n_inst][T*k]    int32 out (may be NULL): slot of each row;
+ *                                entries past the last row are not written
+ *   inst_offset [n_inst][P+1]    int32 out: first row of every instance
+ *                                (exclusive prefix sum of quota)
+ *   dev_status  int32            out: |= EP_DEV_BAD_ID, EP_DEV_QUOTA_OVERFLOW
+ */
+ep_status_t ep_reroute(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T, int32_t n_inst,
+                       const int32_t *counts_src, const int32_t *quota, const int32_t *inst_ptr,
+                       const int32_t *inst_id, const int32_t *inst_cum, int32_t *dst_row,
+                       int32_t *src_slot, int32_t *inst_offset, int32_t *dev_status,
+                       void *stream);
+
+/*
+ * ep_permute -- the local half of dispatch (EPLB tutorial, "EPLB 和 DeepEP
+ * 怎么协同？": every token is sent to the physical copy of each of its
+ * top-k experts): out[dst_row[t*k+j]] = hidden[t] for every slot with a row.
+ * Rows are copied bit for bit (bf16 payload never converted).
+ *
+ *   hidden  [n_inst][T][Hd]   bf16 in
+ *   dst_row [n_inst][T*k]     int32 in (from ep_reroute); < 0: no row
+ *   out     [n_inst][T*k][Hd] bf16 out; rows nobody maps to are not written
+ *   dev_status int32          out: |= EP_DEV_ROW_RANGE for a dst_row >= T*k
+ */
+ep_status_t ep_permute(const void *hidden, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
+                       const int32_t *dst_row, void *out, int32_t *dev_status, void *stream);
+
+/*
+ * ep_unpermute -- the local half of combine (EPLB tutorial, same section:
+ * results on physical copies are gathered back to their logical owner), with
+ * no gate weighting: y[t][j] = grouped[dst_row[t*k+j]]; a slot with no row
+ * (dst_row < 0) gets a zero row.
+ *
+ *   grouped [n_inst][T*k][Hd] bf16 in
+ *   dst_row [n_inst][T*k]     int32 in
+ *   y       [n_inst][T][k][Hd] bf16 out
+ *   dev_status int32          out: |= EP_DEV_ROW_RANGE for a dst_row >= T*k
+ *                             (that output row is zeroed)
+ */
+ep_status_t ep_unpermute(const void *grouped, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
+                         const int32_t *dst_row, void *y, int32_t *dev_status, void *stream);
+
+/* Static string naming a status code. */
+const char *ep_status_str(ep_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ULTRAEP_H */

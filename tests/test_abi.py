@@ -1,0 +1,95 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry point
+include/ultraep.h declares, and rejects bad arguments on the host before any
+CUDA call (no call here reaches a kernel launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from moe_expert_load_id_b300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ultraep.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(libbuild.LIB):
+        libbuild.build()
+    return ctypes.CDLL(libbuild.LIB)
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ep_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path():
+    names = declared_functions()
+    for n in ("ep_count", "ep_plan", "ep_reroute", "ep_permute", "ep_unpermute"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+class Dom(ctypes.Structure):
+    _fields_ = [("R", ctypes.c_int32), ("E", ctypes.c_int32), ("S", ctypes.c_int32),
+                ("k", ctypes.c_int32)]
+
+
+def _setup(lib):
+    vp = ctypes.c_void_p
+    lib.ep_count_workspace_bytes.restype = ctypes.c_size_t
+    lib.ep_count_workspace_bytes.argtypes = [ctypes.POINTER(Dom), ctypes.c_int64, ctypes.c_int32]
+    lib.ep_count.argtypes = [ctypes.POINTER(Dom), vp, ctypes.c_int64, ctypes.c_int32, vp, vp, vp,
+                             vp, ctypes.c_size_t, vp]
+    lib.ep_plan.argtypes = [ctypes.POINTER(Dom), vp, ctypes.c_int32, ctypes.c_int32] + [vp] * 9
+    lib.ep_permute.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                               vp, vp, vp, vp]
+    lib.ep_status_str.restype = ctypes.c_char_p
+
+
+@pytest.mark.parametrize("R,E,S,k,ok", [(8, 32, 1, 4, True), (64, 128, 1, 8, True),
+                                        (64, 256, 2, 8, True), (40, 160, 1, 8, True),
+                                        (0, 32, 1, 4, False), (65, 130, 1, 8, False),
+                                        (8, 30, 1, 4, False), (8, 32, -1, 4, False),
+                                        (8, 32, 1, 0, False), (8, 32, 1, 33, False),
+                                        (4, 8, 1, 9, False), (2, 62, 2, 8, False)])
+def test_domain_validation(lib, R, E, S, k, ok):
+    _setup(lib)
+    d = Dom(R, E, S, k)
+    ws = lib.ep_count_workspace_bytes(ctypes.byref(d), 4096, 4)
+    assert (ws > 0) == ok
+
+
+def test_host_rejections_need_no_gpu(lib):
+    _setup(lib)
+    d = Dom(8, 32, 1, 4)
+    fake = ctypes.c_void_p(0x10000)       # never dereferenced: every call below fails validation
+    # null domain, bad domain, negative T, T*k >= 2^31
+    assert lib.ep_count(None, fake, 16, 1, fake, fake, None, fake, 1 << 20, None) == 1
+    assert lib.ep_count(ctypes.byref(Dom(8, 30, 1, 4)), fake, 16, 1, fake, fake, None, fake,
+                        1 << 20, None) == 1
+    assert lib.ep_count(ctypes.byref(d), fake, -1, 1, fake, fake, None, fake, 1 << 20, None) == 1
+    assert lib.ep_count(ctypes.byref(d), fake, 1 << 29, 1, fake, fake, None, fake, 1 << 20,
+                        None) == 1
+    # missing outputs, misaligned pointer, too-small workspace
+    assert lib.ep_count(ctypes.byref(d), fake, 16, 1, None, fake, None, fake, 1 << 20, None) == 1
+    assert lib.ep_count(ctypes.byref(d), ctypes.c_void_p(0x10002), 16, 1, fake, fake, None,
+                        fake, 1 << 20, None) == 1
+    assert lib.ep_count(ctypes.byref(d), fake, 16, 1, fake, fake, None, fake, 4, None) == 4
+    # zero instances: nothing to do, nothing launched
+    assert lib.ep_count(ctypes.byref(d), None, 16, 0, None, None, None, None, 0, None) == 0
+    assert lib.ep_plan(ctypes.byref(d), None, 0, 0, *([None] * 9)) == 0
+    # permute: Hd not a multiple of 8, misaligned row pointers, k out of range
+    assert lib.ep_permute(fake, 4, 2, 12, 1, fake, fake, None, None) == 1
+    assert lib.ep_permute(ctypes.c_void_p(0x10008), 4, 2, 16, 1, fake, fake, None, None) == 1
+    assert lib.ep_permute(fake, 4, 0, 16, 1, fake, fake, None, None) == 1
+    assert lib.ep_permute(fake, 0, 2, 16, 1, None, fake, None, None) == 0
+    assert lib.ep_status_str(0) == b"EP_OK"
+    assert b"workspace" in lib.ep_status_str(4)

@@ -1,0 +1,307 @@
+"""GPU parity: every C-ABI call against the CPU oracle, bit-exact, on seeded inputs.
+
+Small and medium cases compare every output element; the full-size workloads
+compare the index outputs completely and the bf16 rows on a seeded sample.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from moe_expert_load_id_b300 import workload as W
+
+from golden_io import read_sections, as_array
+from plan_checks import check_plan, check_reroute
+
+pytestmark = pytest.mark.gpu
+
+U = None
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    """Load the C-ABI binding (an ImportError here means the library is not built)."""
+    global U
+    from moe_expert_load_id_b300 import ultraep
+    U = ultraep
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+
+
+def G():
+    import gpu_common
+    return gpu_common
+
+
+def _ids_from_counts(counts, seed):
+    rng = np.random.default_rng(seed)
+    ids = np.repeat(np.arange(len(counts), dtype=np.int32), counts)
+    rng.shuffle(ids)
+    return ids.reshape(1, -1, 1)
+
+
+# ------------------------------------------------------------------ hand examples
+HAND = read_sections("plan_hand_examples.txt")
+
+
+@pytest.mark.parametrize("name", sorted(HAND))
+def test_hand_examples(name):
+    ex = HAND[name]
+    R, E, S = ex["R"], ex["E"], ex["S"]
+    if "ids" in ex:
+        ids = as_array(ex["ids"]).astype(np.int32).reshape(1, ex["T"], ex["k"])
+    else:
+        ids = _ids_from_counts(as_array(ex["counts"]), 5)
+    k = ids.shape[2]
+    dom = G().dom_of(R, E, S, k)
+    out = G().gpu_run(dom, ids, max_iters=ex["max_iters"])
+    for key in ("quota", "rank_load", "inst_ptr"):
+        G().assert_equal(key, out[key][0], as_array(ex[key]))
+    G().assert_equal("slot_expert", out["slot_expert"][0].reshape(-1), as_array(ex["slot_expert"]))
+    m = int(as_array(ex["inst_ptr"])[-1])
+    G().assert_equal("inst_id", out["inst_id"][0][:m], as_array(ex["inst_id"]))
+    G().assert_equal("inst_cum", out["inst_cum"][0][:m], as_array(ex["inst_cum"]))
+    assert int(out["n_iter"][0]) == ex["n_iter"]
+    assert int(out["inst_status"][0]) == ex["status"]
+    if "dst_row" in ex:
+        G().assert_equal("dst_row", out["dst_row"][0], as_array(ex["dst_row"]))
+        G().assert_equal("inst_offset", out["inst_offset"][0], as_array(ex["inst_offset"]))
+        n = int(as_array(ex["inst_offset"])[-1])
+        G().assert_equal("src_slot", out["src_slot"][0][:n], as_array(ex["src_slot"])[:n])
+    orc = G().oracle_run(R, E, S, ids, max_iters=ex["max_iters"])
+    G().compare(R, E, S, out, orc)
+
+
+# ------------------------------------------------------------------ tiny workload
+def _tiny_inputs(layers):
+    w = W.WORKLOADS["tiny"]
+    ids = np.stack([W.topk_ids(w, l, 0).numpy() for l in layers])
+    hid = np.stack([W.bf16_bits(W.hidden(w.T, w.Hd, w.seed(l, 0))) for l in layers])
+    return w, ids, hid
+
+
+def test_tiny_workload_batched():
+    w, ids, hid = _tiny_inputs(range(W.WORKLOADS["tiny"].layers))
+    dom = G().dom_of(w.R, w.E, w.S, w.k)
+    out = G().gpu_run(dom, ids, hid)
+    orc = G().oracle_run(w.R, w.E, w.S, ids, hid)
+    G().compare(w.R, w.E, w.S, out, orc)
+    assert (out["dev_status"] == 0).all()
+    assert (out["y"] == hid[:, :, None, :]).all()          # round trip is the identity
+
+
+@pytest.mark.parametrize("layer", range(4))
+def test_tiny_workload_per_layer(layer):
+    w, ids, hid = _tiny_inputs([layer])
+    dom = G().dom_of(w.R, w.E, w.S, w.k)
+    out = G().gpu_run(dom, ids, hid)
+    G().compare(w.R, w.E, w.S, out, G().oracle_run(w.R, w.E, w.S, ids, hid))
+
+
+# ------------------------------------------------------------------ sweep of shapes and edge cases
+CASES = [
+    # name,                R,  H, S, k,  T,     n_inst, Hd,  kind
+    ("empty_T",            8,  4, 1, 4,  0,     2,      16,  "zipf"),
+    ("k1",                 8,  4, 1, 1,  777,   1,      16,  "zipf"),
+    ("one_expert",         8,  1, 1, 1,  5000,  1,      8,   "one"),
+    ("uniform",            16, 2, 2, 4,  4096,  1,      8,   "uniform"),
+    ("no_spares",          8,  4, 0, 4,  3000,  2,      8,   "zipf"),
+    ("H1",                 32, 1, 1, 2,  2048,  1,      8,   "zipf"),
+    ("R64_mask_width",     64, 2, 1, 8,  8192,  1,      64,  "zipf"),
+    ("R64_S4",             64, 4, 4, 8,  4096,  2,      8,   "zipf"),
+    ("ragged_T",           8,  4, 1, 4,  1001,  3,      24,  "zipf"),
+    ("T_below_R",          8,  2, 1, 3,  5,     1,      8,   "zipf"),
+    ("invalid_and_dups",   8,  4, 1, 4,  2000,  2,      8,   "bad"),
+    ("many_chunks",        4,  4, 2, 8,  40000, 1,      8,   "zipf"),
+    ("max_E_and_k",        64, 16, 16, 32, 1024, 1,     8,   "zipf"),
+    ("many_instances",     8,  4, 1, 4,  512,   33,     8,   "zipf"),
+    ("hidden_264",         8,  4, 1, 4,  300,   1,      264, "zipf"),
+    ("hidden_4096",        16, 4, 1, 8,  512,   1,      4096, "zipf"),
+]
+
+
+def _make_ids(R, E, k, T, n_inst, kind, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for g in range(n_inst):
+        if kind == "one":
+            ids = np.zeros((T, k), np.int32)
+        elif kind == "uniform":
+            ids = (np.arange(T * k, dtype=np.int32) % E).reshape(T, k)
+        else:
+            p = 1.0 / (rng.permutation(E) + 1.0) ** 1.1
+            ids = W.gumbel_topk(p / p.sum(), T, k, seed * 100 + g).numpy()
+            if kind == "bad" and T:
+                ids[rng.integers(0, T, 5), 0] = E + 7
+                ids[rng.integers(0, T, 5), -1] = -3
+                if k > 1:
+                    ids[rng.integers(0, T, 5), 1] = ids[rng.integers(0, T, 5), 0] % E  # duplicates
+        out.append(ids)
+    return np.stack(out) if n_inst else np.zeros((0, T, k), np.int32)
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_shape_sweep(case):
+    name, R, H, S, k, T, n_inst, Hd, kind = case
+    E = R * H
+    ids = _make_ids(R, E, k, T, n_inst, kind, seed=len(name) * 7919 + T)
+    rng = np.random.default_rng(T + Hd)
+    hid = rng.integers(0, 1 << 16, size=(n_inst, T, Hd), dtype=np.uint16)
+    dom = G().dom_of(R, E, S, k)
+    out = G().gpu_run(dom, ids, hid)
+    orc = G().oracle_run(R, E, S, ids, hid)
+    G().compare(R, E, S, out, orc)
+    expect_flag = 1 if any(n > 0 for n in orc["n_bad"]) else 0
+    assert int(out["dev_status"][0]) == expect_flag
+    for g in range(n_inst):
+        pl = {key: out[key][g] for key in ("quota", "slot_expert", "rank_load", "inst_ptr",
+                                          "inst_id", "inst_cum")}
+        pl.update(n_iter=int(out["n_iter"][g]), status=int(out["inst_status"][g]))
+        check_plan(out["counts"][g], R, E, S, pl)
+        check_reroute(ids[g], R, E, S, pl, out["dst_row"][g], out["src_slot"][g],
+                      out["inst_offset"][g])
+
+
+def test_iteration_cap_matches_oracle():
+    R, H, S, k, T = 16, 4, 2, 8, 20000
+    ids = _make_ids(R, R * H, k, T, 3, "zipf", 99)
+    dom = G().dom_of(R, R * H, S, k)
+    full = G().oracle_run(R, R * H, S, ids)
+    for cap in (1, 2, max(1, min(full["n_iter"]) // 2)):
+        out = G().gpu_run(dom, ids, max_iters=cap)
+        orc = G().oracle_run(R, R * H, S, ids, max_iters=cap)
+        G().compare(R, R * H, S, out, orc)
+        assert (out["inst_status"] == 2).any()
+
+
+def test_plan_rejects_bad_counts():
+    dom = G().dom_of(4, 8, 1, 2)
+    b = U.Buffers(dom, 16, 2)
+    b.counts.copy_(torch.tensor([[5, -1, 0, 0, 0, 0, 0, 0],
+                                 [2 ** 30, 2 ** 30, 0, 0, 0, 0, 0, 0]], dtype=torch.int32))
+    b.plan()
+    st = b.inst_status.cpu().numpy()
+    assert st.tolist() == [U.EP_ERR_INVAL, U.EP_ERR_INVAL]
+    assert (b.n_iter.cpu().numpy() == 0).all()
+
+
+def test_device_status_flags():
+    R, E, S, k, T, Hd = 4, 8, 1, 2, 64, 8
+    dom = G().dom_of(R, E, S, k)
+    ids = _make_ids(R, E, k, T, 1, "zipf", 3)
+    ids[0, 3, 1] = 99                                      # bad id
+    out = G().gpu_run(dom, ids)
+    assert int(out["dev_status"][0]) & U.EP_DEV_BAD_ID
+    # a plan whose quotas do not cover the ids: overflowing slots get no row
+    b = U.Buffers(dom, T, 1)
+    dids = torch.from_numpy(ids).cuda()
+    b.count(dids)
+    b.plan()
+    b.quota.zero_()
+    b.inst_cum.zero_()
+    b.dev_status.zero_()
+    b.reroute(dids)
+    assert int(b.dev_status.item()) & U.EP_DEV_QUOTA_OVERFLOW
+    assert (b.dst_row.cpu().numpy() == -1).all()
+    # a dst_row past the last row: permute skips it, unpermute zeroes it
+    hidden = torch.ones((T, Hd), dtype=torch.bfloat16, device="cuda")
+    dst = torch.arange(T * k, dtype=torch.int32, device="cuda")
+    dst[5] = T * k + 3
+    out_rows = torch.zeros((T * k, Hd), dtype=torch.bfloat16, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    U.ep_permute(hidden, k, dst, out_rows, st)
+    assert int(st.item()) & U.EP_DEV_ROW_RANGE
+    assert float(out_rows[5].float().abs().sum()) == 0.0
+    y = torch.full((T, k, Hd), 7.0, dtype=torch.bfloat16, device="cuda")
+    st.zero_()
+    U.ep_unpermute(out_rows, T, k, dst, y, st)
+    assert int(st.item()) & U.EP_DEV_ROW_RANGE
+    assert float(y.reshape(T * k, Hd)[5].float().abs().sum()) == 0.0
+
+
+def test_workspace_reused_across_calls():
+    w, ids, _ = _tiny_inputs([0, 1])
+    dom = G().dom_of(w.R, w.E, w.S, w.k)
+    b = U.Buffers(dom, w.T, 2)
+    d = torch.from_numpy(ids).cuda()
+    outs = []
+    for _ in range(3):
+        b.count(d)
+        outs.append((b.counts.cpu().numpy().copy(), b.counts_src.cpu().numpy().copy()))
+        assert (b.workspace.cpu().numpy()[:2 * (w.R + 1)] == 0).all()
+    for c, cs in outs[1:]:
+        assert (c == outs[0][0]).all() and (cs == outs[0][1]).all()
+
+
+def test_permute_preserves_bit_patterns():
+    # NaN payloads, infinities and -0 pass through unchanged
+    T, k, Hd = 7, 3, 16
+    pat = np.array([0x7FC1, 0xFF80, 0x8000, 0x0001, 0x7F80, 0xFFFF, 0x1234, 0x8001], np.uint16)
+    hid = np.tile(pat, (T, Hd // 8)).reshape(T, Hd)
+    hid[:, 0] = np.arange(T, dtype=np.uint16)
+    ids = np.stack([np.arange(T * k, dtype=np.int32).reshape(T, k) % 4])
+    dom = G().dom_of(2, 4, 1, k)
+    out = G().gpu_run(dom, ids, hid[None])
+    G().compare(2, 4, 1, out, G().oracle_run(2, 4, 1, ids, hid[None]))
+
+
+# ------------------------------------------------------------------ full-size workloads
+def _full_size_layer(name, layer, microbatch, n_samples=4096):
+    w = W.WORKLOADS[name]
+    ids_d = W.topk_ids(w, layer, microbatch, device="cuda")
+    hid_d = W.hidden(w.T, w.Hd, w.seed(layer, microbatch), device="cuda")
+    ids = ids_d.cpu().numpy()[None]
+    dom = U.Domain(w.R, w.E, w.S, w.k)
+    b = U.Buffers(dom, w.T, 1, Hd=w.Hd, device="cuda", src_slot=True)
+    b.balance(ids_d[None], hid_d[None])                    # the per-layer launches the bench times
+    y = torch.empty((1, w.T, w.k, w.Hd), dtype=torch.bfloat16, device="cuda")
+    U.ep_unpermute(b.grouped, w.T, w.k, b.dst_row, y, b.dev_status)
+    torch.cuda.synchronize()
+    orc = G().oracle_run(w.R, w.E, w.S, ids)
+    out = {key: getattr(b, key).cpu().numpy() for key in
+           ("counts", "counts_src", "quota", "slot_expert", "rank_load", "inst_ptr", "inst_id",
+            "inst_cum", "n_iter", "inst_status", "dst_row", "inst_offset", "workspace",
+            "src_slot", "dev_status")}
+    G().compare(w.R, w.E, w.S, out, orc, check_rows=False)
+    assert int(out["dev_status"][0]) == 0
+    # rows: a seeded sample of grouped rows against the oracle's source token
+    rng = np.random.default_rng(layer * 31 + microbatch)
+    n_rows = int(orc["inst_offset"][0][-1])
+    rows = np.sort(rng.choice(n_rows, size=min(n_samples, n_rows), replace=False))
+    src_tok = orc["src_slot"][0][rows] // w.k
+    got = b.grouped[0][torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy()
+    want = hid_d[torch.from_numpy(src_tok).cuda()].view(torch.int16).cpu().numpy()
+    assert np.array_equal(got, want)
+    # unpermute: a seeded sample of slots against the token's own row
+    slots = np.sort(rng.choice(w.N, size=n_samples, replace=False))
+    gy = y.reshape(w.N, w.Hd)[torch.from_numpy(slots).cuda()].view(torch.int16).cpu().numpy()
+    want = hid_d[torch.from_numpy(slots // w.k).cuda()].view(torch.int16).cpu().numpy()
+    assert np.array_equal(gy, want)
+    return out
+
+
+@pytest.mark.parametrize("name,layer", [("qwen3-235b", 0), ("qwen3-235b", 93),
+                                        ("deepseek-v3", 7), ("glm-4.5", 3)])
+def test_full_size_layer(name, layer):
+    out = _full_size_layer(name, layer, 0)
+    w = W.WORKLOADS[name]
+    assert out["rank_load"].max() <= out["counts"][0].reshape(w.R, -1).sum(1).max()
+
+
+def test_full_size_batched_count_and_reroute():
+    # all 94 layers of one Qwen3-235B-like microbatch in one launch per step
+    w = W.WORKLOADS["qwen3-235b"]
+    ids_d = torch.stack([W.topk_ids(w, l, 1, device="cuda") for l in range(w.layers)])
+    ids = ids_d.cpu().numpy()
+    out = G().gpu_run(U.Domain(w.R, w.E, w.S, w.k), ids, src_slot=False)
+    orc = G().oracle_run(w.R, w.E, w.S, ids)
+    G().compare(w.R, w.E, w.S, out, orc, check_rows=False)
+
+
+@pytest.mark.parametrize("R,S,tpr,s", [(8, 4, 8192, 1.6), (64, 4, 512, 0.6), (32, 2, 2048, 1.0)])
+def test_stress_points(R, S, tpr, s):
+    w = W.stress(R, S, tpr, s)
+    ids_d = torch.stack([W.topk_ids(w, l, 0, device="cuda") for l in range(2)])
+    ids = ids_d.cpu().numpy()
+    out = G().gpu_run(U.Domain(w.R, w.E, w.S, w.k), ids, src_slot=True)
+    G().compare(w.R, w.E, w.S, out, G().oracle_run(w.R, w.E, w.S, ids), check_rows=False)
