@@ -10,9 +10,9 @@
 // step instead of one per slot.  The block's histogram is the sum of its
 // warps' rows.  Chunks of one source rank meet in a last-block reduction that
 // writes counts_src[r]; source ranks of one instance meet in a second one that
-// writes counts.  The tickets that find the last block live in the caller's
-// workspace and are reset by that block, so the workspace is all-zero again
-// after every call.
+// writes counts.  The tickets that find the last block live at the start of
+// the caller's workspace and are reset by that block, so they are zero again
+// after every call; the rest of the workspace holds the chunk partials.
 #include "common.cuh"
 
 namespace ultraep {
