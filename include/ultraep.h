@@ -105,6 +105,33 @@ ep_status_t ep_count(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T,
                      void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * ep_count_noalloc -- ep_count for callers that cannot allocate device memory.
+ * The pages have no counterpart of this entry point.  It serves callers that
+ * cannot hand the library a workspace: for example a plugin running inside an
+ * inference engine whose device memory all belongs to the engine's pool, or a
+ * hot path that cannot afford the latency and implicit device synchronisation
+ * of cudaMalloc.  Arguments and results are those of ep_count without the
+ * workspace, which here is a fixed array of EP_COUNT_NOALLOC_SCRATCH_BYTES
+ * inside the library; every GPU that loads the library holds that array until
+ * the process exits.
+ *  - Returns EP_ERR_WORKSPACE, enqueueing nothing, when the shape needs more
+ *    than that (ep_count_workspace_bytes(dom, T, n_inst) is larger).
+ *  - The first call on a device, with that device current, looks up the
+ *    array's device address (cudaGetSymbolAddress); make that first call
+ *    before any stream capture.
+ *  - All calls on a device share the one array.  Each call clears the part
+ *    that must start at zero (the tickets) on `stream` and then launches, so
+ *    calls that overlap on the GPU (different streams or threads) race and
+ *    give wrong counts: keep them ordered, e.g. on one stream.
+ *  - Allocates nothing: it calls no cudaMalloc, cudaFree or allocating
+ *    library routine.
+ */
+#define EP_COUNT_NOALLOC_SCRATCH_BYTES (4u << 20)
+ep_status_t ep_count_noalloc(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T,
+                             int32_t n_inst, int32_t *counts, int32_t *counts_src,
+                             int32_t *dev_status, void *stream);
+
+/*
  * ep_plan -- the coupled replica-placement + quota solve (UltraEP article,
  * "key design", control-plane paragraph: solve how much load each expert
  * instance finally receives, each step either instantiating a replica or

@@ -39,6 +39,10 @@ size_t count_workspace_bytes(const ep_domain_t& d, int64_t T, int32_t n_inst);
 cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                          int32_t* counts, int32_t* counts_src, int32_t* dev_status, void* ws,
                          cudaStream_t s);
+size_t count_noalloc_scratch_capacity();
+cudaError_t launch_count_noalloc(const ep_domain_t& d, const int32_t* ids, int64_t T,
+                                 int32_t n_inst, int32_t* counts, int32_t* counts_src,
+                                 int32_t* dev_status, cudaStream_t s);
 
 // plan
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,

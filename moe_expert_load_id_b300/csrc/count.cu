@@ -13,6 +13,8 @@
 // writes counts.  The tickets that find the last block live at the start of
 // the caller's workspace and are reset by that block, so they are zero again
 // after every call; the rest of the workspace holds the chunk partials.
+#include <mutex>
+
 #include "common.cuh"
 
 namespace ultraep {
@@ -161,6 +163,68 @@ cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, in
                                                               counts_src, dev_status, inst_ticket,
                                                               rank_ticket, partial);
     return cudaGetLastError();
+}
+
+}  // namespace ultraep
+
+// ---------------------------------------------------------------------------
+// ep_count without a caller workspace.
+//
+// Some callers cannot hand the library any device memory beyond the inputs and
+// outputs: for example a plugin running inside an inference engine whose
+// device memory is all owned by the engine's pool, or a hot path where the
+// latency and implicit device synchronisation of cudaMalloc are not
+// acceptable.  For them the workspace of ep_count lives in the fixed array
+// below, which every GPU that loads this library keeps for the life of the
+// process.
+namespace ultraep {
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = (size_t)EP_COUNT_NOALLOC_SCRATCH_BYTES;
+
+// Host code sees only a stand-in for this array: the device address of each
+// GPU's copy comes from cudaGetSymbolAddress, taken once per device.
+static __device__ __align__(256) unsigned char g_count_scratch[kNoAllocScratchBytes];
+
+struct ScratchAddress {
+    std::mutex mu;
+    void* ptr[64] = {};
+};
+
+cudaError_t scratch_address(void** out) {
+    static ScratchAddress cache;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(cache.mu);
+    if (cache.ptr[dev] == nullptr) {
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_count_scratch);
+        if (err != cudaSuccess) return err;
+        cache.ptr[dev] = p;
+    }
+    *out = cache.ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace
+
+size_t count_noalloc_scratch_capacity() { return kNoAllocScratchBytes; }
+
+cudaError_t launch_count_noalloc(const ep_domain_t& d, const int32_t* ids, int64_t T,
+                                 int32_t n_inst, int32_t* counts, int32_t* counts_src,
+                                 int32_t* dev_status, cudaStream_t s) {
+    if (n_inst == 0) return cudaSuccess;
+    void* scratch = nullptr;
+    cudaError_t err = scratch_address(&scratch);
+    if (err != cudaSuccess) return err;
+    // The array keeps whatever the previous call left in it: the tickets that
+    // must start at zero are cleared on the caller's stream before the launch.
+    const size_t tickets = (size_t)n_inst * (d.R + 1) * sizeof(uint32_t);
+    err = cudaMemsetAsync(scratch, 0, tickets, s);
+    if (err != cudaSuccess) return err;
+    return launch_count(d, ids, T, n_inst, counts, counts_src, dev_status, scratch, s);
 }
 
 }  // namespace ultraep

@@ -82,6 +82,21 @@ ep_status_t ep_count(const ep_domain_t* dom, const int32_t* topk_ids, int64_t T,
                                   workspace, static_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_count_noalloc(const ep_domain_t* dom, const int32_t* topk_ids, int64_t T,
+                             int32_t n_inst, int32_t* counts, int32_t* counts_src,
+                             int32_t* dev_status, void* stream) {
+    if (!domain_ok(dom) || !slots_ok(T, dom->k) || n_inst < 0) return EP_ERR_INVAL;
+    const bool any = n_inst > 0;
+    if (!arr_ok(topk_ids, any && T > 0) || !arr_ok(counts, any) || !arr_ok(counts_src, any) ||
+        !arr_ok(dev_status, false))
+        return EP_ERR_INVAL;
+    if (!any) return EP_OK;
+    if (count_workspace_bytes(*dom, T, n_inst) > count_noalloc_scratch_capacity())
+        return EP_ERR_WORKSPACE;
+    return from_cuda(launch_count_noalloc(*dom, topk_ids, T, n_inst, counts, counts_src,
+                                          dev_status, static_cast<cudaStream_t>(stream)));
+}
+
 ep_status_t ep_plan(const ep_domain_t* dom, const int32_t* counts, int32_t n_inst,
                     int32_t max_iters, int32_t* quota, int32_t* slot_expert, int32_t* rank_load, int32_t* inst_ptr,
                     int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,

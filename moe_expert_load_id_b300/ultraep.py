@@ -22,6 +22,7 @@ _lib = ctypes.CDLL(_LIB_PATH)
 EP_OK, EP_ERR_INVAL, EP_ERR_ITER_LIMIT, EP_ERR_BAD_ID, EP_ERR_WORKSPACE, EP_ERR_CUDA = range(6)
 EP_DEV_BAD_ID, EP_DEV_QUOTA_OVERFLOW, EP_DEV_ROW_RANGE = 1, 2, 4
 EP_PLAN_MAX_ITERS = 1 << 16
+EP_COUNT_NOALLOC_SCRATCH_BYTES = 4 << 20
 
 EXPORTS = ("ep_count_workspace_bytes", "ep_count", "ep_plan", "ep_reroute", "ep_permute",
            "ep_unpermute", "ep_status_str")
@@ -65,6 +66,8 @@ _lib.ep_count_workspace_bytes.restype = _sz
 _lib.ep_count_workspace_bytes.argtypes = [_DP, _i64, _i32]
 _lib.ep_count.restype = ctypes.c_int
 _lib.ep_count.argtypes = [_DP, _vp, _i64, _i32, _vp, _vp, _vp, _vp, _sz, _vp]
+_lib.ep_count_noalloc.restype = ctypes.c_int
+_lib.ep_count_noalloc.argtypes = [_DP, _vp, _i64, _i32, _vp, _vp, _vp, _vp]
 _lib.ep_plan.restype = ctypes.c_int
 _lib.ep_plan.argtypes = [_DP, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.ep_reroute.restype = ctypes.c_int
@@ -113,6 +116,15 @@ def ep_count(dom, topk_ids, counts, counts_src, dev_status, workspace, stream=No
                                      _ptr(counts), _ptr(counts_src), _ptr(dev_status),
                                      _ptr(workspace), workspace.numel() * workspace.element_size(),
                                      _stream(stream)))
+
+
+def ep_count_noalloc(dom, topk_ids, counts, counts_src, dev_status, stream=None):
+    """ep_count with the library's own fixed scratch array instead of a workspace,
+    for callers that cannot allocate device memory (see include/ultraep.h)."""
+    n_inst, T = _shape_ids(topk_ids, dom.k)
+    _check("ep_count_noalloc", _lib.ep_count_noalloc(ctypes.byref(dom.c()), _ptr(topk_ids), T,
+                                                     n_inst, _ptr(counts), _ptr(counts_src),
+                                                     _ptr(dev_status), _stream(stream)))
 
 
 def ep_plan(dom, counts, quota, slot_expert, rank_load, inst_ptr, inst_id, inst_cum, n_iter,
