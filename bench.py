@@ -203,6 +203,71 @@ class LayerPipeline:
         return (self.rank_load, self.n_iter, self.inst_status, self.dev_status)
 
 
+def batched_report(U, w, ids, pipe, stream, device, peak, reps=5, warm=2):
+    """count, plan and reroute over ALL layers of the microbatch in one launch
+    each (n_inst = layers), L2 flushed before every launch.  This is the
+    bandwidth view of the two streaming kernels: one layer moves only 4-13 MB,
+    too little to fill HBM, while the whole microbatch moves about 400 MB."""
+    L = w.layers
+    b = U.Buffers(pipe.dom, w.T, L, device=device)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)   # 2x L2
+    names = ("count", "plan", "reroute")
+    acc = {n: [] for n in names}
+    for rep in range(warm + reps):
+        for n in names:
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            if n == "count":
+                b.count(ids, stream)
+            elif n == "plan":
+                b.plan(stream=stream)
+            else:
+                b.reroute(ids, stream)
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            if rep >= warm:
+                acc[n].append(e0.elapsed_time(e1) * 1000.0)
+    # the batched launches must agree with the per-layer launches of the step
+    if not (torch.equal(b.counts, pipe.counts) and torch.equal(b.quota, pipe.quota)
+            and int(b.dev_status.item()) == 0):
+        raise RuntimeError("batched count/plan disagree with the per-layer launches")
+    us = {n: float(np.mean(v)) for n, v in acc.items()}
+    count_bytes = L * (4 * w.N + 4 * w.E * (w.R + 1))
+    reroute_bytes = L * 8 * w.N
+    gbs = lambda by, t: by / (t * 1e-6) / 1e9
+    return {"launch": f"one launch per step over all {w.layers} layers (n_inst={L}), "
+                      "L2 flushed before each launch",
+            "count": {"us": round(us["count"], 2), "bytes": count_bytes,
+                      "gbs": round(gbs(count_bytes, us["count"]), 1),
+                      "frac": round(gbs(count_bytes, us["count"]) / peak, 4)},
+            "plan": {"us": round(us["plan"], 2), "instances": L,
+                     "us_per_instance": round(us["plan"] / L, 3)},
+            "reroute": {"us": round(us["reroute"], 2), "bytes": reroute_bytes,
+                        "gbs": round(gbs(reroute_bytes, us["reroute"]), 1),
+                        "frac": round(gbs(reroute_bytes, us["reroute"]) / peak, 4)}}
+
+
+def unpermute_report(U, w, pipe, stream, device, peak, reps=5):
+    """ep_unpermute of the last layer's grouped rows back to (token, k) order,
+    timed on its own (it is not part of the metric's step)."""
+    y = torch.empty((1, w.T, w.k, w.Hd), dtype=torch.bfloat16, device=device)
+    U.ep_unpermute(pipe.grouped, w.T, w.k, pipe.dst_row, y, pipe.dev_status, stream)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        U.ep_unpermute(pipe.grouped, w.T, w.k, pipe.dst_row, y, pipe.dev_status, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1000.0 / reps
+    by = w.N * (4 * w.Hd + 4)          # read a grouped row + write a y row + dst_row
+    del y
+    return {"us_per_launch": round(us, 2), "bytes": by,
+            "gbs": round(by / (us * 1e-6) / 1e9, 1),
+            "frac": round(by / (us * 1e-6) / 1e9 / peak, 4)}
+
+
 def make_inputs(w, microbatch, device):
     ids = torch.stack([W.topk_ids(w, l, microbatch, device=device) for l in range(w.layers)])
     hiddens = [W.hidden(w.T, w.Hd, w.seed(1000 + b, microbatch), device=device)
@@ -299,7 +364,7 @@ def run_ultraep(args, rank, world, local):
     peak, peak_kind = measured_peaks()
     perm_bytes = w.T * (2 * w.Hd + 4 * w.k + 2 * w.Hd * w.k)   # read row + k dst + k rows
     count_bytes = 4 * w.N + 4 * w.E * (w.R + 1)
-    reroute_bytes = 12 * w.N
+    reroute_bytes = 8 * w.N      # ids read + dst_row written (no src_slot in the step)
     gbs = lambda b, us: b / (us * 1e-6) / 1e9
     roofline = {"kernel": "ep_permute", "bound": "hbm",
                 "achieved": round(gbs(perm_bytes, avg["permute"]), 1), "peak": peak,
@@ -348,6 +413,12 @@ def run_ultraep(args, rank, world, local):
                "steps": args.e2e_steps}
 
     quality = quality_report(U, w, ids, pipe, microbatch, device) if rank == 0 else None
+    batched = batched_report(U, w, ids, pipe, stream, device, peak) if args.extras else None
+    unperm = unpermute_report(U, w, pipe, stream, device, peak) if args.extras else None
+    if unperm is not None:
+        kernels["unpermute"] = unperm
+    # indicative only: a real rank runs 1/R of count, reroute and permute on its own GPU
+    per_rank = (avg["count"] + avg["reroute"] + avg["permute"]) / w.R + avg["plan"]
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_baseline:
@@ -366,7 +437,9 @@ def run_ultraep(args, rank, world, local):
                        "l2": "inputs larger than L2 (1.07 GB hidden per layer, 8.6 GB "
                              "permute output per layer)",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roofline, "kernels": kernels, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "kernels": kernels, "batched": batched,
+            "per_rank_equivalent_us": round(per_rank, 2),
+            "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 4 * L * args.steps, "clocks": clock_rep, "quality": quality,
             "pages_context": {"critical_path_overhead_us": "< 300 (per rank, hardware not "
                                                            "disclosed)",
@@ -441,6 +514,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-extras", dest="extras", action="store_false",
+                    help="skip the batched count/plan/reroute and unpermute timings")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

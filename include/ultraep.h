@@ -92,13 +92,12 @@ size_t ep_count_workspace_bytes(const ep_domain_t *dom, int64_t T, int32_t n_ins
  *   dev_status int32                  out: |= EP_DEV_BAD_ID if an id was
  *                                     outside [0, E) (it is skipped)
  *   workspace  ep_count_workspace_bytes() bytes, caller-owned, 16-byte
- *              aligned.  Its first 4*n_inst*(R+1) bytes are tickets that find
- *              the last block of each source rank and instance: they must be
- *              zero before the first call, and every call resets them to zero
- *              on completion, so the workspace can be reused by later calls on
- *              the same stream without clearing.  The rest is scratch for
- *              per-chunk partial histograms.  Calls that share a workspace must
- *              not overlap on the GPU.
+ *              aligned.  It holds one ticket per instance (its first 4*n_inst
+ *              bytes), which finds the last block of the instance: the tickets
+ *              must be zero before the first call, and every call resets them
+ *              to zero on completion, so the workspace can be reused by later
+ *              calls on the same stream without clearing.  Calls that share a
+ *              workspace must not overlap on the GPU.
  */
 ep_status_t ep_count(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T, int32_t n_inst,
                      int32_t *counts, int32_t *counts_src, int32_t *dev_status,
@@ -126,7 +125,7 @@ ep_status_t ep_count(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T,
  *  - Allocates nothing: it calls no cudaMalloc, cudaFree or allocating
  *    library routine.
  */
-#define EP_COUNT_NOALLOC_SCRATCH_BYTES (4u << 20)
+#define EP_COUNT_NOALLOC_SCRATCH_BYTES (64u << 10) /* tickets of up to 16384 instances per call */
 ep_status_t ep_count_noalloc(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T,
                              int32_t n_inst, int32_t *counts, int32_t *counts_src,
                              int32_t *dev_status, void *stream);

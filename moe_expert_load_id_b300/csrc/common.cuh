@@ -36,6 +36,7 @@ DeviceInfo device_info();
 // count
 int count_chunks_per_rank(const ep_domain_t& d, int64_t T, int32_t n_inst);
 size_t count_workspace_bytes(const ep_domain_t& d, int64_t T, int32_t n_inst);
+size_t count_ticket_bytes(int32_t n_inst);
 cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                          int32_t* counts, int32_t* counts_src, int32_t* dev_status, void* ws,
                          cudaStream_t s);

@@ -3,48 +3,76 @@
 // UltraEP article (m.youleyou.com), "key design" section, forward-pass
 // paragraph: the global load is obtained after gating and before planning.
 //
-// One block per (instance, source rank, chunk).  Each warp keeps a private
-// shared-memory histogram; the lanes of a warp that hold the same expert id
-// are grouped with match.any and the group's lowest lane adds the group size
-// (warp-aggregated update), so a hot expert costs one shared atomic per warp
-// step instead of one per slot.  The block's histogram is the sum of its
-// warps' rows.  Chunks of one source rank meet in a last-block reduction that
-// writes counts_src[r]; source ranks of one instance meet in a second one that
-// writes counts.  The tickets that find the last block live at the start of
-// the caller's workspace and are reset by that block, so they are zero again
-// after every call; the rest of the workspace holds the chunk partials.
+// One block per (instance, source rank, chunk).  The block's histogram is a
+// lane-column table hist[e][C] in shared memory: lane l adds its id e into
+// column l % C, so the 32 updates of one warp instruction never hit the same
+// address when C = 32 (and fall in 32 different banks), whatever the id
+// distribution.  A hot expert therefore costs nothing extra; match.any-based
+// aggregation, whose cost grows with the number of distinct ids in the warp,
+// is not used.  ids are read with 16-byte streaming loads (scalar head and
+// tail).
+//
+// The chunks of one source rank form a thread-block cluster: after a cluster
+// barrier the cluster's first block sums the others' block totals through
+// distributed shared memory and writes counts_src[r].  Source ranks of one
+// instance meet in a last-block reduction (atomic ticket) that writes counts;
+// its ticket lives in the caller's workspace and is reset by that block, so
+// it is zero again after every call.
 #include <mutex>
+
+#include <cooperative_groups.h>
 
 #include "common.cuh"
 
 namespace ultraep {
 namespace {
 
+namespace cg = cooperative_groups;
+
 constexpr int kCountThreads = 512;
 constexpr int kCountWarps = kCountThreads / 32;
-constexpr int kCountUnroll = 4;
-constexpr int kTargetBlocks = 2 * 148;
-constexpr int kMinSlotsPerChunk = 2048;
-constexpr int kMaxChunksPerRank = 64;
+constexpr int kVec = 4;                         // 16-byte loads in flight per thread
+constexpr int kTargetBlocks = 2 * 148;          // two blocks per B300 SM
+constexpr int kMinChunk = kCountThreads * 4;    // at least one 16-byte load per thread
+constexpr int kMaxChunksPerRank = 8;            // portable cluster size
 
-__global__ void __launch_bounds__(kCountThreads)
+// columns of the lane-column histogram: 32 when E*32 ints fit 32 KB
+__host__ __device__ inline int count_cols(int E) {
+    int C = 32;
+    while (C > 1 && E * C > 8192) C >>= 1;
+    return C;
+}
+
+__host__ __device__ inline size_t count_smem_bytes(int E) {
+    const int C = count_cols(E);
+    const int h = E * C > kCountThreads ? E * C : kCountThreads;
+    return sizeof(int32_t) * ((size_t)h + E);
+}
+
+__device__ __forceinline__ void count_one(int v, int E, int32_t* hist, int C, int col, int& bad) {
+    if ((unsigned)v < (unsigned)E) atomicAdd(&hist[v * C + col], 1);
+    else bad = 1;
+}
+
+__global__ void __launch_bounds__(kCountThreads, 3)
 count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int cps,
              int32_t* __restrict__ counts, int32_t* __restrict__ counts_src,
-             int32_t* dev_status, uint32_t* inst_ticket, uint32_t* rank_ticket,
-             int32_t* partial) {
-    extern __shared__ int32_t hist[];  // [kCountWarps][E]
+             int32_t* dev_status, uint32_t* inst_ticket) {
+    extern __shared__ __align__(16) int32_t sh[];
     __shared__ int bad;
     __shared__ int is_last;
+    const int C = count_cols(E);
+    int32_t* hist = sh;                                            // [E][C], later scratch
+    int32_t* blk = sh + (E * C > kCountThreads ? E * C : kCountThreads);  // [E] block total
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t blk = blockIdx.x;
-    const int per_inst = R * cps;
-    const int inst = (int)(blk / per_inst);
-    const int rc = (int)(blk % per_inst);
-    const int r = rc / cps, c = rc % cps;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t b = blockIdx.x;
+    const int inst = (int)(b / ((int64_t)R * cps));
+    const int rc = (int)(b % ((int64_t)R * cps));
+    const int r = rc / cps, c = rc % cps;  // c is also the block's rank in its cluster
 
-    for (int x = threadIdx.x; x < kCountWarps * E; x += kCountThreads) hist[x] = 0;
-    if (threadIdx.x == 0) bad = 0;
+    for (int x = tid; x < E * C; x += kCountThreads) hist[x] = 0;
+    if (tid == 0) bad = 0;
     __syncthreads();
 
     // this block's slots: chunk c of source rank r
@@ -52,82 +80,135 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     const int64_t t0 = min(T, (int64_t)r * Tr), t1 = min(T, (int64_t)(r + 1) * Tr);
     const int64_t a = t0 * k, len = (t1 - t0) * k;
     const int64_t s0 = a + len * c / cps, s1 = a + len * (c + 1) / cps;
-    const int32_t* src = ids + (int64_t)inst * T * k;
-    int32_t* row = hist + warp * E;
-
+    const int32_t* p0 = ids + (int64_t)inst * T * k + s0;
+    const int64_t n = s1 - s0;
+    // split into a scalar head up to the first 16-byte boundary, an int4 body
+    // and a scalar tail
+    const int64_t head = min(n, (int64_t)(((16u - ((uintptr_t)p0 & 15u)) & 15u) >> 2));
+    const int64_t n4 = (n - head) >> 2;
+    const int64_t tail0 = head + 4 * n4;
+    const int4* body = reinterpret_cast<const int4*>(p0 + head);
+    const int col = lane & (C - 1);
     int local_bad = 0;
-    for (int64_t i0 = s0 + (int64_t)warp * 32 * kCountUnroll; i0 < s1;
-         i0 += (int64_t)kCountThreads * kCountUnroll) {
-        int ev[kCountUnroll];
+    if (tid < head) count_one(__ldcs(p0 + tid), E, hist, C, col, local_bad);
+    if (tid < n - tail0) count_one(__ldcs(p0 + tail0 + tid), E, hist, C, col, local_bad);
+    // trip count is warp-uniform (v0 has no lane term)
+    for (int64_t v0 = (int64_t)warp * 32 * kVec; v0 < n4; v0 += (int64_t)kCountThreads * kVec) {
+        int4 w[kVec];
 #pragma unroll
-        for (int u = 0; u < kCountUnroll; ++u) {
-            const int64_t i = i0 + u * 32 + lane;
-            ev[u] = (i < s1) ? __ldg(src + i) : -1;
+        for (int u = 0; u < kVec; ++u) {
+            const int64_t vi = v0 + u * 32 + lane;
+            w[u] = (vi < n4) ? __ldcs(body + vi) : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kCountUnroll; ++u) {
-            const int64_t i = i0 + u * 32 + lane;
-            const bool in = i < s1;
-            const bool valid = in && ev[u] >= 0 && ev[u] < E;
-            local_bad |= (in && !valid);
-            const unsigned grp = __match_any_sync(kFull, valid ? ev[u] : -1);
-            if (valid && lane == __ffs(grp) - 1) atomicAdd(&row[ev[u]], __popc(grp));
+        for (int u = 0; u < kVec; ++u) {
+            if (v0 + u * 32 + lane < n4) {
+                count_one(w[u].x, E, hist, C, col, local_bad);
+                count_one(w[u].y, E, hist, C, col, local_bad);
+                count_one(w[u].z, E, hist, C, col, local_bad);
+                count_one(w[u].w, E, hist, C, col, local_bad);
+            }
         }
     }
     if (local_bad) bad = 1;
     __syncthreads();
 
+    // block total: one warp per expert row, one redux over its C columns
+    for (int e = warp; e < E; e += kCountWarps) {
+        const int v = (lane < C) ? hist[e * C + lane] : 0;
+        const int t = __reduce_add_sync(kFull, v);
+        if (lane == 0) blk[e] = t;
+    }
+    if (tid == 0 && bad) raise_flag(dev_status, EP_DEV_BAD_ID);
+
     const int64_t rank_row = ((int64_t)inst * R + r) * E;
-    int32_t* out = (cps == 1) ? counts_src + rank_row : partial + (rank_row * cps + (int64_t)c * E);
-    for (int e = threadIdx.x; e < E; e += kCountThreads) {
-        int s = 0;
-        for (int w = 0; w < kCountWarps; ++w) s += hist[w * E + e];
-        out[e] = s;
-    }
-    if (threadIdx.x == 0 && bad) raise_flag(dev_status, EP_DEV_BAD_ID);
-
     if (cps > 1) {
-        // the last chunk of source rank r folds the chunk partials into counts_src[r]
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0)
-            is_last = (atomicAdd(&rank_ticket[(int64_t)inst * R + r], 1u) == (unsigned)(cps - 1));
-        __syncthreads();
-        if (!is_last) return;
-        __threadfence();
-        for (int e = threadIdx.x; e < E; e += kCountThreads) {
-            int s = 0;
-            for (int cc = 0; cc < cps; ++cc) s += __ldcg(partial + rank_row * cps + (int64_t)cc * E + e);
-            counts_src[rank_row + e] = s;
+        // the cluster (the cps chunks of rank r) sums its block totals in
+        // distributed shared memory; the second barrier keeps every block's
+        // shared memory alive until the first block has read it
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (c == 0) {
+            for (int e = tid; e < E; e += kCountThreads) {
+                int t = 0;
+                for (int cc = 0; cc < cps; ++cc) t += cluster.map_shared_rank(blk, cc)[e];
+                counts_src[rank_row + e] = t;
+            }
         }
-        if (threadIdx.x == 0) rank_ticket[(int64_t)inst * R + r] = 0u;
+        cluster.sync();
+        if (c != 0) return;
+    } else {
+        __syncthreads();
+        for (int e = tid; e < E; e += kCountThreads) counts_src[rank_row + e] = blk[e];
     }
 
-    // the last source rank of the instance folds counts_src into counts
-    __threadfence();
+    // the last source rank of the instance folds counts_src into counts.  The
+    // barrier orders the block's counts_src writes before thread 0's fence and
+    // ticket (fences are cumulative), so one thread fences for the block; the
+    // last block's thread 0 fences again before the block reads.
     __syncthreads();
-    if (threadIdx.x == 0) is_last = (atomicAdd(&inst_ticket[inst], 1u) == (unsigned)(R - 1));
+    if (tid == 0) {
+        __threadfence();
+        is_last = (atomicAdd(&inst_ticket[inst], 1u) == (unsigned)(R - 1));
+        if (is_last) __threadfence();
+    }
     __syncthreads();
     if (!is_last) return;
-    __threadfence();
-    for (int e = threadIdx.x; e < E; e += kCountThreads) {
-        int s = 0;
-        for (int rr = 0; rr < R; ++rr) s += __ldcg(counts_src + ((int64_t)inst * R + rr) * E + e);
-        counts[(int64_t)inst * E + e] = s;
+    const int32_t* cs = counts_src + (int64_t)inst * R * E;
+    if (E <= kCountThreads) {
+        // thread (g, e) sums rows g, g+G, ... of column e, G = threads / E;
+        // loads are issued eight at a time
+        const int G = kCountThreads / E;
+        const int e = tid % E, g = tid / E;
+        int t = 0;
+        if (g < G) {
+            for (int r0 = g; r0 < R; r0 += 8 * G) {
+                int v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int rr = r0 + u * G;
+                    v[u] = (rr < R) ? __ldcg(cs + (int64_t)rr * E + e) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t += v[u];
+            }
+            hist[g * E + e] = t;
+        }
+        __syncthreads();
+        if (tid < E) {
+            int sum = 0;
+            for (int gg = 0; gg < G; ++gg) sum += hist[gg * E + tid];
+            counts[(int64_t)inst * E + tid] = sum;
+        }
+    } else {
+        for (int e = tid; e < E; e += kCountThreads) {
+            int t = 0;
+            for (int r0 = 0; r0 < R; r0 += 8) {
+                int v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    v[u] = (r0 + u < R) ? __ldcg(cs + (int64_t)(r0 + u) * E + e) : 0;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t += v[u];
+            }
+            counts[(int64_t)inst * E + e] = t;
+        }
     }
-    if (threadIdx.x == 0) inst_ticket[inst] = 0u;
+    if (tid == 0) inst_ticket[inst] = 0u;
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace
 
+// Chunks per source rank: enough blocks for two per SM, chunks of at least
+// kMinChunk slots, and at most a portable cluster.
 int count_chunks_per_rank(const ep_domain_t& d, int64_t T, int32_t n_inst) {
     const int64_t blocks = (int64_t)n_inst * d.R;
     if (blocks <= 0) return 1;
     int64_t cps = (kTargetBlocks + blocks - 1) / blocks;
     const int64_t slots_per_rank = tokens_per_rank(T, d.R) * d.k;
-    int64_t cap = slots_per_rank / kMinSlotsPerChunk;
+    int64_t cap = slots_per_rank / kMinChunk;
     if (cap < 1) cap = 1;
     if (cap > kMaxChunksPerRank) cap = kMaxChunksPerRank;
     if (cps > cap) cps = cap;
@@ -135,14 +216,14 @@ int count_chunks_per_rank(const ep_domain_t& d, int64_t T, int32_t n_inst) {
     return (int)cps;
 }
 
-// Workspace: [n_inst] instance tickets | [n_inst][R] rank tickets | partials
-// [n_inst][R][cps][E] (only when cps > 1).  Tickets must start at zero.
+// Workspace: [n_inst] instance tickets, which must start at zero.
 size_t count_workspace_bytes(const ep_domain_t& d, int64_t T, int32_t n_inst) {
-    const int cps = count_chunks_per_rank(d, T, n_inst);
-    size_t ints = (size_t)n_inst + (size_t)n_inst * d.R;
-    if (cps > 1) ints += (size_t)n_inst * d.R * cps * d.E;
-    return align_up(ints * sizeof(int32_t), 256);
+    (void)d;
+    (void)T;
+    return align_up((size_t)n_inst * sizeof(uint32_t), 256);
 }
+
+size_t count_ticket_bytes(int32_t n_inst) { return (size_t)n_inst * sizeof(uint32_t); }
 
 cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                          int32_t* counts, int32_t* counts_src, int32_t* dev_status, void* ws,
@@ -150,19 +231,21 @@ cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, in
     if (n_inst == 0) return cudaSuccess;
     const int cps = count_chunks_per_rank(d, T, n_inst);
     uint32_t* inst_ticket = static_cast<uint32_t*>(ws);
-    uint32_t* rank_ticket = inst_ticket + n_inst;
-    int32_t* partial = reinterpret_cast<int32_t*>(rank_ticket + (size_t)n_inst * d.R);
-    const size_t smem = (size_t)kCountWarps * d.E * sizeof(int32_t);
-    if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
-        if (err != cudaSuccess) return err;
-    }
-    const int64_t blocks = (int64_t)n_inst * d.R * cps;
-    count_kernel<<<(unsigned)blocks, kCountThreads, smem, s>>>(ids, T, d.k, d.R, d.E, cps, counts,
-                                                              counts_src, dev_status, inst_ticket,
-                                                              rank_ticket, partial);
-    return cudaGetLastError();
+    const size_t smem = count_smem_bytes(d.E);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)n_inst * d.R * cps));
+    cfg.blockDim = dim3(kCountThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cps;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = cps > 1 ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, count_kernel, ids, T, (int)d.k, (int)d.R, (int)d.E, cps,
+                              counts, counts_src, dev_status, inst_ticket);
 }
 
 }  // namespace ultraep
@@ -221,7 +304,7 @@ cudaError_t launch_count_noalloc(const ep_domain_t& d, const int32_t* ids, int64
     if (err != cudaSuccess) return err;
     // The array keeps whatever the previous call left in it: the tickets that
     // must start at zero are cleared on the caller's stream before the launch.
-    const size_t tickets = (size_t)n_inst * (d.R + 1) * sizeof(uint32_t);
+    const size_t tickets = count_ticket_bytes(n_inst);
     err = cudaMemsetAsync(scratch, 0, tickets, s);
     if (err != cudaSuccess) return err;
     return launch_count(d, ids, T, n_inst, counts, counts_src, dev_status, scratch, s);

@@ -10,15 +10,22 @@
 // documented in ultraep.h (hot = argmax load, its largest instance, cold =
 // least-loaded eligible rank, q = min(quota, floor(gap/2)), global stop).
 //
-// One warp per (layer, microbatch) instance, all state on chip:
-//   - rank loads in registers, lane l holds ranks l and l+32;
-//   - quota[P], slot_expert[R*S] and a 64-bit holder mask per expert in the
-//     warp's slice of shared memory;
-//   - argmax / argmin over ranks: one redux.sync (__reduce_max/min_sync) on the
-//     load, then a ballot for the lowest rank that attains it (no key packing,
-//     so loads up to 2^31-1 are exact);
-//   - eligibility is a 64-bit mask: (holders of e | ranks with a free slot)
-//     minus the hot rank.
+// One warp per (layer, microbatch) instance.  The moves form one serial
+// chain, so the design goal is the shortest dependent path per move:
+//   - lane l owns ranks l and l+32 and keeps, in registers, each rank's load,
+//     its instances (quota and expert, unrolled over a compile-time bound WB on
+//     H+S) and its largest instance;
+//   - hot and cold are each ONE redux.sync over a packed key
+//     (load << 6 | rank index, the index flipped for the max so that the lowest
+//     rank wins ties); instances whose loads could overflow the packing
+//     (total >= 2^25) take a two-collective path (redux on the load, then a
+//     ballot for the lowest rank that attains it);
+//   - "rank c holds e" is a register compare in c's owner lane, so a move
+//     touches no shared memory at all;
+//   - every lane runs the same branch-free update on its own registers (a
+//     no-op unless it owns hot or cold), so the warp never diverges.
+// Shared memory is used only after the loop, to build the logical->physical
+// CSR table.
 #include <climits>
 
 #include "common.cuh"
@@ -27,6 +34,7 @@ namespace ultraep {
 namespace {
 
 constexpr int kPlanWarps = 4;
+constexpr long long kPackLimit = 1ll << 25;  // total below this: loads fit a 6-bit-shifted key
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
@@ -35,7 +43,195 @@ __host__ __device__ inline size_t plan_warp_bytes(int R, int E, int S) {
     return align16((size_t)P * 4) + align16((size_t)R * S * 4) + (size_t)E * 8;
 }
 
-__global__ void __launch_bounds__(kPlanWarps * 32)
+// Registers of one rank: quota and expert of local instance j (j < H: home of
+// expert r*H + j; H <= j < W: spare slot j-H, expert -1 while empty).
+template <int WB>
+struct RankRegs {
+    int q[WB];
+    int x[WB];
+    int load;   // -1: the rank does not exist
+    int used;   // filled spare slots
+    int bq;     // largest quota among its instances
+    int bx;     // that instance: expert << 5 | j (lowest expert on ties)
+
+    __device__ __forceinline__ void best(int W) {
+        bq = -1;
+        bx = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < WB; ++j) {
+            const int cx = (x[j] << 5) | j;
+            const bool take = j < W && x[j] >= 0 && (q[j] > bq || (q[j] == bq && cx < bx));
+            bq = take ? q[j] : bq;
+            bx = take ? cx : bx;
+        }
+    }
+    __device__ __forceinline__ bool holds(int e) const {
+        bool h = false;
+#pragma unroll
+        for (int j = 0; j < WB; ++j) h |= (x[j] == e);
+        return h;
+    }
+    // (the rank's load is updated by the move loop itself, ahead of these)
+    // hot side: the owner lane (mine) removes mv from its instance j
+    __device__ __forceinline__ void take(int j, bool mine, int mv) {
+#pragma unroll
+        for (int jj = 0; jj < WB; ++jj) q[jj] -= (mine && jj == j) ? mv : 0;
+    }
+    // cold side: the owner lane adds mv to its instance of e, filling the
+    // lowest free spare slot (local index H + used) when it does not hold e
+    // yet.  Only one instance grew, so the largest instance is updated in
+    // place.
+    __device__ __forceinline__ void give(int e, bool held, bool mine, int H, int mv) {
+        const int jn = held ? -1 : H + used;
+        int nq = 0, nj = 0;
+#pragma unroll
+        for (int jj = 0; jj < WB; ++jj) {
+            const bool to = mine && (held ? (x[jj] == e) : (jj == jn));
+            x[jj] = to ? e : x[jj];
+            q[jj] += to ? mv : 0;
+            nq = to ? q[jj] : nq;
+            nj = to ? jj : nj;
+        }
+        used += (mine && !held) ? 1 : 0;
+        const int cx = (e << 5) | nj;
+        const bool better = mine && (nq > bq || (nq == bq && cx < bx));
+        bq = better ? nq : bq;
+        bx = better ? cx : bx;
+    }
+};
+
+// Hottest rank (lowest index on ties) and its load.
+template <bool kTwo, bool kPacked>
+__device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB, int lane,
+                                            int& hot, int& Lmax) {
+    if (kPacked) {
+        const unsigned ka = hasA ? ((unsigned)la << 6) | (unsigned)(63 - lane) : 0u;
+        const unsigned kb = hasB ? ((unsigned)lb << 6) | (unsigned)(31 - lane) : 0u;
+        const unsigned k = __reduce_max_sync(kFull, kTwo ? max(ka, kb) : ka);
+        hot = 63 - (int)(k & 63u);
+        Lmax = (int)(k >> 6);
+    } else {
+        Lmax = __reduce_max_sync(kFull, kTwo ? max(la, lb) : la);
+        const unsigned b0 = __ballot_sync(kFull, la == Lmax);
+        const unsigned b1 = kTwo ? __ballot_sync(kFull, lb == Lmax) : 0u;
+        hot = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+    }
+}
+
+// One warp's move loop.  kPacked: hot and cold by one redux on a packed key.
+// kTwo: R > 32, every lane owns a second rank (B).  Which half holds hot or
+// cold is warp-uniform, so only that half's instance registers are updated.
+// The loop is software-pipelined: as soon as the amount is known the two
+// loads change and the next move's argmax is issued; the instance bookkeeping
+// of the current move (take, give, largest instance) overlaps it.
+template <int WB, bool kTwo, bool kPacked>
+__device__ __forceinline__ void plan_moves(RankRegs<WB>& A, RankRegs<WB>& B, int lane, int H,
+                                           int S, int W, int max_iters, int& iters,
+                                           int& status) {
+    const bool hasA = A.load >= 0, hasB = kTwo && B.load >= 0;
+    const int ra = lane, rb = lane + 32;
+    int hot, Lmax;
+    argmax_rank<kTwo, kPacked>(A.load, B.load, hasA, hasB, lane, hot, Lmax);
+    while (true) {
+        const bool hotB = kTwo && hot >= 32;
+        const int hl = hot & 31;
+
+        // 2. hot's largest-quota instance (lowest expert id on ties)
+        const int qmax = __shfl_sync(kFull, hotB ? B.bq : A.bq, hl);
+        const int bx = __shfl_sync(kFull, hotB ? B.bx : A.bx, hl);
+        const int e = bx >> 5, src_j = bx & 31;
+
+        // 3. eligible: other ranks that hold e or have a free spare slot
+        const bool holdA = A.holds(e);
+        const bool holdB = kTwo && B.holds(e);
+        const bool elA = hasA && ra != hot && (holdA || A.used < S);
+        const bool elB = hasB && rb != hot && (holdB || B.used < S);
+
+        // 4. coldest eligible rank, lowest index on ties
+        int cold, Lmin;
+        if (kPacked) {
+            const unsigned ca = elA ? ((unsigned)A.load << 6) | (unsigned)ra : 0xffffffffu;
+            const unsigned cb = elB ? ((unsigned)B.load << 6) | (unsigned)rb : 0xffffffffu;
+            const unsigned k = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            if (k == 0xffffffffu) break;  // slots ran out
+            cold = (int)(k & 63u);
+            Lmin = (int)(k >> 6);
+        } else {
+            if (!__any_sync(kFull, elA || elB)) break;  // slots ran out
+            const int ca = elA ? A.load : INT_MAX;
+            const int cb = elB ? B.load : INT_MAX;
+            Lmin = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            const unsigned b0 = __ballot_sync(kFull, elA && ca == Lmin);
+            const unsigned b1 = kTwo ? __ballot_sync(kFull, elB && cb == Lmin) : 0u;
+            cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+        }
+        const bool coldB = kTwo && cold >= 32;
+        const int cl = cold & 31;
+
+        // 5. amount, 6. safety cap
+        const int mv = min(qmax, (Lmax - Lmin) >> 1);
+        if (mv <= 0) break;
+        if (iters == max_iters) {
+            status = EP_ERR_ITER_LIMIT;
+            break;
+        }
+
+        // 7. move.  Loads first, then the next move's argmax ...
+        A.load += (ra == cold ? mv : 0) - (ra == hot ? mv : 0);
+        if (kTwo) B.load += (rb == cold ? mv : 0) - (rb == hot ? mv : 0);
+        int nhot, nLmax;
+        argmax_rank<kTwo, kPacked>(A.load, B.load, hasA, hasB, lane, nhot, nLmax);
+        // ... while hot's owner lane takes, cold's owner lane gives, and hot's
+        // half refreshes its largest instance (only the half holding each of
+        // them is touched)
+        if (hotB) B.take(src_j, lane == hl, mv); else A.take(src_j, lane == hl, mv);
+        if (coldB) B.give(e, holdB, lane == cl, H, mv); else A.give(e, holdA, lane == cl, H, mv);
+        if (hotB) B.best(W); else A.best(W);
+        hot = nhot;
+        Lmax = nLmax;
+        ++iters;
+    }
+}
+
+template <int WB>
+__device__ __forceinline__ void init_rank(RankRegs<WB>& X, int rk, int R, int H, int W,
+                                          const int32_t* cnt) {
+    const bool has = rk < R;
+    unsigned sum = 0;
+#pragma unroll
+    for (int j = 0; j < WB; ++j) {
+        const bool home = has && j < H;
+        X.q[j] = home ? cnt[rk * H + j] : 0;
+        X.x[j] = home ? rk * H + j : -1;
+        sum += (unsigned)X.q[j];
+    }
+    X.load = has ? (int)sum : -1;
+    X.used = 0;
+    X.best(W);
+}
+
+template <int WB>
+__device__ __forceinline__ void store_rank(const RankRegs<WB>& X, int rk, int R, int H, int S,
+                                           int W, int32_t* q, int32_t* slot, uint64_t* holder,
+                                           int32_t* qo, int32_t* so, int32_t* lo) {
+    if (rk >= R) return;
+#pragma unroll
+    for (int j = 0; j < WB; ++j) {
+        if (j < W) {
+            q[rk * W + j] = X.q[j];
+            qo[rk * W + j] = X.q[j];
+        }
+        if (j >= H && j < W) {
+            slot[rk * S + (j - H)] = X.x[j];
+            so[rk * S + (j - H)] = X.x[j];
+            if (X.x[j] >= 0) atomicOr((unsigned long long*)&holder[X.x[j]], 1ull << rk);
+        }
+    }
+    lo[rk] = X.load;
+}
+
+template <int WB, bool kTwo>
+__global__ void __launch_bounds__(kPlanWarps * 32, 1)
 plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S, int max_iters,
             int32_t* __restrict__ quota_out, int32_t* __restrict__ slot_out,
             int32_t* __restrict__ load_out, int32_t* __restrict__ ptr_out,
@@ -47,45 +243,14 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     if (g >= n_inst) return;  // whole warp; no block-wide barrier follows
 
     const int H = E / R, W = H + S, P = R * W;
-    unsigned char* base = smem + (size_t)warp * plan_warp_bytes(R, E, S);
-    int32_t* q = reinterpret_cast<int32_t*>(base);
-    int32_t* slot = reinterpret_cast<int32_t*>(base + align16((size_t)P * 4));
-    uint64_t* holder = reinterpret_cast<uint64_t*>(base + align16((size_t)P * 4) +
-                                                   align16((size_t)R * S * 4));
     const int32_t* cnt = counts + (int64_t)g * E;
-
-    for (int p = lane; p < P; p += 32) q[p] = 0;
-    for (int x = lane; x < R * S; x += 32) slot[x] = -1;
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) {
-        const int r = e / H;
-        q[r * W + (e - r * H)] = cnt[e];
-        holder[e] = 1ull << r;
-    }
-    __syncwarp();
-
-    // loads of ranks lane and lane+32; -1 marks a rank that does not exist
-    int L0 = -1, L1 = -1;
-    if (lane < R) {
-        int s = 0;
-        for (int j = 0; j < H; ++j) s += q[lane * W + j];
-        L0 = s;
-    }
-    if (lane + 32 < R) {
-        int s = 0;
-        for (int j = 0; j < H; ++j) s += q[(lane + 32) * W + j];
-        L1 = s;
-    }
-    int used0 = 0, used1 = 0;  // filled spare slots of ranks lane, lane+32
-    const uint64_t ranks = (R == 64) ? ~0ull : ((1ull << R) - 1);
-    uint64_t free_mask = (S > 0) ? ranks : 0ull;  // ranks with a free spare slot
-    int iters = 0, status = EP_OK;
 
     // counts must be >= 0 with a total below 2^31; otherwise the instance is
     // rejected (EP_ERR_INVAL) and its outputs describe the home-only placement
+    int status = EP_OK;
+    long long tot = 0;
     {
         bool bad = false;
-        long long tot = 0;
         for (int e = lane; e < E; e += 32) {
             bad |= cnt[e] < 0;
             tot += cnt[e];
@@ -95,94 +260,33 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
         if (bad || tot > (long long)INT_MAX) status = EP_ERR_INVAL;
     }
 
-    while (status == EP_OK) {
-        // 1. hottest rank, lowest index on ties
-        const int Lmax = __reduce_max_sync(kFull, max(L0, L1));
-        const unsigned bh = __ballot_sync(kFull, L0 == Lmax);
-        const int hot = bh ? __ffs(bh) - 1 : 32 + __ffs(__ballot_sync(kFull, L1 == Lmax)) - 1;
+    // registers of ranks lane (A) and lane+32 (B)
+    RankRegs<WB> A, B;
+    init_rank(A, lane, R, H, W, cnt);
+    init_rank(B, lane + 32, R, H, W, cnt);
 
-        // 2. hot's largest-quota instance, lowest expert id on ties (lane j = instance j)
-        int ej = -1, qj = -1;
-        if (lane < W) {
-            ej = (lane < H) ? hot * H + lane : slot[hot * S + (lane - H)];
-            if (ej >= 0) qj = q[hot * W + lane];
-        }
-        const int qmax = __reduce_max_sync(kFull, qj);
-        const unsigned tie = __ballot_sync(kFull, qj == qmax);
-        int src_lane;
-        if (__popc(tie) == 1) {
-            src_lane = __ffs(tie) - 1;
-        } else {
-            const bool in_tie = (tie >> lane) & 1u;
-            const int emin = __reduce_min_sync(kFull, in_tie ? ej : INT_MAX);
-            src_lane = __ffs(__ballot_sync(kFull, in_tie && ej == emin)) - 1;
-        }
-        const int e = __shfl_sync(kFull, ej, src_lane);
-
-        // 3. eligible ranks: hold e or have a free slot, not the hot rank
-        const uint64_t hm = holder[e];
-        const uint64_t elig = (hm | free_mask) & ~(1ull << hot);
-        if (elig == 0ull) break;  // slots ran out
-
-        // 4. coldest eligible rank, lowest index on ties
-        const int c0 = ((elig >> lane) & 1ull) ? L0 : INT_MAX;
-        const int c1 = ((elig >> (lane + 32)) & 1ull) ? L1 : INT_MAX;
-        const int Lmin = __reduce_min_sync(kFull, min(c0, c1));
-        const unsigned bc = __ballot_sync(kFull, c0 == Lmin);
-        const int cold = bc ? __ffs(bc) - 1 : 32 + __ffs(__ballot_sync(kFull, c1 == Lmin)) - 1;
-
-        // 5. amount
-        const int mv = min(qmax, (Lmax - Lmin) >> 1);
-        if (mv <= 0) break;
-        // 6. safety cap
-        if (iters == max_iters) {
-            status = EP_ERR_ITER_LIMIT;
-            break;
-        }
-
-        // 7. cold's instance of e, filling its lowest free slot if it has none
-        int p_dst;
-        if ((hm >> cold) & 1ull) {
-            if (cold == e / H) {
-                p_dst = cold * W + (e - cold * H);
-            } else {
-                const unsigned bs = __ballot_sync(kFull, lane < S && slot[cold * S + lane] == e);
-                p_dst = cold * W + H + __ffs(bs) - 1;
-            }
-        } else {
-            const int uc = __shfl_sync(kFull, cold < 32 ? used0 : used1, cold & 31);
-            p_dst = cold * W + H + uc;
-            if (lane == 0) {
-                slot[cold * S + uc] = e;
-                holder[e] = hm | (1ull << cold);
-            }
-            if (lane == (cold & 31)) {
-                if (cold < 32) ++used0; else ++used1;
-            }
-            if (uc + 1 == S) free_mask &= ~(1ull << cold);
-        }
-        if (lane == 0) {
-            q[hot * W + src_lane] -= mv;
-            q[p_dst] += mv;
-        }
-        if (lane == (hot & 31)) {
-            if (hot < 32) L0 -= mv; else L1 -= mv;
-        }
-        if (lane == (cold & 31)) {
-            if (cold < 32) L0 += mv; else L1 += mv;
-        }
-        ++iters;
-        __syncwarp();
+    int iters = 0;
+    if (status == EP_OK) {
+        if (tot < kPackLimit)
+            plan_moves<WB, kTwo, true>(A, B, lane, H, S, W, max_iters, iters, status);
+        else
+            plan_moves<WB, kTwo, false>(A, B, lane, H, S, W, max_iters, iters, status);
     }
-    __syncwarp();
 
-    // ---- outputs
+    // ---- outputs: quota, spare slots and loads straight from registers; the
+    // CSR is built from a shared-memory copy
+    unsigned char* base = smem + (size_t)warp * plan_warp_bytes(R, E, S);
+    int32_t* q = reinterpret_cast<int32_t*>(base);
+    int32_t* slot = reinterpret_cast<int32_t*>(base + align16((size_t)P * 4));
+    uint64_t* holder = reinterpret_cast<uint64_t*>(base + align16((size_t)P * 4) +
+                                                   align16((size_t)R * S * 4));
     int32_t* qo = quota_out + (int64_t)g * P;
-    for (int p = lane; p < P; p += 32) qo[p] = q[p];
     int32_t* so = slot_out + (int64_t)g * R * S;
-    for (int x = lane; x < R * S; x += 32) so[x] = slot[x];
-    if (lane < R) load_out[(int64_t)g * R + lane] = L0;
-    if (lane + 32 < R) load_out[(int64_t)g * R + lane + 32] = L1;
+    for (int e = lane; e < E; e += 32) holder[e] = 1ull << (e / H);
+    __syncwarp();
+    store_rank(A, lane, R, H, S, W, q, slot, holder, qo, so, load_out + (int64_t)g * R);
+    store_rank(B, lane + 32, R, H, S, W, q, slot, holder, qo, so, load_out + (int64_t)g * R);
+    __syncwarp();
 
     // logical -> physical CSR: home first, then replicas by ascending rank (= ascending p)
     int32_t* po = ptr_out + (int64_t)g * (E + 1);
@@ -230,6 +334,41 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     }
 }
 
+template <int WB, bool kTwo>
+cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
+                           int32_t max_iters, int32_t* quota, int32_t* slot_expert,
+                           int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
+                           int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
+                           cudaStream_t s) {
+    const size_t smem = kPlanWarps * plan_warp_bytes(d.R, d.E, d.S);
+    if (smem > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(plan_kernel<WB, kTwo>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)smem);
+        if (err != cudaSuccess) return err;
+    }
+    const unsigned blocks = (unsigned)((n_inst + kPlanWarps - 1) / kPlanWarps);
+    plan_kernel<WB, kTwo><<<blocks, kPlanWarps * 32, smem, s>>>(
+        counts, n_inst, d.R, d.E, d.S, max_iters, quota, slot_expert, rank_load, inst_ptr,
+        inst_id, inst_cum, n_iter, inst_status);
+    return cudaGetLastError();
+}
+
+template <int WB>
+cudaError_t launch_plan_r(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
+                          int32_t max_iters, int32_t* quota, int32_t* slot_expert,
+                          int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
+                          int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
+                          cudaStream_t s) {
+    if (d.R > 32)
+        return launch_plan_wb<WB, true>(d, counts, n_inst, max_iters, quota, slot_expert,
+                                        rank_load, inst_ptr, inst_id, inst_cum, n_iter,
+                                        inst_status, s);
+    return launch_plan_wb<WB, false>(d, counts, n_inst, max_iters, quota, slot_expert,
+                                     rank_load, inst_ptr, inst_id, inst_cum, n_iter,
+                                     inst_status, s);
+}
+
 }  // namespace
 
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
@@ -237,18 +376,21 @@ cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_i
                         int32_t* inst_ptr, int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter,
                         int32_t* inst_status, cudaStream_t s) {
     if (n_inst == 0) return cudaSuccess;
-    const size_t smem = kPlanWarps * plan_warp_bytes(d.R, d.E, d.S);
-    if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(plan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)smem);
-        if (err != cudaSuccess) return err;
-    }
-    const unsigned blocks = (unsigned)((n_inst + kPlanWarps - 1) / kPlanWarps);
-    plan_kernel<<<blocks, kPlanWarps * 32, smem, s>>>(counts, n_inst, d.R, d.E, d.S,
-                                                       max_iters, quota, slot_expert,
-                                                       rank_load, inst_ptr, inst_id, inst_cum,
-                                                       n_iter, inst_status);
-    return cudaGetLastError();
+    // register arrays sized to the instances per rank W = H + S (<= 32)
+    const int W = d.E / d.R + d.S;
+#define EP_PLAN_WB(wb)                                                                       \
+    if (W <= wb)                                                                             \
+        return launch_plan_r<wb>(d, counts, n_inst, max_iters, quota, slot_expert, rank_load, \
+                                 inst_ptr, inst_id, inst_cum, n_iter, inst_status, s);
+    EP_PLAN_WB(2)
+    EP_PLAN_WB(3)
+    EP_PLAN_WB(4)
+    EP_PLAN_WB(6)
+    EP_PLAN_WB(8)
+    EP_PLAN_WB(16)
+#undef EP_PLAN_WB
+    return launch_plan_r<32>(d, counts, n_inst, max_iters, quota, slot_expert, rank_load,
+                             inst_ptr, inst_id, inst_cum, n_iter, inst_status, s);
 }
 
 }  // namespace ultraep

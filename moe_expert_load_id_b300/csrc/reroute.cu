@@ -28,104 +28,140 @@
 namespace ultraep {
 namespace {
 
-constexpr int kRrThreads = 512;
-constexpr int kRrWarps = kRrThreads / 32;
-constexpr int kItems = 8;  // 32-slot steps per warp per chunk
-constexpr int kChunk = kRrThreads * kItems;
+constexpr int kItems = 16;  // 32-slot steps per warp per chunk (ids held in registers)
 
 struct RrLayout {
     int P, M;  // instances, CSR capacity
     size_t bytes;
 };
 
-__host__ __device__ inline RrLayout rr_layout(int R, int E, int S) {
+__host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps) {
     RrLayout l;
     l.P = R * (E / R + S);
     l.M = E + R * S;
-    // off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wcnt[kRrWarps][E]
+    // off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wcnt[warps][E]
     l.bytes = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
-                                 (size_t)kRrWarps * E);
+                                 (size_t)warps * E);
     return l;
 }
 
-__global__ void __launch_bounds__(kRrThreads)
+// One block per (instance, source rank); the rank's slots are processed in
+// chunks of kThreads * kItems.  kThreads = 1024 when few blocks run (one
+// instance: the whole rank is one chunk), 512 for batched calls.
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads)
 reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
                const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
                const int32_t* __restrict__ inst_ptr, const int32_t* __restrict__ inst_id,
                const int32_t* __restrict__ inst_cum, int32_t* __restrict__ dst_row,
                int32_t* __restrict__ src_slot, int32_t* __restrict__ inst_offset,
                int32_t* dev_status) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kChunk = kThreads * kItems;
+    constexpr int kIpt = (2048 + kThreads - 1) / kThreads;  // P <= 2048 quota per thread
     extern __shared__ __align__(16) int32_t sm[];
-    __shared__ int32_t warp_tot[kRrWarps];
+    __shared__ int32_t warp_tot[kWarps];
     __shared__ int32_t flags;
 
-    const RrLayout lay = rr_layout(R, E, S);
+    const RrLayout lay = rr_layout(R, E, S, kWarps);
     const int P = lay.P, M = lay.M;
     int32_t* off = sm;              // [P+1] first row of each instance
     int32_t* ptr = off + (P + 1);   // [E+1] CSR row pointers (clamped)
     int32_t* bcum = ptr + (E + 1);  // [M]   inclusive cumulative quota
     int32_t* bdel = bcum + M;       // [M]   row - within-expert rank
-    int32_t* base = bdel + M;       // [E]   running within-expert rank
-    int32_t* wcnt = base + E;       // [kRrWarps][E]
+    int32_t* base = bdel + M;       // [E]   within-expert rank of the chunk's first slot
+    int32_t* wcnt = base + E;       // [kWarps][E] per-warp counts, then per-warp bases
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int inst = blockIdx.x / R, r = blockIdx.x % R;
     const int32_t* qg = quota + (int64_t)inst * P;
-    if (tid == 0) flags = 0;
 
-    // ---- inst_offset: exclusive prefix of quota over p (P <= 2048, 4 per thread)
+    // ---- this block's slots (source rank r); the first chunk's ids are loaded
+    // before the prologue so their latency overlaps it
+    const int64_t Tr = tokens_per_rank(T, R);
+    const int64_t N = T * k;
+    const int64_t s0 = min(T, (int64_t)r * Tr) * k, s1 = min(T, (int64_t)(r + 1) * Tr) * k;
+    const int32_t* idi = ids + (int64_t)inst * N;
+    int ev[kItems];
     {
-        constexpr int kIpt = 4;
-        const int i0 = tid * kIpt;
-        int v[kIpt];
-        int local = 0;
+        const int64_t wb = s0 + (int64_t)warp * 32 * kItems + lane;
 #pragma unroll
-        for (int u = 0; u < kIpt; ++u) {
-            v[u] = (i0 + u < P) ? qg[i0 + u] : 0;
-            local += v[u];
+        for (int it = 0; it < kItems; ++it) {
+            const int64_t i = wb + it * 32;
+            ev[it] = (i < s1) ? __ldcs(idi + i) : -1;
         }
-        int x = local;
+    }
+
+    // ---- prologue
+    if (tid == 0) flags = 0;
+    for (int x = tid; x < (kWarps + 1) * E; x += kThreads) base[x] = 0;  // base and wcnt
+    int qv[kIpt];
+    int qlocal = 0;
+#pragma unroll
+    for (int u = 0; u < kIpt; ++u) {
+        const int p = tid * kIpt + u;
+        qv[u] = (p < P) ? qg[p] : 0;
+        qlocal += qv[u];
+    }
+    const int32_t* pg = inst_ptr + (int64_t)inst * (E + 1);
+    for (int e = tid; e <= E; e += kThreads) ptr[e] = min(max(pg[e], 0), M);
+    // inst_offset: exclusive prefix of quota over p
+    int qx = qlocal;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, qx, o);
+        if (lane >= o) qx += y;
+    }
+    if (lane == 31) warp_tot[warp] = qx;
+    __syncthreads();
+    if (warp == 0) {
+        int w = (lane < kWarps) ? warp_tot[lane] : 0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += y;
+            const int y = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += y;
         }
-        if (lane == 31) warp_tot[warp] = x;
-        __syncthreads();
-        if (warp == 0) {
-            int w = (lane < kRrWarps) ? warp_tot[lane] : 0;
+        if (lane < kWarps) warp_tot[lane] = w;  // inclusive over warps
+    }
+    // per-expert slots on earlier source ranks: thread (g, e) sums rows
+    // g, g+G, ... < r of column e (G = threads / E), loads eight at a time,
+    // then adds its partial into base[e]
+    {
+        const int32_t* cs = counts_src + (int64_t)inst * R * E;
+        const int G = (E <= kThreads) ? kThreads / E : 1;
+        for (int x = tid; x < G * E; x += kThreads) {
+            const int e = x % E, g = x / E;
+            int t = 0;
+            for (int r0 = g; r0 < r; r0 += 8 * G) {
+                int v[8];
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int y = __shfl_up_sync(kFull, w, o);
-                if (lane >= o) w += y;
+                for (int u = 0; u < 8; ++u) {
+                    const int rr = r0 + u * G;
+                    v[u] = (rr < r) ? cs[(int64_t)rr * E + e] : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t += v[u];
             }
-            if (lane < kRrWarps) warp_tot[lane] = w;  // inclusive over warps
+            if (t != 0) atomicAdd(&base[e], t);
         }
-        __syncthreads();
-        int run = x - local + (warp > 0 ? warp_tot[warp - 1] : 0);
+    }
+    __syncthreads();
+    {
+        int run = qx - qlocal + (warp > 0 ? warp_tot[warp - 1] : 0);
 #pragma unroll
         for (int u = 0; u < kIpt; ++u) {
-            if (i0 + u < P) off[i0 + u] = run;
-            run += v[u];
+            const int p = tid * kIpt + u;
+            if (p < P) off[p] = run;
+            run += qv[u];
         }
-        if (tid == kRrThreads - 1) off[P] = warp_tot[kRrWarps - 1];
+        if (tid == kThreads - 1) off[P] = warp_tot[kWarps - 1];
     }
-    // ---- CSR pointers, per-expert base from earlier source ranks, zero warp counters
-    const int32_t* pg = inst_ptr + (int64_t)inst * (E + 1);
-    for (int e = tid; e <= E; e += kRrThreads) ptr[e] = min(max(pg[e], 0), M);
-    for (int e = tid; e < E; e += kRrThreads) {
-        int s = 0;
-        const int32_t* cs = counts_src + (int64_t)inst * R * E + e;
-        for (int rr = 0; rr < r; ++rr) s += cs[(int64_t)rr * E];
-        base[e] = s;
-    }
-    for (int x = tid; x < kRrWarps * E; x += kRrThreads) wcnt[x] = 0;
     __syncthreads();
     {
         const int nM = ptr[E];
         const int32_t* ig = inst_id + (int64_t)inst * M;
         const int32_t* cg = inst_cum + (int64_t)inst * M;
-        for (int m = tid; m < M; m += kRrThreads) {
+        for (int m = tid; m < M; m += kThreads) {
             int cum = INT_MIN, del = 0;
             if (m < nM) {
                 const int p = ig[m];
@@ -140,70 +176,121 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     }
     if (r == 0) {
         int32_t* og = inst_offset + (int64_t)inst * (P + 1);
-        for (int p = tid; p <= P; p += kRrThreads) og[p] = off[p];
+        for (int p = tid; p <= P; p += kThreads) og[p] = off[p];
     }
-    __syncthreads();
+    // (the first chunk's phase A below touches only wcnt; its barrier orders
+    // the writes above before any read of bcum / bdel)
 
-    // ---- this block's slots: source rank r
-    const int64_t Tr = tokens_per_rank(T, R);
-    const int64_t N = T * k;
-    const int64_t s0 = min(T, (int64_t)r * Tr) * k, s1 = min(T, (int64_t)(r + 1) * Tr) * k;
-    const int32_t* idi = ids + (int64_t)inst * N;
     int32_t* dsti = dst_row + (int64_t)inst * N;
     int32_t* srci = src_slot ? src_slot + (int64_t)inst * N : nullptr;
     int32_t* wrow = wcnt + warp * E;
     const unsigned lt = lanemask_lt();
     int my_flags = 0;
+    // bits of an expert id (ids 0 .. E-1)
+    const int id_bits = (E > 1) ? 32 - __clz(E - 1) : 0;
+    // experts per phase-B pass: G consecutive threads share one expert's warps
+    int G = 1;
+    while (G * 2 <= kWarps && G * 2 * E <= kThreads) G *= 2;
 
     for (int64_t cs = s0; cs < s1; cs += kChunk) {
         const int64_t wb = cs + (int64_t)warp * 32 * kItems + lane;
-        int ev[kItems];
-        unsigned gm[kItems];
+        if (cs != s0) {
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int64_t i = wb + it * 32;
-            ev[it] = (i < s1) ? __ldcs(idi + i) : -1;
+            for (int it = 0; it < kItems; ++it) {
+                const int64_t i = wb + it * 32;
+                ev[it] = (i < s1) ? __ldcs(idi + i) : -1;
+            }
         }
-        // phase A: per-warp histogram of this chunk (warp-aggregated)
+        // phase A: per-warp histogram.  The lanes holding the same valid id are
+        // found with one ballot per id bit (match.any costs grow with the number
+        // of distinct ids in the warp; this does not); the group leader's
+        // atomic returns the group's base inside the warp, so every slot leaves
+        // phase A knowing its rank among the warp's slots of its expert.
+        // ev becomes e | rank << 10 (-1: invalid id).
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
             const int64_t i = wb + it * 32;
-            const bool valid = ev[it] >= 0 && ev[it] < E;
+            const int e = ev[it];
+            const bool valid = (unsigned)e < (unsigned)E;
             if (i < s1 && !valid) my_flags |= EP_DEV_BAD_ID;
-            if (!valid) ev[it] = -1;
-            gm[it] = __match_any_sync(kFull, ev[it]);
-            if (valid && lane == __ffs(gm[it]) - 1) atomicAdd(&wrow[ev[it]], __popc(gm[it]));
+            const int key = valid ? e : 0;
+            unsigned g = __ballot_sync(kFull, valid);
+#pragma unroll
+            for (int b = 0; b < 10; ++b) {
+                if (b < id_bits) {
+                    const bool bit = (key >> b) & 1;
+                    const unsigned bb = __ballot_sync(kFull, bit);
+                    g &= bit ? bb : ~bb;
+                }
+            }
+            const int leader = __ffs(g) - 1;
+            int old = 0;
+            if (valid && lane == leader) old = atomicAdd(&wrow[e], __popc(g));
+            old = __shfl_sync(kFull, old, leader & 31);
+            ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
         }
         __syncthreads();
-        // phase B: per expert, exclusive scan over warps on top of the running base
-        for (int e = tid; e < E; e += kRrThreads) {
-            int run = base[e];
-            for (int w = 0; w < kRrWarps; ++w) {
-                const int c = wcnt[w * E + e];
-                wcnt[w * E + e] = run;
-                run += c;
+        // phase B: per expert, exclusive scan over warps on top of base
+        if (G == 1) {
+            for (int e = tid; e < E; e += kThreads) {
+                int run = base[e];
+                for (int w = 0; w < kWarps; ++w) {
+                    const int c = wcnt[w * E + e];
+                    wcnt[w * E + e] = run;
+                    run += c;
+                }
+                base[e] = run;
             }
-            base[e] = run;
+        } else {
+            const int e = tid / G, gi = tid % G;
+            const bool act = e < E;
+            const int per = kWarps / G;
+            int loc = 0;
+            const int b0 = act ? base[e] : 0;
+            if (act)
+                for (int w = gi * per; w < (gi + 1) * per; ++w) loc += wcnt[w * E + e];
+            int incl = loc;
+            for (int o = 1; o < G; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o, G);
+                if (gi >= o) incl += y;
+            }
+            __syncwarp();
+            if (act) {
+                int run = b0 + incl - loc;
+                for (int w = gi * per; w < (gi + 1) * per; ++w) {
+                    const int c = wcnt[w * E + e];
+                    wcnt[w * E + e] = run;
+                    run += c;
+                }
+                if (gi == G - 1) base[e] = run;
+            }
         }
         __syncthreads();
         // phase C: within-expert rank -> instance -> row
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
             const int64_t i = wb + it * 32;
-            const int e = ev[it];
-            const unsigned g = gm[it];
-            const int b = (e >= 0) ? wrow[e] : 0;
-            __syncwarp();
-            if (e >= 0 && lane == __ffs(g) - 1) wrow[e] = b + __popc(g);
-            __syncwarp();
             if (i < s1) {
                 int d = -1;
-                if (e >= 0) {
-                    const int x = b + __popc(g & lt);
+                const int v = ev[it];
+                if (v >= 0) {
+                    const int e = v & 1023;
+                    const int x = wrow[e] + (v >> 10);
+                    // first entry of e's list whose inclusive cumulative
+                    // quota exceeds x (binary search: a hot expert can have
+                    // dozens of replicas)
                     int m = ptr[e];
-                    const int me = ptr[e + 1] - 1;
-                    while (m < me && bcum[m] <= x) ++m;
-                    if (m <= me && bcum[m] > x) {
+                    int n = ptr[e + 1] - m;
+                    while (n > 0) {
+                        const int h = n >> 1;
+                        if (bcum[m + h] <= x) {
+                            m += h + 1;
+                            n -= h + 1;
+                        } else {
+                            n = h;
+                        }
+                    }
+                    if (m < ptr[e + 1]) {
                         d = x + bdel[m];
                         if (d < 0 || d >= N) d = -1;
                     }
@@ -213,12 +300,33 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
                 if (srci != nullptr && d >= 0) srci[d] = (int32_t)i;
             }
         }
+        __syncwarp();
         for (int e = lane; e < E; e += 32) wrow[e] = 0;
         __syncwarp();
     }
     if (my_flags) atomicOr(&flags, my_flags);
     __syncthreads();
     if (tid == 0 && flags) raise_flag(dev_status, flags);
+}
+
+template <int kThreads>
+cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
+                             const int32_t* counts_src, const int32_t* quota,
+                             const int32_t* inst_ptr, const int32_t* inst_id,
+                             const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
+                             int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
+    const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32);
+    if (lay.bytes > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)lay.bytes);
+        if (err != cudaSuccess) return err;
+    }
+    const int64_t blocks = (int64_t)n_inst * d.R;
+    reroute_kernel<kThreads><<<(unsigned)blocks, kThreads, lay.bytes, s>>>(
+        ids, T, d.k, d.R, d.E, d.S, counts_src, quota, inst_ptr, inst_id, inst_cum, dst_row,
+        src_slot, inst_offset, dev_status);
+    return cudaGetLastError();
 }
 
 }  // namespace
@@ -229,17 +337,13 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
                            const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
                            int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
     if (n_inst == 0) return cudaSuccess;
-    const RrLayout lay = rr_layout(d.R, d.E, d.S);
-    if (lay.bytes > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(reroute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)lay.bytes);
-        if (err != cudaSuccess) return err;
-    }
     const int64_t blocks = (int64_t)n_inst * d.R;
-    reroute_kernel<<<(unsigned)blocks, kRrThreads, lay.bytes, s>>>(
-        ids, T, d.k, d.R, d.E, d.S, counts_src, quota, inst_ptr, inst_id, inst_cum, dst_row,
-        src_slot, inst_offset, dev_status);
-    return cudaGetLastError();
+    const int sms = device_info().sms;
+    if (blocks >= 2 * (int64_t)sms)
+        return launch_reroute_t<512>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+                                     inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
+    return launch_reroute_t<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+                                  inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
 }
 
 }  // namespace ultraep

@@ -228,7 +228,7 @@ def test_workspace_reused_across_calls():
     for _ in range(3):
         b.count(d)
         outs.append((b.counts.cpu().numpy().copy(), b.counts_src.cpu().numpy().copy()))
-        assert (b.workspace.cpu().numpy()[:2 * (w.R + 1)] == 0).all()
+        assert (b.workspace.cpu().numpy()[:2] == 0).all()          # the two instance tickets
     for c, cs in outs[1:]:
         assert (c == outs[0][0]).all() and (cs == outs[0][1]).all()
 
