@@ -68,6 +68,8 @@ typedef enum {
 #define EP_DEV_BAD_ID 1         /* an expert id outside [0, E) was seen and skipped */
 #define EP_DEV_QUOTA_OVERFLOW 2 /* a slot's within-expert rank exceeded its expert's quotas */
 #define EP_DEV_ROW_RANGE 4      /* a dst_row entry was >= T*k; that row was skipped */
+#define EP_DEV_COPY_TIMEOUT 8   /* a row copy did not complete within the kernel's wait
+                                   limit; the call stopped early and its output is incomplete */
 
 #define EP_PLAN_MAX_ITERS (1 << 16)
 #define EP_MAX_R 64
@@ -208,7 +210,13 @@ ep_status_t ep_reroute(const ep_domain_t *dom, const int32_t *topk_ids, int64_t 
  *   hidden  [n_inst][T][Hd]   bf16 in
  *   dst_row [n_inst][T*k]     int32 in (from ep_reroute); < 0: no row
  *   out     [n_inst][T*k][Hd] bf16 out; rows nobody maps to are not written
- *   dev_status int32          out: |= EP_DEV_ROW_RANGE for a dst_row >= T*k
+ *   dev_status int32          out: |= EP_DEV_ROW_RANGE for a dst_row >= T*k;
+ *                             |= EP_DEV_COPY_TIMEOUT if a bulk row copy did not
+ *                             complete within the kernel's bounded wait
+ *
+ * Rows of 1 KiB or more move through shared memory with TMA bulk copies
+ * (one global->shared copy per row, k shared->global copies); shorter rows
+ * use 16-byte vector loads and stores.
  */
 ep_status_t ep_permute(const void *hidden, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
                        const int32_t *dst_row, void *out, int32_t *dev_status, void *stream);

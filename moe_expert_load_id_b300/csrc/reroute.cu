@@ -13,10 +13,18 @@
 //                                              prefix over r (no extra pass)
 //   + (slots of e earlier in this rank)        running per-expert base
 //   + (slots of e in earlier warps of a chunk) per-expert scan over warps
-//   + (lanes below in the same 32-slot step)   popc(match.any group & lanemask_lt)
+//   + (lanes below in the same 32-slot step)   popc(group & lanemask_lt)
+// The group of lanes holding the same id is found with one ballot per id bit
+// (NB ballots, NB = bits of E-1); its leader's shared atomic returns the
+// group's base inside the warp.
+//
 // A slot of rank x goes to the first instance of e's list whose inclusive
 // cumulative quota exceeds x, at row  inst_offset[p] + x - (cum before p),
-// i.e. x + delta[m] with delta precomputed per list entry.
+// i.e. x + delta[m] with delta precomputed per list entry.  The per-warp
+// scan also records, for every (warp, expert), the list entry holding the
+// warp's first rank; a slot then steps forward from there (rarely more than
+// zero steps) instead of searching the whole list, which for a hot expert
+// holds dozens of replicas.
 //
 // ids are read once from memory (kept in registers between the histogram and
 // the assignment phase of a chunk); dst_row is written with coalesced
@@ -31,7 +39,8 @@ namespace {
 constexpr int kItems = 16;  // 32-slot steps per warp per chunk (ids held in registers)
 
 struct RrLayout {
-    int P, M;  // instances, CSR capacity
+    int P, M;      // instances, CSR capacity
+    size_t wm_off; // byte offset of the uint16 list-entry table
     size_t bytes;
 };
 
@@ -39,16 +48,33 @@ __host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps) {
     RrLayout l;
     l.P = R * (E / R + S);
     l.M = E + R * S;
-    // off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wcnt[warps][E]
-    l.bytes = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
-                                 (size_t)warps * E);
+    // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wcnt[warps][E]; uint16: wm[warps][E]
+    l.wm_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
+                                  (size_t)warps * E);
+    l.bytes = l.wm_off + sizeof(uint16_t) * (size_t)warps * E;
     return l;
+}
+
+// first index m in [lo, hi) with a[m] > x (hi when none)
+__device__ __forceinline__ int upper_bound(const int32_t* a, int lo, int hi, int x) {
+    int n = hi - lo;
+    while (n > 0) {
+        const int h = n >> 1;
+        if (a[lo + h] <= x) {
+            lo += h + 1;
+            n -= h + 1;
+        } else {
+            n = h;
+        }
+    }
+    return lo;
 }
 
 // One block per (instance, source rank); the rank's slots are processed in
 // chunks of kThreads * kItems.  kThreads = 1024 when few blocks run (one
-// instance: the whole rank is one chunk), 512 for batched calls.
-template <int kThreads>
+// instance: the whole rank is one chunk), 512 for batched calls.  NB >= bits
+// of E-1 (extra ballots on always-zero bits are harmless).
+template <int kThreads, int NB>
 __global__ void __launch_bounds__(kThreads)
 reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
                const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
@@ -71,6 +97,8 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     int32_t* bdel = bcum + M;       // [M]   row - within-expert rank
     int32_t* base = bdel + M;       // [E]   within-expert rank of the chunk's first slot
     int32_t* wcnt = base + E;       // [kWarps][E] per-warp counts, then per-warp bases
+    uint16_t* wm = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(sm) + lay.wm_off);
+                                    // [kWarps][E] list entry of each warp's base
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int inst = blockIdx.x / R, r = blockIdx.x % R;
@@ -184,10 +212,9 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     int32_t* dsti = dst_row + (int64_t)inst * N;
     int32_t* srci = src_slot ? src_slot + (int64_t)inst * N : nullptr;
     int32_t* wrow = wcnt + warp * E;
+    const uint16_t* wmrow = wm + warp * E;
     const unsigned lt = lanemask_lt();
     int my_flags = 0;
-    // bits of an expert id (ids 0 .. E-1)
-    const int id_bits = (E > 1) ? 32 - __clz(E - 1) : 0;
     // experts per phase-B pass: G consecutive threads share one expert's warps
     int G = 1;
     while (G * 2 <= kWarps && G * 2 * E <= kThreads) G *= 2;
@@ -201,12 +228,8 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
                 ev[it] = (i < s1) ? __ldcs(idi + i) : -1;
             }
         }
-        // phase A: per-warp histogram.  The lanes holding the same valid id are
-        // found with one ballot per id bit (match.any costs grow with the number
-        // of distinct ids in the warp; this does not); the group leader's
-        // atomic returns the group's base inside the warp, so every slot leaves
-        // phase A knowing its rank among the warp's slots of its expert.
-        // ev becomes e | rank << 10 (-1: invalid id).
+        // phase A: per-warp histogram and ranks inside the warp; ev becomes
+        // e | rank << 10 (-1: invalid id)
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
             const int64_t i = wb + it * 32;
@@ -216,12 +239,10 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             const int key = valid ? e : 0;
             unsigned g = __ballot_sync(kFull, valid);
 #pragma unroll
-            for (int b = 0; b < 10; ++b) {
-                if (b < id_bits) {
-                    const bool bit = (key >> b) & 1;
-                    const unsigned bb = __ballot_sync(kFull, bit);
-                    g &= bit ? bb : ~bb;
-                }
+            for (int b = 0; b < NB; ++b) {
+                const bool bit = (key >> b) & 1;
+                const unsigned bb = __ballot_sync(kFull, bit);
+                g &= bit ? bb : ~bb;
             }
             const int leader = __ffs(g) - 1;
             int old = 0;
@@ -230,13 +251,18 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
         }
         __syncthreads();
-        // phase B: per expert, exclusive scan over warps on top of base
+        // phase B: per expert, exclusive scan over warps on top of base, and
+        // the list entry holding each warp's first rank
         if (G == 1) {
             for (int e = tid; e < E; e += kThreads) {
                 int run = base[e];
+                const int end = ptr[e + 1];
+                int m = upper_bound(bcum, ptr[e], end, run);
                 for (int w = 0; w < kWarps; ++w) {
                     const int c = wcnt[w * E + e];
+                    while (m < end && bcum[m] <= run) ++m;
                     wcnt[w * E + e] = run;
+                    wm[w * E + e] = (uint16_t)m;
                     run += c;
                 }
                 base[e] = run;
@@ -257,9 +283,13 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             __syncwarp();
             if (act) {
                 int run = b0 + incl - loc;
+                const int end = ptr[e + 1];
+                int m = upper_bound(bcum, ptr[e], end, run);
                 for (int w = gi * per; w < (gi + 1) * per; ++w) {
                     const int c = wcnt[w * E + e];
+                    while (m < end && bcum[m] <= run) ++m;
                     wcnt[w * E + e] = run;
+                    wm[w * E + e] = (uint16_t)m;
                     run += c;
                 }
                 if (gi == G - 1) base[e] = run;
@@ -276,21 +306,10 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
                 if (v >= 0) {
                     const int e = v & 1023;
                     const int x = wrow[e] + (v >> 10);
-                    // first entry of e's list whose inclusive cumulative
-                    // quota exceeds x (binary search: a hot expert can have
-                    // dozens of replicas)
-                    int m = ptr[e];
-                    int n = ptr[e + 1] - m;
-                    while (n > 0) {
-                        const int h = n >> 1;
-                        if (bcum[m + h] <= x) {
-                            m += h + 1;
-                            n -= h + 1;
-                        } else {
-                            n = h;
-                        }
-                    }
-                    if (m < ptr[e + 1]) {
+                    const int end = ptr[e + 1];
+                    int m = wmrow[e];
+                    while (m < end && bcum[m] <= x) ++m;
+                    if (m < end) {
                         d = x + bdel[m];
                         if (d < 0 || d >= N) d = -1;
                     }
@@ -309,7 +328,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     if (tid == 0 && flags) raise_flag(dev_status, flags);
 }
 
-template <int kThreads>
+template <int kThreads, int NB>
 cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                              const int32_t* counts_src, const int32_t* quota,
                              const int32_t* inst_ptr, const int32_t* inst_id,
@@ -317,16 +336,39 @@ cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T
                              int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
     const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32);
     if (lay.bytes > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads>,
+        cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads, NB>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)lay.bytes);
         if (err != cudaSuccess) return err;
     }
     const int64_t blocks = (int64_t)n_inst * d.R;
-    reroute_kernel<kThreads><<<(unsigned)blocks, kThreads, lay.bytes, s>>>(
+    reroute_kernel<kThreads, NB><<<(unsigned)blocks, kThreads, lay.bytes, s>>>(
         ids, T, d.k, d.R, d.E, d.S, counts_src, quota, inst_ptr, inst_id, inst_cum, dst_row,
         src_slot, inst_offset, dev_status);
     return cudaGetLastError();
+}
+
+template <int kThreads>
+cudaError_t launch_reroute_nb(const ep_domain_t& d, const int32_t* ids, int64_t T,
+                              int32_t n_inst, const int32_t* counts_src, const int32_t* quota,
+                              const int32_t* inst_ptr, const int32_t* inst_id,
+                              const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
+                              int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
+    int bits = 0;  // bits of the largest id E-1
+    while ((1 << bits) < d.E) ++bits;
+#define EP_RR_NB(nb)                                                                       \
+    if (bits <= nb)                                                                        \
+        return launch_reroute_t<kThreads, nb>(d, ids, T, n_inst, counts_src, quota, inst_ptr, \
+                                              inst_id, inst_cum, dst_row, src_slot,          \
+                                              inst_offset, dev_status, s);
+    EP_RR_NB(3)
+    EP_RR_NB(5)
+    EP_RR_NB(7)
+    EP_RR_NB(8)
+#undef EP_RR_NB
+    return launch_reroute_t<kThreads, 10>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+                                          inst_cum, dst_row, src_slot, inst_offset, dev_status,
+                                          s);
 }
 
 }  // namespace
@@ -340,10 +382,10 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
     const int64_t blocks = (int64_t)n_inst * d.R;
     const int sms = device_info().sms;
     if (blocks >= 2 * (int64_t)sms)
-        return launch_reroute_t<512>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
-                                     inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
-    return launch_reroute_t<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
-                                  inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
+        return launch_reroute_nb<512>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+                                      inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
+    return launch_reroute_nb<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+                                   inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
 }
 
 }  // namespace ultraep

@@ -117,6 +117,11 @@ CASES = [
     ("many_instances",     8,  4, 1, 4,  512,   33,     8,   "zipf"),
     ("hidden_264",         8,  4, 1, 4,  300,   1,      264, "zipf"),
     ("hidden_4096",        16, 4, 1, 8,  512,   1,      4096, "zipf"),
+    # rows moved by TMA bulk copies: exactly the 1 KiB threshold, three
+    # segments of 8192 + 8192 + 16 bytes, several instances with invalid ids
+    ("bulk_row_1KiB",      8,  4, 1, 4,  333,   2,      512,  "zipf"),
+    ("bulk_row_3_segments", 4, 2, 1, 3,  97,    1,      8200, "zipf"),
+    ("bulk_rows_bad_ids",  8,  4, 2, 4,  250,   3,      1024, "bad"),
 ]
 
 
