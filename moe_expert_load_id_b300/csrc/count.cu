@@ -66,20 +66,26 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     int32_t* blk = sh + (E * C > kCountThreads ? E * C : kCountThreads);  // [E] block total
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int64_t b = blockIdx.x;
-    const int inst = (int)(b / ((int64_t)R * cps));
-    const int rc = (int)(b % ((int64_t)R * cps));
-    const int r = rc / cps, c = rc % cps;  // c is also the block's rank in its cluster
+    // block -> (instance, source rank, chunk); 32-bit divisions only (a 64-bit
+    // division by a run-time value is a long software routine)
+    const int b = (int)blockIdx.x;
+    const int per_inst = R * cps;
+    const int inst = b / per_inst;
+    const int rc = b - inst * per_inst;
+    const int r = rc / cps, c = rc - r * cps;  // c is also the block's rank in its cluster
 
     for (int x = tid; x < E * C; x += kCountThreads) hist[x] = 0;
     if (tid == 0) bad = 0;
     __syncthreads();
 
-    // this block's slots: chunk c of source rank r
-    const int64_t Tr = tokens_per_rank(T, R);
-    const int64_t t0 = min(T, (int64_t)r * Tr), t1 = min(T, (int64_t)(r + 1) * Tr);
-    const int64_t a = t0 * k, len = (t1 - t0) * k;
-    const int64_t s0 = a + len * c / cps, s1 = a + len * (c + 1) / cps;
+    // this block's slots: chunk c of source rank r (T < 2^31 since T*k < 2^31)
+    const int Ti = (int)T;
+    const int Tr = (Ti + R - 1) / R;
+    const int64_t t0 = min((int64_t)Ti, (int64_t)r * Tr), t1 = min((int64_t)Ti, (int64_t)(r + 1) * Tr);
+    const int len = (int)((t1 - t0) * k);
+    const int q = len / cps, rem = len - q * cps;
+    const int64_t s0 = t0 * k + (int64_t)q * c + min(c, rem);
+    const int64_t s1 = s0 + q + (c < rem ? 1 : 0);
     const int32_t* p0 = ids + (int64_t)inst * T * k + s0;
     const int64_t n = s1 - s0;
     // split into a scalar head up to the first 16-byte boundary, an int4 body

@@ -35,7 +35,7 @@ permute_kernel(const uint4* __restrict__ hidden, int64_t n_tok, int64_t T, int k
     const int64_t nw = ((int64_t)gridDim.x * kMoveThreads) >> 5;
     bool range_err = false;
     for (int64_t tok = w0; tok < n_tok; tok += nw) {
-        const int64_t inst = tok / T;
+        const int64_t inst = (tok < T) ? 0 : tok / T;
         int d = -1;
         if (lane < k) {
             d = __ldcs(dst_row + tok * k + lane);
@@ -78,7 +78,7 @@ unpermute_kernel(const uint4* __restrict__ grouped, int64_t n_tok, int64_t T, in
     bool range_err = false;
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     for (int64_t tok = w0; tok < n_tok; tok += nw) {
-        const int64_t inst = tok / T;
+        const int64_t inst = (tok < T) ? 0 : tok / T;
         int d = -1;
         if (lane < k) {
             d = __ldcs(dst_row + tok * k + lane);
@@ -197,11 +197,22 @@ permute_tma_kernel(const char* __restrict__ hidden, int64_t n_tok, int64_t T, in
     const int64_t nw = (int64_t)gridDim.x * kTmaWarps;
     const int64_t my_n = gw < n_units ? (n_units - 1 - gw) / nw + 1 : 0;
 
+    // unit -> (token, segment); one row segment is the common case
+    auto split = [&](int64_t u, int64_t& tok, int& sg) {
+        if (n_seg == 1) {
+            tok = u;
+            sg = 0;
+        } else {
+            tok = u / n_seg;
+            sg = (int)(u - tok * n_seg);
+        }
+    };
     // lane 0: issue the load of the warp's unit i into its buffer
     auto issue_load = [&](int64_t i) {
         const int64_t u = gw + i * nw;
-        const int64_t tok = u / n_seg;
-        const int sg = (int)(u - tok * n_seg);
+        int64_t tok;
+        int sg;
+        split(u, tok, sg);
         const uint32_t len = (uint32_t)min(seg, rowbytes - sg * seg);
         const int b = (int)(i % kStages);
         mbar_expect_tx(&bar[b], len);
@@ -216,8 +227,9 @@ permute_tma_kernel(const char* __restrict__ hidden, int64_t n_tok, int64_t T, in
     int64_t i = 0;
     for (; i < my_n; ++i) {
         const int64_t u = gw + i * nw;
-        const int64_t tok = u / n_seg;
-        const int sg = (int)(u - tok * n_seg);
+        int64_t tok;
+        int sg;
+        split(u, tok, sg);
         const uint32_t len = (uint32_t)min(seg, rowbytes - sg * seg);
         const int b = (int)(i % kStages);
         int d = -1;
@@ -230,7 +242,7 @@ permute_tma_kernel(const char* __restrict__ hidden, int64_t n_tok, int64_t T, in
         }
         if (lane == 0) timed_out = mbar_wait(&bar[b], (uint32_t)((i / kStages) & 1)) ? 0 : 1;
         if (__shfl_sync(kFull, timed_out, 0)) break;
-        const int64_t inst = tok / T;
+        const int64_t inst = (tok < T) ? 0 : tok / T;
         char* obase = out + (inst * N) * (int64_t)rowbytes + (int64_t)sg * seg;
         for (int j = 0; j < k; ++j) {
             const int dj = __shfl_sync(kFull, d, j);

@@ -14,22 +14,24 @@
 //   + (slots of e earlier in this rank)        running per-expert base
 //   + (slots of e in earlier warps of a chunk) per-expert scan over warps
 //   + (lanes below in the same 32-slot step)   popc(group & lanemask_lt)
-// The group of lanes holding the same id is found with one ballot per id bit
-// (NB ballots, NB = bits of E-1); its leader's shared atomic returns the
-// group's base inside the warp.
+// The group of lanes holding the same id is found through a per-warp mask
+// table in shared memory (each lane ORs in its bit; after a warp barrier the
+// mask is the group); the group's leader advances the warp's running count.
 //
 // A slot of rank x goes to the first instance of e's list whose inclusive
 // cumulative quota exceeds x, at row  inst_offset[p] + x - (cum before p),
 // i.e. x + delta[m] with delta precomputed per list entry.  The per-warp
-// scan also records, for every (warp, expert), the list entry holding the
-// warp's first rank; a slot then steps forward from there (rarely more than
-// zero steps) instead of searching the whole list, which for a hot expert
-// holds dozens of replicas.
+// scan also records, for every (warp, expert), the row of the warp's first
+// rank and how many ranks its instance holds from there; a slot inside that
+// range gets its row with one add, the rest (a warp's ranks crossing into the
+// next replica) binary search the expert's list, which for a hot expert holds
+// dozens of replicas.
 //
 // ids are read once from memory (kept in registers between the histogram and
 // the assignment phase of a chunk); dst_row is written with coalesced
 // streaming stores; the optional src_slot inverse is a scattered store.
 #include <climits>
+#include <type_traits>
 
 #include "common.cuh"
 
@@ -39,8 +41,8 @@ namespace {
 constexpr int kItems = 16;  // 32-slot steps per warp per chunk (ids held in registers)
 
 struct RrLayout {
-    int P, M;      // instances, CSR capacity
-    size_t wm_off; // byte offset of the uint16 list-entry table
+    int P, M;        // instances, CSR capacity
+    size_t lim_off;  // byte offset of the uint16 table wlim
     size_t bytes;
 };
 
@@ -48,10 +50,11 @@ __host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps) {
     RrLayout l;
     l.P = R * (E / R + S);
     l.M = E + R * S;
-    // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wcnt[warps][E]; uint16: wm[warps][E]
-    l.wm_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
-                                  (size_t)warps * E);
-    l.bytes = l.wm_off + sizeof(uint16_t) * (size_t)warps * E;
+    // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wx0[warps][E] wdb[warps][E]
+    // uint16: wlim[warps][E]
+    l.lim_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
+                                   2 * (size_t)warps * E);
+    l.bytes = l.lim_off + sizeof(uint16_t) * (size_t)warps * E;
     return l;
 }
 
@@ -72,9 +75,8 @@ __device__ __forceinline__ int upper_bound(const int32_t* a, int lo, int hi, int
 
 // One block per (instance, source rank); the rank's slots are processed in
 // chunks of kThreads * kItems.  kThreads = 1024 when few blocks run (one
-// instance: the whole rank is one chunk), 512 for batched calls.  NB >= bits
-// of E-1 (extra ballots on always-zero bits are harmless).
-template <int kThreads, int NB>
+// instance: the whole rank is one chunk) and E <= 512, else 512.
+template <int kThreads>
 __global__ void __launch_bounds__(kThreads)
 reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
                const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
@@ -96,33 +98,42 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     int32_t* bcum = ptr + (E + 1);  // [M]   inclusive cumulative quota
     int32_t* bdel = bcum + M;       // [M]   row - within-expert rank
     int32_t* base = bdel + M;       // [E]   within-expert rank of the chunk's first slot
-    int32_t* wcnt = base + E;       // [kWarps][E] per-warp counts, then per-warp bases
-    uint16_t* wm = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(sm) + lay.wm_off);
-                                    // [kWarps][E] list entry of each warp's base
+    int32_t* wx0 = base + E;        // [kWarps][E] per-warp counts, then each warp's first rank
+    int32_t* wdb = wx0 + kWarps * E;  // [kWarps][E] row of that first rank
+    uint16_t* wlim = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(sm) + lay.lim_off);
+                                    // [kWarps][E] ranks left in its instance (capped)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int inst = blockIdx.x / R, r = blockIdx.x % R;
     const int32_t* qg = quota + (int64_t)inst * P;
 
     // ---- this block's slots (source rank r); the first chunk's ids are loaded
-    // before the prologue so their latency overlaps it
-    const int64_t Tr = tokens_per_rank(T, R);
+    // before the prologue so their latency overlaps it.  Out-of-range ids are
+    // flagged here, at load time; slots past the end load as -1.
+    // (32-bit division: T < 2^31 since T*k < 2^31)
+    const int Tr = ((int)T + R - 1) / R;
     const int64_t N = T * k;
     const int64_t s0 = min(T, (int64_t)r * Tr) * k, s1 = min(T, (int64_t)(r + 1) * Tr) * k;
     const int32_t* idi = ids + (int64_t)inst * N;
+    int my_flags = 0;
     int ev[kItems];
-    {
-        const int64_t wb = s0 + (int64_t)warp * 32 * kItems + lane;
+    const int lbase = warp * 32 * kItems + lane;  // chunk-local index of item 0
+    auto load_chunk = [&](int64_t cs) {
+        const int nc = (int)min((int64_t)kChunk, s1 - cs);
+        const int32_t* src = idi + cs;
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
-            const int64_t i = wb + it * 32;
-            ev[it] = (i < s1) ? __ldcs(idi + i) : -1;
+            const int li = lbase + it * 32;
+            const int v = (li < nc) ? __ldcs(src + li) : -1;
+            if (li < nc && (unsigned)v >= (unsigned)E) my_flags |= EP_DEV_BAD_ID;
+            ev[it] = v;
         }
-    }
+    };
+    if (s0 < s1) load_chunk(s0);
 
     // ---- prologue
     if (tid == 0) flags = 0;
-    for (int x = tid; x < (kWarps + 1) * E; x += kThreads) base[x] = 0;  // base and wcnt
+    for (int x = tid; x < (2 * kWarps + 1) * E; x += kThreads) base[x] = 0;  // base, wx0, wdb
     int qv[kIpt];
     int qlocal = 0;
 #pragma unroll
@@ -206,63 +217,75 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         int32_t* og = inst_offset + (int64_t)inst * (P + 1);
         for (int p = tid; p <= P; p += kThreads) og[p] = off[p];
     }
-    // (the first chunk's phase A below touches only wcnt; its barrier orders
+    // (the first chunk's phase A below touches only wx0; its barrier orders
     // the writes above before any read of bcum / bdel)
 
     int32_t* dsti = dst_row + (int64_t)inst * N;
     int32_t* srci = src_slot ? src_slot + (int64_t)inst * N : nullptr;
-    int32_t* wrow = wcnt + warp * E;
-    const uint16_t* wmrow = wm + warp * E;
+    int32_t* wrow = wx0 + warp * E;
+    const int32_t* dbrow = wdb + warp * E;
+    const uint16_t* limrow = wlim + warp * E;
     const unsigned lt = lanemask_lt();
-    int my_flags = 0;
     // experts per phase-B pass: G consecutive threads share one expert's warps
     int G = 1;
     while (G * 2 <= kWarps && G * 2 * E <= kThreads) G *= 2;
 
+    // phase-B bookkeeping of one (warp, expert): its first rank x0, the row of
+    // that rank and how many ranks its instance still holds from there
+    auto warp_entry = [&](int w, int e, int x0, int& m, int end) {
+        while (m < end && bcum[m] <= x0) ++m;
+        wx0[w * E + e] = x0;
+        if (m < end) {
+            wdb[w * E + e] = x0 + bdel[m];
+            wlim[w * E + e] = (uint16_t)min(bcum[m] - x0, 0xffff);
+        } else {
+            wdb[w * E + e] = -1;
+            wlim[w * E + e] = 0;
+        }
+    };
+
     for (int64_t cs = s0; cs < s1; cs += kChunk) {
-        const int64_t wb = cs + (int64_t)warp * 32 * kItems + lane;
-        if (cs != s0) {
+        const int nc = (int)min((int64_t)kChunk, s1 - cs);
+        if (cs != s0) load_chunk(cs);
+        // phase A: per-warp histogram and ranks inside the warp; ev becomes
+        // e | rank << 10 (-1: no valid id).  The lanes holding the same id
+        // find each other through the warp's mask row (the wdb row, idle until
+        // phase B): each ORs its lane bit into mask[e]; after a warp barrier
+        // mask[e] is the group.  The group's lowest lane (leader) advances the
+        // warp's running count of e and clears mask[e] for the next step.
+        {
+            uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * E;
 #pragma unroll
             for (int it = 0; it < kItems; ++it) {
-                const int64_t i = wb + it * 32;
-                ev[it] = (i < s1) ? __ldcs(idi + i) : -1;
+                const int e = ev[it];
+                const bool valid = (unsigned)e < (unsigned)E;
+                if (valid) atomicOr(&mrow[e], 1u << lane);
+                __syncwarp();
+                const unsigned g = valid ? mrow[e] : 0u;
+                const int leader = __ffs(g) - 1;
+                __syncwarp();
+                int old = 0;
+                if (valid && lane == leader) {
+                    old = wrow[e];
+                    wrow[e] = old + __popc(g);
+                    mrow[e] = 0u;
+                }
+                __syncwarp();  // the clear lands before the next step's ORs
+                old = __shfl_sync(kFull, old, leader & 31);
+                ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
             }
-        }
-        // phase A: per-warp histogram and ranks inside the warp; ev becomes
-        // e | rank << 10 (-1: invalid id)
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int64_t i = wb + it * 32;
-            const int e = ev[it];
-            const bool valid = (unsigned)e < (unsigned)E;
-            if (i < s1 && !valid) my_flags |= EP_DEV_BAD_ID;
-            const int key = valid ? e : 0;
-            unsigned g = __ballot_sync(kFull, valid);
-#pragma unroll
-            for (int b = 0; b < NB; ++b) {
-                const bool bit = (key >> b) & 1;
-                const unsigned bb = __ballot_sync(kFull, bit);
-                g &= bit ? bb : ~bb;
-            }
-            const int leader = __ffs(g) - 1;
-            int old = 0;
-            if (valid && lane == leader) old = atomicAdd(&wrow[e], __popc(g));
-            old = __shfl_sync(kFull, old, leader & 31);
-            ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
         }
         __syncthreads();
         // phase B: per expert, exclusive scan over warps on top of base, and
-        // the list entry holding each warp's first rank
+        // each warp's entry (first rank, its row, ranks left in its instance)
         if (G == 1) {
             for (int e = tid; e < E; e += kThreads) {
                 int run = base[e];
                 const int end = ptr[e + 1];
                 int m = upper_bound(bcum, ptr[e], end, run);
                 for (int w = 0; w < kWarps; ++w) {
-                    const int c = wcnt[w * E + e];
-                    while (m < end && bcum[m] <= run) ++m;
-                    wcnt[w * E + e] = run;
-                    wm[w * E + e] = (uint16_t)m;
+                    const int c = wx0[w * E + e];
+                    warp_entry(w, e, run, m, end);
                     run += c;
                 }
                 base[e] = run;
@@ -274,7 +297,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             int loc = 0;
             const int b0 = act ? base[e] : 0;
             if (act)
-                for (int w = gi * per; w < (gi + 1) * per; ++w) loc += wcnt[w * E + e];
+                for (int w = gi * per; w < (gi + 1) * per; ++w) loc += wx0[w * E + e];
             int incl = loc;
             for (int o = 1; o < G; o <<= 1) {
                 const int y = __shfl_up_sync(kFull, incl, o, G);
@@ -286,41 +309,52 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
                 const int end = ptr[e + 1];
                 int m = upper_bound(bcum, ptr[e], end, run);
                 for (int w = gi * per; w < (gi + 1) * per; ++w) {
-                    const int c = wcnt[w * E + e];
-                    while (m < end && bcum[m] <= run) ++m;
-                    wcnt[w * E + e] = run;
-                    wm[w * E + e] = (uint16_t)m;
+                    const int c = wx0[w * E + e];
+                    warp_entry(w, e, run, m, end);
                     run += c;
                 }
                 if (gi == G - 1) base[e] = run;
             }
         }
         __syncthreads();
-        // phase C: within-expert rank -> instance -> row
+        // phase C: rank -> row.  Fast path: the rank is still inside the
+        // instance of the warp's first rank; else binary search the list.
+        // Full chunks skip the per-slot bounds test (warp-uniform branch).
+        int32_t* dst = dsti + cs;
+        auto phase_c = [&](auto full_tag) {
+            constexpr bool kFullChunk = decltype(full_tag)::value;
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int64_t i = wb + it * 32;
-            if (i < s1) {
-                int d = -1;
-                const int v = ev[it];
-                if (v >= 0) {
-                    const int e = v & 1023;
-                    const int x = wrow[e] + (v >> 10);
-                    const int end = ptr[e + 1];
-                    int m = wmrow[e];
-                    while (m < end && bcum[m] <= x) ++m;
-                    if (m < end) {
-                        d = x + bdel[m];
-                        if (d < 0 || d >= N) d = -1;
+            for (int it = 0; it < kItems; ++it) {
+                const int li = lbase + it * 32;
+                if (kFullChunk || li < nc) {
+                    const int v = ev[it];
+                    const bool has = v >= 0;
+                    const int e = has ? (v & 1023) : 0;
+                    const int rr = v >> 10;
+                    int d = dbrow[e] + rr;
+                    if (has && rr >= (int)limrow[e]) {
+                        const int x = wrow[e] + rr;
+                        const int end = ptr[e + 1];
+                        const int m = upper_bound(bcum, ptr[e], end, x);
+                        d = (m < end) ? x + bdel[m < M ? m : M - 1] : -1;
                     }
-                    if (d < 0) my_flags |= EP_DEV_QUOTA_OVERFLOW;
+                    if (has && (unsigned)d >= (unsigned)N) {
+                        d = -1;
+                        my_flags |= EP_DEV_QUOTA_OVERFLOW;
+                    }
+                    d = has ? d : -1;
+                    __stcs(dst + li, d);
+                    if (srci != nullptr && d >= 0) srci[d] = (int32_t)(cs + li);
                 }
-                __stcs(dsti + i, d);
-                if (srci != nullptr && d >= 0) srci[d] = (int32_t)i;
             }
-        }
+        };
+        if (nc == kChunk) phase_c(std::true_type{});
+        else phase_c(std::false_type{});
         __syncwarp();
-        for (int e = lane; e < E; e += 32) wrow[e] = 0;
+        for (int e = lane; e < E; e += 32) {
+            wrow[e] = 0;
+            wdb[warp * E + e] = 0;  // mask row of the next chunk's phase A
+        }
         __syncwarp();
     }
     if (my_flags) atomicOr(&flags, my_flags);
@@ -328,7 +362,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     if (tid == 0 && flags) raise_flag(dev_status, flags);
 }
 
-template <int kThreads, int NB>
+template <int kThreads>
 cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                              const int32_t* counts_src, const int32_t* quota,
                              const int32_t* inst_ptr, const int32_t* inst_id,
@@ -336,39 +370,16 @@ cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T
                              int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
     const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32);
     if (lay.bytes > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads, NB>,
+        cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)lay.bytes);
         if (err != cudaSuccess) return err;
     }
     const int64_t blocks = (int64_t)n_inst * d.R;
-    reroute_kernel<kThreads, NB><<<(unsigned)blocks, kThreads, lay.bytes, s>>>(
+    reroute_kernel<kThreads><<<(unsigned)blocks, kThreads, lay.bytes, s>>>(
         ids, T, d.k, d.R, d.E, d.S, counts_src, quota, inst_ptr, inst_id, inst_cum, dst_row,
         src_slot, inst_offset, dev_status);
     return cudaGetLastError();
-}
-
-template <int kThreads>
-cudaError_t launch_reroute_nb(const ep_domain_t& d, const int32_t* ids, int64_t T,
-                              int32_t n_inst, const int32_t* counts_src, const int32_t* quota,
-                              const int32_t* inst_ptr, const int32_t* inst_id,
-                              const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
-                              int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
-    int bits = 0;  // bits of the largest id E-1
-    while ((1 << bits) < d.E) ++bits;
-#define EP_RR_NB(nb)                                                                       \
-    if (bits <= nb)                                                                        \
-        return launch_reroute_t<kThreads, nb>(d, ids, T, n_inst, counts_src, quota, inst_ptr, \
-                                              inst_id, inst_cum, dst_row, src_slot,          \
-                                              inst_offset, dev_status, s);
-    EP_RR_NB(3)
-    EP_RR_NB(5)
-    EP_RR_NB(7)
-    EP_RR_NB(8)
-#undef EP_RR_NB
-    return launch_reroute_t<kThreads, 10>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
-                                          inst_cum, dst_row, src_slot, inst_offset, dev_status,
-                                          s);
 }
 
 }  // namespace
@@ -381,10 +392,10 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
     if (n_inst == 0) return cudaSuccess;
     const int64_t blocks = (int64_t)n_inst * d.R;
     const int sms = device_info().sms;
-    if (blocks >= 2 * (int64_t)sms)
-        return launch_reroute_nb<512>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+    if (blocks >= 2 * (int64_t)sms || d.E > 512)
+        return launch_reroute_t<512>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
                                       inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
-    return launch_reroute_nb<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+    return launch_reroute_t<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
                                    inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
 }
 
