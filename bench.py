@@ -2,9 +2,9 @@
 
 One step = one microbatch of the Qwen3-235B-like workload (R=64 ranks, E=128
 experts, S=1 spare slot per rank, top-8, T=131072 tokens, 94 MoE layers,
-hidden 4096 bf16) through all 94 layers; every layer runs
-ep_count -> ep_plan -> ep_reroute -> ep_permute through the C ABI, in that
-order, on one stream.  The metric is microseconds per MoE layer.
+hidden 4096 bf16) through all 94 layers; every layer runs ep_balance
+(ep_count -> ep_plan -> ep_reroute, chained on the device) then ep_permute
+through the C ABI, on one stream.  The metric is microseconds per MoE layer.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ultraep|reference]
 
@@ -23,6 +23,7 @@ import subprocess
 import sys
 import tempfile
 import time
+import types
 
 import numpy as np
 import torch
@@ -170,33 +171,57 @@ class LayerPipeline:
         self.inst_offset = torch.empty((1, dom.P + 1), **i32)
         self.grouped = torch.empty((1, w.N, w.Hd), dtype=torch.bfloat16, device=device)
 
+        # per-layer views of the outputs, in the form ep_balance takes
+        self.outs = [types.SimpleNamespace(
+            counts=self.counts[l:l + 1], counts_src=self.counts_src[l:l + 1],
+            quota=self.quota[l:l + 1], slot_expert=self.slot_expert[l:l + 1],
+            rank_load=self.rank_load[l:l + 1], inst_ptr=self.inst_ptr[l:l + 1],
+            inst_id=self.inst_id[l:l + 1], inst_cum=self.inst_cum[l:l + 1],
+            n_iter=self.n_iter[l:l + 1], inst_status=self.inst_status[l:l + 1],
+            dst_row=self.dst_row, src_slot=None, inst_offset=self.inst_offset)
+            for l in range(L)]
+
     def layer(self, l, ids_l, hidden_l, stream, ev=None):
+        """One layer as the library is meant to be called: ep_balance (count ->
+        plan -> reroute, chained on the device) then ep_permute."""
         U, d = self.U, self.dom
-        s = slice(l, l + 1)
         if ev is not None:
             ev[0].record(stream)
-        U.ep_count(d, ids_l, self.counts[s], self.counts_src[s], self.dev_status, self.workspace,
-                   stream)
+        U.ep_balance(d, ids_l, self.outs[l], self.dev_status, self.workspace, 0, stream)
         if ev is not None:
             ev[1].record(stream)
+        U.ep_permute(hidden_l, d.k, self.dst_row, self.grouped, self.dev_status, stream)
+        if ev is not None:
+            ev[2].record(stream)
+
+    def layer_split(self, l, ids_l, hidden_l, stream, ev):
+        """The same layer as four separate calls with an event between each,
+        for the per-kernel breakdown."""
+        U, d = self.U, self.dom
+        s = slice(l, l + 1)
+        ev[0].record(stream)
+        U.ep_count(d, ids_l, self.counts[s], self.counts_src[s], self.dev_status, self.workspace,
+                   stream)
+        ev[1].record(stream)
         U.ep_plan(d, self.counts[s], self.quota[s], self.slot_expert[s], self.rank_load[s],
                   self.inst_ptr[s], self.inst_id[s], self.inst_cum[s], self.n_iter[s],
                   self.inst_status[s], 0, stream)
-        if ev is not None:
-            ev[2].record(stream)
+        ev[2].record(stream)
         U.ep_reroute(d, ids_l, self.counts_src[s], self.quota[s], self.inst_ptr[s],
                      self.inst_id[s], self.inst_cum[s], self.dst_row, None, self.inst_offset,
                      self.dev_status, stream)
-        if ev is not None:
-            ev[3].record(stream)
+        ev[3].record(stream)
         U.ep_permute(hidden_l, d.k, self.dst_row, self.grouped, self.dev_status, stream)
-        if ev is not None:
-            ev[4].record(stream)
+        ev[4].record(stream)
 
     def step(self, ids, hiddens, stream, events=None):
         for l in range(self.w.layers):
             self.layer(l, ids[l:l + 1], hiddens[l % len(hiddens)][None], stream,
                        None if events is None else events[l])
+
+    def step_split(self, ids, hiddens, stream, events):
+        for l in range(self.w.layers):
+            self.layer_split(l, ids[l:l + 1], hiddens[l % len(hiddens)][None], stream, events[l])
 
     def results(self):
         """The step's result the host reads back: per-layer plan outcome."""
@@ -328,7 +353,7 @@ def run_ultraep(args, rank, world, local):
     # ---- timed region: K steps, device events per step and per launch
     L = w.layers
     step_ev = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps + 1)]
-    kern_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(L)]
+    kern_ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
                for _ in range(args.steps)]
     clocks = ClockSampler(device)
     barrier(world)
@@ -346,14 +371,21 @@ def run_ultraep(args, rank, world, local):
     ms_per_step = total_ms / args.steps
     value = total_ms * 1000.0 / (args.steps * L * world)
 
-    names = ("count", "plan", "reroute", "permute")
-    per = {n: [] for n in names}
+    per = {"balance": [], "permute": []}
     for k in range(args.steps):
         for l in range(L):
             e = kern_ev[k][l]
-            for i, n in enumerate(names):
-                per[n].append(e[i].elapsed_time(e[i + 1]) * 1000.0)
+            per["balance"].append(e[0].elapsed_time(e[1]) * 1000.0)
+            per["permute"].append(e[1].elapsed_time(e[2]) * 1000.0)
     avg = {n: float(np.mean(v)) for n, v in per.items()}
+
+    # ---- per-kernel breakdown: one more (untimed) step as four separate calls
+    names = ("count", "plan", "reroute", "permute")
+    split_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(L)]
+    pipe.step_split(ids, hiddens, stream, split_ev)
+    torch.cuda.synchronize(device)
+    split = {n: float(np.mean([split_ev[l][i].elapsed_time(split_ev[l][i + 1]) * 1000.0
+                               for l in range(L)])) for i, n in enumerate(names)}
 
     status = int(pipe.dev_status.item())
     plan_status = pipe.inst_status.cpu().numpy()
@@ -371,13 +403,18 @@ def run_ultraep(args, rank, world, local):
                 "unit": "GB/s", "frac": round(gbs(perm_bytes, avg["permute"]) / peak, 4),
                 "traffic": permute_traffic(), "algorithmic_bytes": perm_bytes,
                 "peak_source": f"{peak_kind} hbm_gbs"}
-    kernels = {n: {"us_per_launch": round(avg[n], 2)} for n in names}
-    kernels["count"].update(gbs=round(gbs(count_bytes, avg["count"]), 1),
-                            frac=round(gbs(count_bytes, avg["count"]) / peak, 4))
-    kernels["reroute"].update(gbs=round(gbs(reroute_bytes, avg["reroute"]), 1),
-                              frac=round(gbs(reroute_bytes, avg["reroute"]) / peak, 4))
-    kernels["permute"].update(gbs=roofline["achieved"], frac=roofline["frac"])
-    kernels["plan"].update(n_iter_mean=float(pipe.n_iter.float().mean().item()))
+    kernels = {"balance": {"us_per_launch": round(avg["balance"], 2),
+                           "launches": "ep_count + ep_plan + ep_reroute, one ep_balance call"},
+               "permute": {"us_per_launch": round(avg["permute"], 2),
+                           "gbs": roofline["achieved"], "frac": roofline["frac"]}}
+    breakdown = {n: {"us_per_launch": round(split[n], 2)} for n in names}
+    breakdown["count"].update(gbs=round(gbs(count_bytes, split["count"]), 1),
+                              frac=round(gbs(count_bytes, split["count"]) / peak, 4))
+    breakdown["reroute"].update(gbs=round(gbs(reroute_bytes, split["reroute"]), 1),
+                                frac=round(gbs(reroute_bytes, split["reroute"]) / peak, 4))
+    breakdown["plan"].update(n_iter_mean=float(pipe.n_iter.float().mean().item()))
+    breakdown["note"] = ("one extra step, outside the timed region, with the four calls made "
+                         "separately and an event between each")
 
     # ---- end to end: host (pinned) inputs -> device -> path -> host results
     e2e = None
@@ -418,7 +455,7 @@ def run_ultraep(args, rank, world, local):
     if unperm is not None:
         kernels["unpermute"] = unperm
     # indicative only: a real rank runs 1/R of count, reroute and permute on its own GPU
-    per_rank = (avg["count"] + avg["reroute"] + avg["permute"]) / w.R + avg["plan"]
+    per_rank = (split["count"] + split["reroute"] + split["permute"]) / w.R + split["plan"]
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_baseline:
@@ -433,11 +470,13 @@ def run_ultraep(args, rank, world, local):
                                    f"T={w.T} layers={w.layers} hidden={w.Hd} bf16, "
                                    f"Zipf(s={w.s}) popularity re-drawn per microbatch",
                        "step": "one microbatch through all layers, per layer "
-                               "ep_count -> ep_plan -> ep_reroute -> ep_permute",
+                               "ep_balance (ep_count -> ep_plan -> ep_reroute chained on the "
+                               "device) then ep_permute",
                        "l2": "inputs larger than L2 (1.07 GB hidden per layer, 8.6 GB "
                              "permute output per layer)",
                        "parallelism": f"replicas x{world}"},
-            "roofline": roofline, "kernels": kernels, "batched": batched,
+            "roofline": roofline, "kernels": kernels, "split_breakdown": breakdown,
+            "batched": batched,
             "per_rank_equivalent_us": round(per_rank, 2),
             "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": 4 * L * args.steps, "clocks": clock_rep, "quality": quality,

@@ -202,6 +202,46 @@ ep_status_t ep_reroute(const ep_domain_t *dom, const int32_t *topk_ids, int64_t 
                        void *stream);
 
 /*
+ * ep_balance -- ep_count, ep_plan and ep_reroute in one call, for the
+ * per-layer critical path (UltraEP article, "key design", forward-pass
+ * paragraph: obtain the load, solve the plan, reroute, all on the GPU before
+ * dispatch).  The three kernels are enqueued back to back on `stream` with
+ * programmatic dependent launch: the planner launches while the count is
+ * still running and waits on the device for its counts; the reroute launches
+ * while the planner is still running, loads and ranks its first chunk of ids
+ * (which depend on nothing the planner computes) and only then waits for the
+ * plan.  Results are exactly those of the three separate calls.
+ *
+ *   topk_ids, T, n_inst, max_iters, dev_status   as for ep_count / ep_plan
+ *   workspace   as for ep_count (ep_count_workspace_bytes() bytes)
+ *   out         the output arrays of the three calls (layouts as documented
+ *               there); out->src_slot may be NULL
+ * Errors: EP_ERR_INVAL / EP_ERR_WORKSPACE before anything is enqueued;
+ * EP_ERR_CUDA if a launch failed (earlier launches of the call may have been
+ * enqueued).
+ */
+typedef struct {
+    int32_t *counts;      /* [n_inst][E]       */
+    int32_t *counts_src;  /* [n_inst][R][E]    */
+    int32_t *quota;       /* [n_inst][P]       */
+    int32_t *slot_expert; /* [n_inst][R][S]    */
+    int32_t *rank_load;   /* [n_inst][R]       */
+    int32_t *inst_ptr;    /* [n_inst][E+1]     */
+    int32_t *inst_id;     /* [n_inst][E+R*S]   */
+    int32_t *inst_cum;    /* [n_inst][E+R*S]   */
+    int32_t *n_iter;      /* [n_inst]          */
+    int32_t *inst_status; /* [n_inst]          */
+    int32_t *dst_row;     /* [n_inst][T*k]     */
+    int32_t *src_slot;    /* [n_inst][T*k] or NULL */
+    int32_t *inst_offset; /* [n_inst][P+1]     */
+} ep_balance_out_t;
+
+ep_status_t ep_balance(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T,
+                       int32_t n_inst, int32_t max_iters, const ep_balance_out_t *out,
+                       int32_t *dev_status, void *workspace, size_t workspace_bytes,
+                       void *stream);
+
+/*
  * ep_permute -- the local half of dispatch (EPLB tutorial, "EPLB 和 DeepEP
  * 怎么协同？": every token is sent to the physical copy of each of its
  * top-k experts): out[dst_row[t*k+j]] = hidden[t] for every slot with a row.

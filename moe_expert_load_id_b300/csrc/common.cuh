@@ -16,6 +16,13 @@ __device__ __forceinline__ unsigned lanemask_lt() {
     return m;
 }
 
+// Programmatic dependent launch.  pdl_wait blocks until the grid this one
+// depends on has completed and its writes are visible; it returns at once
+// when the kernel was launched without that dependency.  pdl_trigger lets a
+// dependent grid start launching; it has no effect when none is waiting.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // Set bits in the caller's device status word.
 __device__ __forceinline__ void raise_flag(int32_t* dev_status, int32_t bits) {
     if (dev_status != nullptr) atomicOr(dev_status, bits);
@@ -49,14 +56,15 @@ cudaError_t launch_count_noalloc(const ep_domain_t& d, const int32_t* ids, int64
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
                         int32_t max_iters, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
                         int32_t* inst_ptr, int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter,
-                        int32_t* inst_status, cudaStream_t s);
+                        int32_t* inst_status, cudaStream_t s, bool pdl = false);
 
 // reroute
 cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                            const int32_t* counts_src, const int32_t* quota,
                            const int32_t* inst_ptr, const int32_t* inst_id,
                            const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
-                           int32_t* inst_offset, int32_t* dev_status, cudaStream_t s);
+                           int32_t* inst_offset, int32_t* dev_status, cudaStream_t s,
+                           bool pdl = false);
 
 // permute / unpermute
 cudaError_t launch_permute(const void* hidden, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,

@@ -65,6 +65,7 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     int32_t* hist = sh;                                            // [E][C], later scratch
     int32_t* blk = sh + (E * C > kCountThreads ? E * C : kCountThreads);  // [E] block total
 
+    pdl_trigger();  // a dependent planner may launch now; it waits for this grid
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // block -> (instance, source rank, chunk); 32-bit divisions only (a 64-bit
     // division by a run-time value is a long software routine)

@@ -238,6 +238,11 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
             int32_t* __restrict__ id_out, int32_t* __restrict__ cum_out,
             int32_t* __restrict__ iter_out, int32_t* __restrict__ status_out) {
     extern __shared__ __align__(16) unsigned char smem[];
+    // counts come from the previous grid (ep_balance launches this kernel as a
+    // programmatic dependent of ep_count); once they are visible, a dependent
+    // reroute may start its plan-independent work
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.x * kPlanWarps + warp;
     if (g >= n_inst) return;  // whole warp; no block-wide barrier follows
@@ -339,7 +344,7 @@ cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t 
                            int32_t max_iters, int32_t* quota, int32_t* slot_expert,
                            int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                            int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
-                           cudaStream_t s) {
+                           cudaStream_t s, bool pdl) {
     const size_t smem = kPlanWarps * plan_warp_bytes(d.R, d.E, d.S);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(plan_kernel<WB, kTwo>,
@@ -347,11 +352,19 @@ cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t 
                                                (int)smem);
         if (err != cudaSuccess) return err;
     }
-    const unsigned blocks = (unsigned)((n_inst + kPlanWarps - 1) / kPlanWarps);
-    plan_kernel<WB, kTwo><<<blocks, kPlanWarps * 32, smem, s>>>(
-        counts, n_inst, d.R, d.E, d.S, max_iters, quota, slot_expert, rank_load, inst_ptr,
-        inst_id, inst_cum, n_iter, inst_status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((n_inst + kPlanWarps - 1) / kPlanWarps));
+    cfg.blockDim = dim3(kPlanWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, plan_kernel<WB, kTwo>, counts, (int)n_inst, (int)d.R,
+                              (int)d.E, (int)d.S, (int)max_iters, quota, slot_expert, rank_load,
+                              inst_ptr, inst_id, inst_cum, n_iter, inst_status);
 }
 
 template <int WB>
@@ -359,14 +372,14 @@ cudaError_t launch_plan_r(const ep_domain_t& d, const int32_t* counts, int32_t n
                           int32_t max_iters, int32_t* quota, int32_t* slot_expert,
                           int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                           int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool pdl) {
     if (d.R > 32)
         return launch_plan_wb<WB, true>(d, counts, n_inst, max_iters, quota, slot_expert,
                                         rank_load, inst_ptr, inst_id, inst_cum, n_iter,
-                                        inst_status, s);
+                                        inst_status, s, pdl);
     return launch_plan_wb<WB, false>(d, counts, n_inst, max_iters, quota, slot_expert,
                                      rank_load, inst_ptr, inst_id, inst_cum, n_iter,
-                                     inst_status, s);
+                                     inst_status, s, pdl);
 }
 
 }  // namespace
@@ -374,14 +387,14 @@ cudaError_t launch_plan_r(const ep_domain_t& d, const int32_t* counts, int32_t n
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
                         int32_t max_iters, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
                         int32_t* inst_ptr, int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter,
-                        int32_t* inst_status, cudaStream_t s) {
+                        int32_t* inst_status, cudaStream_t s, bool pdl) {
     if (n_inst == 0) return cudaSuccess;
     // register arrays sized to the instances per rank W = H + S (<= 32)
     const int W = d.E / d.R + d.S;
 #define EP_PLAN_WB(wb)                                                                       \
     if (W <= wb)                                                                             \
         return launch_plan_r<wb>(d, counts, n_inst, max_iters, quota, slot_expert, rank_load, \
-                                 inst_ptr, inst_id, inst_cum, n_iter, inst_status, s);
+                                 inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl);
     EP_PLAN_WB(2)
     EP_PLAN_WB(3)
     EP_PLAN_WB(4)
@@ -390,7 +403,7 @@ cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_i
     EP_PLAN_WB(16)
 #undef EP_PLAN_WB
     return launch_plan_r<32>(d, counts, n_inst, max_iters, quota, slot_expert, rank_load,
-                             inst_ptr, inst_id, inst_cum, n_iter, inst_status, s);
+                             inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl);
 }
 
 }  // namespace ultraep

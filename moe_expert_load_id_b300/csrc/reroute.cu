@@ -107,9 +107,8 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     const int inst = blockIdx.x / R, r = blockIdx.x % R;
     const int32_t* qg = quota + (int64_t)inst * P;
 
-    // ---- this block's slots (source rank r); the first chunk's ids are loaded
-    // before the prologue so their latency overlaps it.  Out-of-range ids are
-    // flagged here, at load time; slots past the end load as -1.
+    // ---- this block's slots (source rank r).  Out-of-range ids are flagged
+    // at load time; slots past the end load as -1.
     // (32-bit division: T < 2^31 since T*k < 2^31)
     const int Tr = ((int)T + R - 1) / R;
     const int64_t N = T * k;
@@ -129,11 +128,52 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             ev[it] = v;
         }
     };
-    if (s0 < s1) load_chunk(s0);
-
-    // ---- prologue
+    // ---- shared tables that phase A needs: zero them first
     if (tid == 0) flags = 0;
     for (int x = tid; x < (2 * kWarps + 1) * E; x += kThreads) base[x] = 0;  // base, wx0, wdb
+    __syncthreads();
+
+    int32_t* wrow = wx0 + warp * E;
+    const unsigned lt = lanemask_lt();
+    // phase A: per-warp histogram and ranks inside the warp; ev becomes
+    // e | rank << 10 (-1: no valid id).  The lanes holding the same id find
+    // each other through the warp's mask row (the wdb row, idle until phase
+    // B): each ORs its lane bit into mask[e]; after a warp barrier mask[e] is
+    // the group.  The group's lowest lane (leader) advances the warp's running
+    // count of e and clears mask[e] for the next step.
+    auto phase_a = [&]() {
+        uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * E;
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int e = ev[it];
+            const bool valid = (unsigned)e < (unsigned)E;
+            if (valid) atomicOr(&mrow[e], 1u << lane);
+            __syncwarp();
+            const unsigned g = valid ? mrow[e] : 0u;
+            const int leader = __ffs(g) - 1;
+            __syncwarp();
+            int old = 0;
+            if (valid && lane == leader) {
+                old = wrow[e];
+                wrow[e] = old + __popc(g);
+                mrow[e] = 0u;
+            }
+            __syncwarp();  // the clear lands before the next step's ORs
+            old = __shfl_sync(kFull, old, leader & 31);
+            ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
+        }
+    };
+    // The first chunk's ids depend on nothing this library computes, so they
+    // are loaded and ranked before waiting for the plan (ep_balance launches
+    // this kernel as a programmatic dependent of ep_plan; a plain launch
+    // returns from the wait at once).
+    if (s0 < s1) {
+        load_chunk(s0);
+        phase_a();
+    }
+    pdl_wait();
+
+    // ---- prologue: plan tables
     int qv[kIpt];
     int qlocal = 0;
 #pragma unroll
@@ -217,15 +257,13 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         int32_t* og = inst_offset + (int64_t)inst * (P + 1);
         for (int p = tid; p <= P; p += kThreads) og[p] = off[p];
     }
-    // (the first chunk's phase A below touches only wx0; its barrier orders
-    // the writes above before any read of bcum / bdel)
+    // (the barrier before phase B orders the writes above before any read of
+    // bcum / bdel)
 
     int32_t* dsti = dst_row + (int64_t)inst * N;
     int32_t* srci = src_slot ? src_slot + (int64_t)inst * N : nullptr;
-    int32_t* wrow = wx0 + warp * E;
     const int32_t* dbrow = wdb + warp * E;
     const uint16_t* limrow = wlim + warp * E;
-    const unsigned lt = lanemask_lt();
     // experts per phase-B pass: G consecutive threads share one expert's warps
     int G = 1;
     while (G * 2 <= kWarps && G * 2 * E <= kThreads) G *= 2;
@@ -246,34 +284,9 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 
     for (int64_t cs = s0; cs < s1; cs += kChunk) {
         const int nc = (int)min((int64_t)kChunk, s1 - cs);
-        if (cs != s0) load_chunk(cs);
-        // phase A: per-warp histogram and ranks inside the warp; ev becomes
-        // e | rank << 10 (-1: no valid id).  The lanes holding the same id
-        // find each other through the warp's mask row (the wdb row, idle until
-        // phase B): each ORs its lane bit into mask[e]; after a warp barrier
-        // mask[e] is the group.  The group's lowest lane (leader) advances the
-        // warp's running count of e and clears mask[e] for the next step.
-        {
-            uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * E;
-#pragma unroll
-            for (int it = 0; it < kItems; ++it) {
-                const int e = ev[it];
-                const bool valid = (unsigned)e < (unsigned)E;
-                if (valid) atomicOr(&mrow[e], 1u << lane);
-                __syncwarp();
-                const unsigned g = valid ? mrow[e] : 0u;
-                const int leader = __ffs(g) - 1;
-                __syncwarp();
-                int old = 0;
-                if (valid && lane == leader) {
-                    old = wrow[e];
-                    wrow[e] = old + __popc(g);
-                    mrow[e] = 0u;
-                }
-                __syncwarp();  // the clear lands before the next step's ORs
-                old = __shfl_sync(kFull, old, leader & 31);
-                ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
-            }
+        if (cs != s0) {
+            load_chunk(cs);
+            phase_a();
         }
         __syncthreads();
         // phase B: per expert, exclusive scan over warps on top of base, and
@@ -367,7 +380,8 @@ cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T
                              const int32_t* counts_src, const int32_t* quota,
                              const int32_t* inst_ptr, const int32_t* inst_id,
                              const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
-                             int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
+                             int32_t* inst_offset, int32_t* dev_status, cudaStream_t s,
+                             bool pdl) {
     const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32);
     if (lay.bytes > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads>,
@@ -375,11 +389,19 @@ cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T
                                                (int)lay.bytes);
         if (err != cudaSuccess) return err;
     }
-    const int64_t blocks = (int64_t)n_inst * d.R;
-    reroute_kernel<kThreads><<<(unsigned)blocks, kThreads, lay.bytes, s>>>(
-        ids, T, d.k, d.R, d.E, d.S, counts_src, quota, inst_ptr, inst_id, inst_cum, dst_row,
-        src_slot, inst_offset, dev_status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)n_inst * d.R));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = lay.bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, reroute_kernel<kThreads>, ids, T, (int)d.k, (int)d.R,
+                              (int)d.E, (int)d.S, counts_src, quota, inst_ptr, inst_id, inst_cum,
+                              dst_row, src_slot, inst_offset, dev_status);
 }
 
 }  // namespace
@@ -388,15 +410,17 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
                            const int32_t* counts_src, const int32_t* quota,
                            const int32_t* inst_ptr, const int32_t* inst_id,
                            const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
-                           int32_t* inst_offset, int32_t* dev_status, cudaStream_t s) {
+                           int32_t* inst_offset, int32_t* dev_status, cudaStream_t s,
+                           bool pdl) {
     if (n_inst == 0) return cudaSuccess;
     const int64_t blocks = (int64_t)n_inst * d.R;
     const int sms = device_info().sms;
     if (blocks >= 2 * (int64_t)sms || d.E > 512)
         return launch_reroute_t<512>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
-                                      inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
+                                      inst_cum, dst_row, src_slot, inst_offset, dev_status, s, pdl);
     return launch_reroute_t<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
-                                   inst_cum, dst_row, src_slot, inst_offset, dev_status, s);
+                                   inst_cum, dst_row, src_slot, inst_offset, dev_status, s,
+                                   pdl);
 }
 
 }  // namespace ultraep

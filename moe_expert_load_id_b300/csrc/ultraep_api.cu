@@ -133,6 +133,40 @@ ep_status_t ep_reroute(const ep_domain_t* dom, const int32_t* topk_ids, int64_t 
                                     dev_status, static_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_balance(const ep_domain_t* dom, const int32_t* topk_ids, int64_t T,
+                       int32_t n_inst, int32_t max_iters, const ep_balance_out_t* out,
+                       int32_t* dev_status, void* workspace, size_t workspace_bytes,
+                       void* stream) {
+    if (out == nullptr || !domain_ok(dom) || !slots_ok(T, dom->k) || n_inst < 0)
+        return EP_ERR_INVAL;
+    const bool any = n_inst > 0;
+    const bool slots = any && T > 0;
+    if (!arr_ok(topk_ids, slots) || !arr_ok(out->counts, any) || !arr_ok(out->counts_src, any) ||
+        !arr_ok(out->quota, any) || !arr_ok(out->slot_expert, any && dom->S > 0) ||
+        !arr_ok(out->rank_load, any) || !arr_ok(out->inst_ptr, any) ||
+        !arr_ok(out->inst_id, any) || !arr_ok(out->inst_cum, any) || !arr_ok(out->n_iter, any) ||
+        !arr_ok(out->inst_status, any) || !arr_ok(out->dst_row, slots) ||
+        !arr_ok(out->src_slot, false) || !arr_ok(out->inst_offset, any) ||
+        !arr_ok(dev_status, false) || (any && !aligned(workspace, 16)))
+        return EP_ERR_INVAL;
+    if (!any) return EP_OK;
+    if (workspace == nullptr || workspace_bytes < count_workspace_bytes(*dom, T, n_inst))
+        return EP_ERR_WORKSPACE;
+    if (max_iters <= 0) max_iters = EP_PLAN_MAX_ITERS;
+    const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = launch_count(*dom, topk_ids, T, n_inst, out->counts, out->counts_src,
+                                   dev_status, workspace, s);
+    if (err != cudaSuccess) return EP_ERR_CUDA;
+    err = launch_plan(*dom, out->counts, n_inst, max_iters, out->quota, out->slot_expert,
+                      out->rank_load, out->inst_ptr, out->inst_id, out->inst_cum, out->n_iter,
+                      out->inst_status, s, /*pdl=*/true);
+    if (err != cudaSuccess) return EP_ERR_CUDA;
+    return from_cuda(launch_reroute(*dom, topk_ids, T, n_inst, out->counts_src, out->quota,
+                                    out->inst_ptr, out->inst_id, out->inst_cum, out->dst_row,
+                                    out->src_slot, out->inst_offset, dev_status, s,
+                                    /*pdl=*/true));
+}
+
 ep_status_t ep_permute(const void* hidden, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
                        const int32_t* dst_row, void* out, int32_t* dev_status, void* stream) {
     if (!rows_ok(T, k, Hd, n_inst)) return EP_ERR_INVAL;

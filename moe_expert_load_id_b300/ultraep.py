@@ -24,8 +24,8 @@ EP_DEV_BAD_ID, EP_DEV_QUOTA_OVERFLOW, EP_DEV_ROW_RANGE, EP_DEV_COPY_TIMEOUT = 1,
 EP_PLAN_MAX_ITERS = 1 << 16
 EP_COUNT_NOALLOC_SCRATCH_BYTES = 64 << 10
 
-EXPORTS = ("ep_count_workspace_bytes", "ep_count", "ep_plan", "ep_reroute", "ep_permute",
-           "ep_unpermute", "ep_status_str")
+EXPORTS = ("ep_count_workspace_bytes", "ep_count", "ep_count_noalloc", "ep_plan", "ep_reroute",
+           "ep_balance", "ep_permute", "ep_unpermute", "ep_status_str")
 
 
 class _Domain(ctypes.Structure):
@@ -72,6 +72,17 @@ _lib.ep_plan.restype = ctypes.c_int
 _lib.ep_plan.argtypes = [_DP, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 _lib.ep_reroute.restype = ctypes.c_int
 _lib.ep_reroute.argtypes = [_DP, _vp, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+
+
+class _BalanceOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "counts", "counts_src", "quota", "slot_expert", "rank_load", "inst_ptr", "inst_id",
+        "inst_cum", "n_iter", "inst_status", "dst_row", "src_slot", "inst_offset")]
+
+
+_lib.ep_balance.restype = ctypes.c_int
+_lib.ep_balance.argtypes = [_DP, _vp, _i64, _i32, _i32, ctypes.POINTER(_BalanceOut), _vp, _vp,
+                            _sz, _vp]
 _lib.ep_permute.restype = ctypes.c_int
 _lib.ep_permute.argtypes = [_vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
 _lib.ep_unpermute.restype = ctypes.c_int
@@ -147,6 +158,19 @@ def ep_reroute(dom, topk_ids, counts_src, quota, inst_ptr, inst_id, inst_cum, ds
                                          _stream(stream)))
 
 
+def ep_balance(dom, topk_ids, out, dev_status, workspace, max_iters=0, stream=None):
+    """count -> plan -> reroute in one call (three chained launches).  ``out``
+    has the attributes named like the fields of ep_balance_out_t (a Buffers
+    object does); ``out.src_slot`` may be None."""
+    n_inst, T = _shape_ids(topk_ids, dom.k)
+    o = _BalanceOut(*[_ptr(getattr(out, n)) for n, _ in _BalanceOut._fields_])
+    _check("ep_balance", _lib.ep_balance(ctypes.byref(dom.c()), _ptr(topk_ids), T, n_inst,
+                                         max_iters, ctypes.byref(o), _ptr(dev_status),
+                                         _ptr(workspace),
+                                         workspace.numel() * workspace.element_size(),
+                                         _stream(stream)))
+
+
 def _rows(x, k):
     if x.dim() == 2:
         return 1, x.shape[0], x.shape[1]
@@ -213,6 +237,10 @@ class Buffers:
 
     def permute(self, hidden, stream=None):
         ep_permute(hidden, self.dom.k, self.dst_row, self.grouped, self.dev_status, stream)
+
+    def balance_fused(self, topk_ids, max_iters=0, stream=None):
+        """count -> plan -> reroute through the single chained ep_balance call."""
+        ep_balance(self.dom, topk_ids, self, self.dev_status, self.workspace, max_iters, stream)
 
     def balance(self, topk_ids, hidden=None, stream=None):
         """count -> plan -> reroute (-> permute) for one batch of instances."""

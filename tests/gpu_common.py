@@ -11,16 +11,21 @@ def dom_of(R, E, S, k):
     return U.Domain(R, E, S, k)
 
 
-def gpu_run(dom, ids_np, hidden_u16=None, src_slot=True, max_iters=0, unpermute=True):
-    """ids_np [n_inst, T, k] int32 (host).  Returns host numpy views of every output."""
+def gpu_run(dom, ids_np, hidden_u16=None, src_slot=True, max_iters=0, unpermute=True,
+            fused=False):
+    """ids_np [n_inst, T, k] int32 (host).  Returns host numpy views of every output.
+    fused: count -> plan -> reroute through the single ep_balance call."""
     n_inst, T, k = ids_np.shape
     dev = "cuda"
     ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).to(dev)
     Hd = 0 if hidden_u16 is None else hidden_u16.shape[-1]
     b = U.Buffers(dom, T, n_inst, Hd=Hd, device=dev, src_slot=src_slot)
-    b.count(ids)
-    b.plan(max_iters=max_iters)
-    b.reroute(ids)
+    if fused:
+        b.balance_fused(ids, max_iters=max_iters)
+    else:
+        b.count(ids)
+        b.plan(max_iters=max_iters)
+        b.reroute(ids)
     out = {}
     if hidden_u16 is not None:
         hid = torch.from_numpy(np.ascontiguousarray(hidden_u16).view(np.int16)).to(dev)

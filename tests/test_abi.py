@@ -93,3 +93,39 @@ def test_host_rejections_need_no_gpu(lib):
     assert lib.ep_permute(fake, 0, 2, 16, 1, None, fake, None, None) == 0
     assert lib.ep_status_str(0) == b"EP_OK"
     assert b"workspace" in lib.ep_status_str(4)
+
+
+class BalanceOut(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in (
+        "counts", "counts_src", "quota", "slot_expert", "rank_load", "inst_ptr", "inst_id",
+        "inst_cum", "n_iter", "inst_status", "dst_row", "src_slot", "inst_offset")]
+
+
+def test_balance_host_rejections_need_no_gpu(lib):
+    vp = ctypes.c_void_p
+    lib.ep_balance.argtypes = [ctypes.POINTER(Dom), vp, ctypes.c_int64, ctypes.c_int32,
+                               ctypes.c_int32, ctypes.POINTER(BalanceOut), vp, vp,
+                               ctypes.c_size_t, vp]
+    d = Dom(8, 32, 1, 4)
+    fake = 0x10000                        # never dereferenced: every call below fails validation
+    full = BalanceOut(*([fake] * 10), fake, None, fake)
+    ws = vp(fake)
+    # no output struct, bad domain, T*k >= 2^31
+    assert lib.ep_balance(ctypes.byref(d), vp(fake), 16, 1, 0, None, None, ws, 1 << 20, None) == 1
+    assert lib.ep_balance(ctypes.byref(Dom(8, 30, 1, 4)), vp(fake), 16, 1, 0, ctypes.byref(full),
+                          None, ws, 1 << 20, None) == 1
+    assert lib.ep_balance(ctypes.byref(d), vp(fake), 1 << 29, 1, 0, ctypes.byref(full), None, ws,
+                          1 << 20, None) == 1
+    # a missing output array, a misaligned one, a workspace that is too small
+    missing = BalanceOut(*([fake] * 10), None, None, fake)
+    assert lib.ep_balance(ctypes.byref(d), vp(fake), 16, 1, 0, ctypes.byref(missing), None, ws,
+                          1 << 20, None) == 1
+    skew = BalanceOut(fake + 2, *([fake] * 9), fake, None, fake)
+    assert lib.ep_balance(ctypes.byref(d), vp(fake), 16, 1, 0, ctypes.byref(skew), None, ws,
+                          1 << 20, None) == 1
+    assert lib.ep_balance(ctypes.byref(d), vp(fake), 16, 1, 0, ctypes.byref(full), None, ws, 4,
+                          None) == 4
+    # zero instances: nothing to do
+    empty = BalanceOut(*([None] * 13))
+    assert lib.ep_balance(ctypes.byref(d), None, 16, 0, 0, ctypes.byref(empty), None, None, 0,
+                          None) == 0
