@@ -5,9 +5,8 @@
 //
 // One block per (instance, source rank, chunk).  The block's histogram is a
 // lane-column table hist[e][C] in shared memory: lane l adds its id e into
-// column l % C, so the 32 updates of one warp instruction never hit the same
-// address when C = 32 (and fall in 32 different banks), whatever the id
-// distribution.  A hot expert therefore costs nothing extra; match.any-based
+// column l % C, so at most 32/C updates of one warp instruction hit the same
+// address, whatever the id distribution.  A hot expert therefore costs nothing extra; match.any-based
 // aggregation, whose cost grows with the number of distinct ids in the warp,
 // is not used.  ids are read with 16-byte streaming loads (scalar head and
 // tail).
@@ -31,14 +30,17 @@ namespace cg = cooperative_groups;
 
 constexpr int kCountThreads = 512;
 constexpr int kCountWarps = kCountThreads / 32;
-constexpr int kVec = 4;                         // 16-byte loads in flight per thread
+constexpr int kVec = 2;                         // 16-byte loads in flight per thread
 constexpr int kTargetBlocks = 2 * 148;          // two blocks per B300 SM
 constexpr int kMinChunk = kCountThreads * 4;    // at least one 16-byte load per thread
 constexpr int kMaxChunksPerRank = 8;            // portable cluster size
 
-// columns of the lane-column histogram: 32 when E*32 ints fit 32 KB
+// columns of the lane-column histogram: 16 (lanes l and l+16 share a column,
+// at most a 2-way same-address collision) while E*16 ints fit 32 KB.  Four
+// blocks per SM with two 16-byte loads per thread measured faster than three
+// blocks with four loads and 32 columns.
 __host__ __device__ inline int count_cols(int E) {
-    int C = 32;
+    int C = 16;
     while (C > 1 && E * C > 8192) C >>= 1;
     return C;
 }
@@ -54,7 +56,7 @@ __device__ __forceinline__ void count_one(int v, int E, int32_t* hist, int C, in
     else bad = 1;
 }
 
-__global__ void __launch_bounds__(kCountThreads, 3)
+__global__ void __launch_bounds__(kCountThreads, 4)
 count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int cps,
              int32_t* __restrict__ counts, int32_t* __restrict__ counts_src,
              int32_t* dev_status, uint32_t* inst_ticket) {
@@ -65,7 +67,8 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     int32_t* hist = sh;                                            // [E][C], later scratch
     int32_t* blk = sh + (E * C > kCountThreads ? E * C : kCountThreads);  // [E] block total
 
-    pdl_trigger();  // a dependent planner may launch now; it waits for this grid
+    // A dependent planner (ep_balance) may launch now; it waits for this grid.
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // block -> (instance, source rank, chunk); 32-bit divisions only (a 64-bit
     // division by a run-time value is a long software routine)

@@ -238,9 +238,9 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
             int32_t* __restrict__ id_out, int32_t* __restrict__ cum_out,
             int32_t* __restrict__ iter_out, int32_t* __restrict__ status_out) {
     extern __shared__ __align__(16) unsigned char smem[];
-    // counts come from the previous grid (ep_balance launches this kernel as a
-    // programmatic dependent of ep_count); once they are visible, a dependent
-    // reroute may start its plan-independent work
+    // in ep_balance this grid is a programmatic dependent of ep_count: wait for
+    // its counts, then let the dependent reroute start its plan-independent
+    // work (for a plain launch both are no-ops)
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

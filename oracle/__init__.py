@@ -60,6 +60,9 @@ def _load(path):
     L.oracle_permute.restype = None
     L.oracle_permute.argtypes = [u16p, ctypes.c_int32, ctypes.c_int32, i32p,
                                  ctypes.c_int64, u16p]
+    L.oracle_combine.restype = None
+    L.oracle_combine.argtypes = [u16p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, i32p,
+                                 ctypes.POINTER(ctypes.c_float), u16p]
     L.oracle_unpermute.restype = None
     L.oracle_unpermute.argtypes = [u16p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                    i32p, u16p]
@@ -148,4 +151,19 @@ def unpermute(grouped_u16, T, k, dst_row):
     y = np.zeros((T, k, Hd), np.uint16)
     lib().oracle_unpermute(_p(grouped_u16, ctypes.c_uint16), T, k, Hd,
                            _p(dst_row, ctypes.c_int32), _p(y, ctypes.c_uint16))
+    return y
+
+
+def combine(grouped_u16, T, k, dst_row, weights):
+    """grouped_u16: uint16 [rows, Hd] (bf16 bits); dst_row int32 [T*k]; weights
+    float32 [T, k].  Returns uint16 [T, Hd]: the gate-weighted sum of each
+    token's k expert rows, float32 in ascending j, rounded to bf16."""
+    grouped_u16 = np.ascontiguousarray(grouped_u16, dtype=np.uint16)
+    Hd = grouped_u16.shape[1]
+    dst_row = _i32(dst_row)
+    w = np.ascontiguousarray(weights, dtype=np.float32)
+    y = np.zeros((T, Hd), np.uint16)
+    lib().oracle_combine(_p(grouped_u16, ctypes.c_uint16), T, k, Hd,
+                         _p(dst_row, ctypes.c_int32), _p(w, ctypes.c_float),
+                         _p(y, ctypes.c_uint16))
     return y

@@ -15,7 +15,9 @@ def build(force: bool = False) -> str:
     if (not force and os.path.exists(LIB)
             and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
         return LIB
-    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror",
+    # -ffp-contract=off: the combine rounds every product and every sum to
+    # float32 on its own (no fused multiply-add)
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-Werror", "-ffp-contract=off",
            "-shared", "-fPIC", SRC, "-o", LIB]
     subprocess.run(cmd, check=True)
     return LIB

@@ -22,7 +22,10 @@
  * The pages give no formula; where they are silent this file takes the
  * plainest reading, and every such reading is marked READING below.
  *
- * Integer-only: no floating point appears anywhere in this file.
+ * Steps 1-5 are integer-only.  The weighted combine at the end of the file
+ * (the step after unpermute) is the one place with floating point: float32
+ * products and sums, each rounded separately (the build disables FMA
+ * contraction), then a round-to-nearest-even conversion to bf16.
  *
  * Domain: R ranks, E logical experts, H = E/R home experts per rank, S spare
  * (redundant) slots per rank, P = R*(H+S) physical instances numbered
@@ -277,5 +280,55 @@ void oracle_unpermute(const uint16_t *grouped, int64_t T, int32_t k, int32_t Hd,
         int64_t row = dst_row[i];
         for (int32_t h = 0; h < Hd; h++)
             y[i * Hd + h] = (row < 0) ? 0 : grouped[row * Hd + h];
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Weighted combine -- combine with the gate weights ([C]: results on the
+ * physical copies return to their logical owner; the owner sums its top-k
+ * expert outputs weighted by the gate):
+ *   y[t][:] = bf16( sum over j = 0, 1, ..., k-1 of  w[t][j] * grouped[dst_row[t*k+j]][:] )
+ * READING (the pages give no arithmetic):
+ *   - float32 throughout; each product w*x is rounded to float32, then added
+ *     to the running sum (rounded to float32), in ascending j, starting from
+ *     +0.0;
+ *   - a slot with no row (dst_row < 0) adds nothing;
+ *   - the sum is rounded to bf16 to nearest, ties to even; any NaN result is
+ *     stored as the quiet NaN 0x7FC0 (NaN payloads are not portable).       */
+static float bf16_bits_to_f32(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+static uint16_t f32_to_bf16_bits(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu) != 0) return 0x7FC0u;
+    /* keep the upper 16 bits; round on the lower 16: above half rounds up,
+     * exactly half rounds to the even upper value */
+    uint32_t upper = u >> 16, lower = u & 0xFFFFu;
+    if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;
+    return (uint16_t)upper;
+}
+
+void oracle_combine(const uint16_t *grouped, int64_t T, int32_t k, int32_t Hd,
+                    const int32_t *dst_row, const float *w, uint16_t *y)
+{
+    for (int64_t t = 0; t < T; t++) {
+        for (int32_t h = 0; h < Hd; h++) {
+            float sum = 0.0f;
+            for (int32_t j = 0; j < k; j++) {
+                int64_t row = dst_row[t * k + j];
+                if (row < 0) continue;
+                float x = bf16_bits_to_f32(grouped[row * Hd + h]);
+                float prod = w[t * k + j] * x;
+                sum = sum + prod;
+            }
+            y[t * Hd + h] = f32_to_bf16_bits(sum);
+        }
     }
 }

@@ -8,6 +8,7 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_combine as combine_pins
 import test_oracle_pins as pins
 from golden_io import read_sections
 
@@ -43,6 +44,19 @@ MUTANTS = {
     "permute reads the row's own index": ("int64_t t = src_slot[row] / k;", "int64_t t = row / k;"),
     "missing slot not zeroed": ("(row < 0) ? 0 : grouped[row * Hd + h]",
                                 "(row < 0) ? grouped[h] : grouped[row * Hd + h]"),
+    "combine sums in descending j": (
+        "for (int32_t j = 0; j < k; j++) {\n                int64_t row = dst_row[t * k + j];",
+        "for (int32_t j = k - 1; j >= 0; j--) {\n                int64_t row = dst_row[t * k + j];"),
+    "combine rounds toward zero": (
+        "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;",
+        "if (lower > 0xFFFFu) upper += 1u;"),
+    "combine rounds ties up": (
+        "if (lower > 0x8000u || (lower == 0x8000u && (upper & 1u))) upper += 1u;",
+        "if (lower >= 0x8000u) upper += 1u;"),
+    "combine keeps NaN payloads": ("!= 0) return 0x7FC0u;", "!= 0) return (uint16_t)(u >> 16);"),
+    "combine reads row 0 for missing slots": ("if (row < 0) continue;", "if (row < 0) row = 0;"),
+    "combine accumulates in double": ("float sum = 0.0f;", "double sum = 0.0;"),
+    "combine multiplies after the sum": ("sum = sum + prod;", "sum = sum + x;"),
 }
 
 
@@ -64,6 +78,12 @@ def battery():
     for args in [(17, 3, 16), (64, 8, 24)]:
         pins.test_permute_unpermute_are_gathers(*args)
     pins.test_pipeline_round_trip_tiny_workload()
+    for name in ("test_exact_binary_fractions", "test_float32_sum_in_ascending_j",
+                 "test_bf16_round_to_nearest_even", "test_nan_inf_and_signed_zero",
+                 "test_missing_slots_add_nothing_and_zero_weights",
+                 "test_rows_follow_dst_row_per_token"):
+        getattr(combine_pins, name)()
+    combine_pins.test_k1_unit_weight_is_the_identity(0)
 
 
 def test_battery_passes_on_the_oracle():
@@ -78,8 +98,8 @@ def test_planted_mistake_is_caught(name, tmp_path):
     mutated = tmp_path / "mutant.c"
     mutated.write_text(src.replace(old, new))
     so = tmp_path / "libmutant.so"
-    subprocess.run(["gcc", "-O1", "-std=c11", "-shared", "-fPIC", str(mutated), "-o", str(so)],
-                   check=True)
+    subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-shared", "-fPIC",
+                    str(mutated), "-o", str(so)], check=True)
     with oracle.using_library(str(so)):
         with pytest.raises(AssertionError):
             battery()
