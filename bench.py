@@ -293,6 +293,28 @@ def unpermute_report(U, w, pipe, stream, device, peak, reps=5):
             "frac": round(by / (us * 1e-6) / 1e9 / peak, 4)}
 
 
+def combine_report(U, w, pipe, stream, device, peak, reps=5):
+    """ep_combine of the last layer's grouped rows with seeded softmax gate
+    weights, timed on its own (the step after unpermute; not in the metric)."""
+    gen = torch.Generator(device=device).manual_seed(7)
+    wts = torch.softmax(torch.randn((1, w.T, w.k), device=device, generator=gen), -1)
+    y = torch.empty((1, w.T, w.Hd), dtype=torch.bfloat16, device=device)
+    U.ep_combine(pipe.grouped, w.T, w.k, pipe.dst_row, wts, y, pipe.dev_status, stream)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        U.ep_combine(pipe.grouped, w.T, w.k, pipe.dst_row, wts, y, pipe.dev_status, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1000.0 / reps
+    by = w.T * (2 * w.Hd * w.k + 2 * w.Hd + 8 * w.k)   # k rows read, one written, dst + weights
+    del y
+    return {"us_per_launch": round(us, 2), "bytes": by,
+            "gbs": round(by / (us * 1e-6) / 1e9, 1),
+            "frac": round(by / (us * 1e-6) / 1e9 / peak, 4)}
+
+
 def make_inputs(w, microbatch, device):
     ids = torch.stack([W.topk_ids(w, l, microbatch, device=device) for l in range(w.layers)])
     hiddens = [W.hidden(w.T, w.Hd, w.seed(1000 + b, microbatch), device=device)
@@ -454,6 +476,8 @@ def run_ultraep(args, rank, world, local):
     unperm = unpermute_report(U, w, pipe, stream, device, peak) if args.extras else None
     if unperm is not None:
         kernels["unpermute"] = unperm
+    if args.extras:
+        kernels["combine"] = combine_report(U, w, pipe, stream, device, peak)
     # indicative only: a real rank runs 1/R of count, reroute and permute on its own GPU
     per_rank = (split["count"] + split["reroute"] + split["permute"]) / w.R + split["plan"]
 

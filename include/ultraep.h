@@ -276,6 +276,30 @@ ep_status_t ep_permute(const void *hidden, int64_t T, int32_t k, int32_t Hd, int
 ep_status_t ep_unpermute(const void *grouped, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
                          const int32_t *dst_row, void *y, int32_t *dev_status, void *stream);
 
+/*
+ * ep_combine -- the combine step with the gate weights, fused with the gather
+ * of unpermute (EPLB tutorial, "EPLB 和 DeepEP 怎么协同？": results on the
+ * physical copies return to their logical owner, which adds its top-k expert
+ * outputs weighted by the gate):
+ *     y[t][:] = bf16( sum over j = 0 .. k-1 of weights[t][j] * grouped[dst_row[t*k+j]][:] )
+ * The pages give no arithmetic; this library fixes it: float32, every product
+ * and every partial sum rounded on its own (no fused multiply-add), in
+ * ascending j starting from +0.0; a slot with no row (dst_row < 0) adds
+ * nothing; the sum is rounded to bf16 to nearest, ties to even; any NaN
+ * result is stored as 0x7FC0.  The result is therefore deterministic and
+ * bit-reproducible on any IEEE float32 machine.
+ *
+ *   grouped [n_inst][T*k][Hd] bf16 in (expert outputs in grouped row order)
+ *   dst_row [n_inst][T*k]     int32 in (from ep_reroute)
+ *   weights [n_inst][T][k]    float32 in (the gate's top-k weights)
+ *   y       [n_inst][T][Hd]   bf16 out
+ *   dev_status int32          out: |= EP_DEV_ROW_RANGE for a dst_row >= T*k
+ *                             (that slot adds nothing)
+ */
+ep_status_t ep_combine(const void *grouped, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
+                       const int32_t *dst_row, const float *weights, void *y,
+                       int32_t *dev_status, void *stream);
+
 /* Static string naming a status code. */
 const char *ep_status_str(ep_status_t status);
 

@@ -74,4 +74,9 @@ cudaError_t launch_unpermute(const void* grouped, int64_t T, int32_t k, int32_t 
                              int32_t n_inst, const int32_t* dst_row, void* y,
                              int32_t* dev_status, cudaStream_t s);
 
+// combine
+cudaError_t launch_combine(const void* grouped, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
+                           const int32_t* dst_row, const float* weights, void* y,
+                           int32_t* dev_status, cudaStream_t s);
+
 }  // namespace ultraep

@@ -193,6 +193,21 @@ ep_status_t ep_unpermute(const void* grouped, int64_t T, int32_t k, int32_t Hd, 
                                       static_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_combine(const void* grouped, int64_t T, int32_t k, int32_t Hd, int32_t n_inst,
+                       const int32_t* dst_row, const float* weights, void* y,
+                       int32_t* dev_status, void* stream) {
+    if (!rows_ok(T, k, Hd, n_inst)) return EP_ERR_INVAL;
+    const bool rows = n_inst > 0 && T > 0;
+    if (rows && Hd > 0 && (grouped == nullptr || y == nullptr || !aligned(grouped, 16) ||
+                           !aligned(y, 16)))
+        return EP_ERR_INVAL;
+    if (!arr_ok(dst_row, rows) || !arr_ok(weights, rows) || !arr_ok(dev_status, false))
+        return EP_ERR_INVAL;
+    if (!rows) return EP_OK;
+    return from_cuda(launch_combine(grouped, T, k, Hd, n_inst, dst_row, weights, y, dev_status,
+                                    static_cast<cudaStream_t>(stream)));
+}
+
 const char* ep_status_str(ep_status_t s) {
     switch (s) {
         case EP_OK: return "EP_OK";

@@ -25,7 +25,7 @@ EP_PLAN_MAX_ITERS = 1 << 16
 EP_COUNT_NOALLOC_SCRATCH_BYTES = 64 << 10
 
 EXPORTS = ("ep_count_workspace_bytes", "ep_count", "ep_count_noalloc", "ep_plan", "ep_reroute",
-           "ep_balance", "ep_permute", "ep_unpermute", "ep_status_str")
+           "ep_balance", "ep_permute", "ep_unpermute", "ep_combine", "ep_status_str")
 
 
 class _Domain(ctypes.Structure):
@@ -87,6 +87,8 @@ _lib.ep_permute.restype = ctypes.c_int
 _lib.ep_permute.argtypes = [_vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
 _lib.ep_unpermute.restype = ctypes.c_int
 _lib.ep_unpermute.argtypes = [_vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
+_lib.ep_combine.restype = ctypes.c_int
+_lib.ep_combine.argtypes = [_vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
 _lib.ep_status_str.restype = ctypes.c_char_p
 _lib.ep_status_str.argtypes = [ctypes.c_int]
 
@@ -190,6 +192,16 @@ def ep_unpermute(grouped, T, k, dst_row, y, dev_status=None, stream=None):
     n_inst = grouped.shape[0] if grouped.dim() == 3 else 1
     _check("ep_unpermute", _lib.ep_unpermute(_ptr(grouped), T, k, Hd, n_inst, _ptr(dst_row),
                                              _ptr(y), _ptr(dev_status), _stream(stream)))
+
+
+def ep_combine(grouped, T, k, dst_row, weights, y, dev_status=None, stream=None):
+    """grouped [T*k, Hd] or [n_inst, T*k, Hd] bf16, weights [.., T, k] float32 ->
+    y [.., T, Hd] bf16: the gate-weighted sum of each token's k expert rows."""
+    Hd = grouped.shape[-1]
+    n_inst = grouped.shape[0] if grouped.dim() == 3 else 1
+    _check("ep_combine", _lib.ep_combine(_ptr(grouped), T, k, Hd, n_inst, _ptr(dst_row),
+                                         _ptr(weights), _ptr(y), _ptr(dev_status),
+                                         _stream(stream)))
 
 
 # ------------------------------------------------------------------ buffers
