@@ -63,6 +63,10 @@ def _load(path):
     L.oracle_combine.restype = None
     L.oracle_combine.argtypes = [u16p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, i32p,
                                  ctypes.POINTER(ctypes.c_float), u16p]
+    L.oracle_stage.restype = None
+    L.oracle_stage.argtypes = [ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, i32p, i32p,
+                               ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, i32p,
+                               ctypes.POINTER(ctypes.c_int64)]
     L.oracle_unpermute.restype = None
     L.oracle_unpermute.argtypes = [u16p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                    i32p, u16p]
@@ -167,3 +171,20 @@ def combine(grouped_u16, T, k, dst_row, weights):
                          _p(dst_row, ctypes.c_int32), _p(w, ctypes.c_float),
                          _p(y, ctypes.c_uint16))
     return y
+
+
+def stage(expert_w, slot_expert, R, S, slot_w, prev=None):
+    """expert_w: uint8 [E, expert_bytes]; slot_expert int32 [R*S]; slot_w uint8
+    [R*S, expert_bytes], updated in place (a copy is returned).  Returns
+    (slot_w, n_copied, n_bad)."""
+    expert_w = np.ascontiguousarray(expert_w, dtype=np.uint8)
+    E, nb = expert_w.shape
+    se = _i32(np.asarray(slot_expert).reshape(-1))
+    out = np.ascontiguousarray(slot_w, dtype=np.uint8).copy()
+    pv = None if prev is None else _i32(np.asarray(prev).reshape(-1))
+    n_copied = ctypes.c_int32(0)
+    n_bad = ctypes.c_int64(0)
+    lib().oracle_stage(expert_w.ctypes.data, E, nb, _p(se, ctypes.c_int32),
+                       None if pv is None else _p(pv, ctypes.c_int32), R, S, out.ctypes.data,
+                       ctypes.byref(n_copied), ctypes.byref(n_bad))
+    return out, int(n_copied.value), int(n_bad.value)

@@ -332,3 +332,30 @@ void oracle_combine(const uint16_t *grouped, int64_t T, int32_t k, int32_t Hd,
         }
     }
 }
+
+/* ------------------------------------------------------------------------ */
+/* Replica weight staging -- the single-GPU half of weight distribution ([A]
+ * forward-pass paragraph: after planning, the replicas' expert weights are
+ * distributed to the ranks that host them; reserved-slot paragraph: the
+ * redundant slots are fixed buffers, reused across layers).  For every spare
+ * slot x = r*S + s:
+ *   e = slot_expert[x];  e == -1: empty, nothing copied;
+ *   e outside [-1, E): invalid, nothing copied, counted in *n_bad;
+ *   prev given and prev[x] == e: the slot already holds e, nothing copied;
+ *   else slot_w[x][:] = expert_w[e][:]  (expert_bytes bytes), counted.
+ * READING: "new replica" is a slot whose expert differs from what it held.  */
+void oracle_stage(const uint8_t *expert_w, int32_t E, int64_t expert_bytes,
+                  const int32_t *slot_expert, const int32_t *prev, int32_t R, int32_t S,
+                  uint8_t *slot_w, int32_t *n_copied, int64_t *n_bad)
+{
+    *n_copied = 0;
+    *n_bad = 0;
+    for (int64_t x = 0; x < (int64_t)R * S; x++) {
+        int32_t e = slot_expert[x];
+        if (e == -1) continue;
+        if (e < -1 || e >= E) { (*n_bad)++; continue; }
+        if (prev != NULL && prev[x] == e) continue;
+        memcpy(slot_w + x * expert_bytes, expert_w + (int64_t)e * expert_bytes, (size_t)expert_bytes);
+        (*n_copied)++;
+    }
+}

@@ -10,6 +10,7 @@ import pytest
 import oracle
 import test_oracle_combine as combine_pins
 import test_oracle_pins as pins
+import test_oracle_stage as stage_pins
 from golden_io import read_sections
 
 SRC = os.path.join(os.path.dirname(oracle.__file__), "ultraep_oracle.c")
@@ -57,6 +58,13 @@ MUTANTS = {
     "combine reads row 0 for missing slots": ("if (row < 0) continue;", "if (row < 0) row = 0;"),
     "combine accumulates in double": ("float sum = 0.0f;", "double sum = 0.0;"),
     "combine multiplies after the sum": ("sum = sum + prod;", "sum = sum + x;"),
+    "stage ignores what a slot holds": ("if (prev != NULL && prev[x] == e) continue;",
+                                        "if (prev != NULL && prev[x] == e + E) continue;"),
+    "stage clears empty slots": (
+        "if (e == -1) continue;",
+        "if (e == -1) { memset(slot_w + x * expert_bytes, 0, (size_t)expert_bytes); continue; }"),
+    "stage copies the next expert": ("expert_w + (int64_t)e * expert_bytes",
+                                     "expert_w + (int64_t)((e + 1) % E) * expert_bytes"),
 }
 
 
@@ -84,6 +92,8 @@ def battery():
                  "test_rows_follow_dst_row_per_token"):
         getattr(combine_pins, name)()
     combine_pins.test_k1_unit_weight_is_the_identity(0)
+    stage_pins.test_stage_is_a_gather_of_expert_rows()
+    stage_pins.test_empty_invalid_and_unchanged_slots_are_left_alone()
 
 
 def test_battery_passes_on_the_oracle():
