@@ -315,6 +315,32 @@ def combine_report(U, w, pipe, stream, device, peak, reps=5):
             "frac": round(by / (us * 1e-6) / 1e9 / peak, 4)}
 
 
+def stage_report(U, w, pipe, stream, device, peak, reps=3):
+    """ep_stage of the last layer's plan: every filled spare slot receives its
+    expert's weights (3 x hidden x 1536 bf16 = 37.7 MB per Qwen3-235B expert)
+    in a slot buffer reused across layers.  One synthetic expert table stands
+    in for the layer's (its contents do not change the copy)."""
+    expert_bytes = 3 * w.Hd * 1536 * 2
+    ew = torch.empty((w.E, expert_bytes), dtype=torch.uint8, device=device).fill_(1)
+    sw = torch.empty((w.R, w.S, expert_bytes), dtype=torch.uint8, device=device)
+    se = pipe.slot_expert[w.layers - 1:w.layers]
+    U.ep_stage(pipe.dom, ew, se, sw, None, pipe.dev_status, stream)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        U.ep_stage(pipe.dom, ew, se, sw, None, pipe.dev_status, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1000.0 / reps
+    filled = int((se >= 0).sum().item())
+    by = 2 * filled * expert_bytes                      # read the expert, write the slot
+    del ew, sw
+    return {"us_per_layer": round(us, 2), "replicas": filled, "expert_bytes": expert_bytes,
+            "bytes": by, "gbs": round(by / (us * 1e-6) / 1e9, 1),
+            "frac": round(by / (us * 1e-6) / 1e9 / peak, 4)}
+
+
 def make_inputs(w, microbatch, device):
     ids = torch.stack([W.topk_ids(w, l, microbatch, device=device) for l in range(w.layers)])
     hiddens = [W.hidden(w.T, w.Hd, w.seed(1000 + b, microbatch), device=device)
@@ -478,6 +504,7 @@ def run_ultraep(args, rank, world, local):
         kernels["unpermute"] = unperm
     if args.extras:
         kernels["combine"] = combine_report(U, w, pipe, stream, device, peak)
+        kernels["stage"] = stage_report(U, w, pipe, stream, device, peak)
     # indicative only: a real rank runs 1/R of count, reroute and permute on its own GPU
     per_rank = (split["count"] + split["reroute"] + split["permute"]) / w.R + split["plan"]
 

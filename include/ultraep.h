@@ -300,6 +300,31 @@ ep_status_t ep_combine(const void *grouped, int64_t T, int32_t k, int32_t Hd, in
                        const int32_t *dst_row, const float *weights, void *y,
                        int32_t *dev_status, void *stream);
 
+/*
+ * ep_stage -- replica weight staging, the single-GPU half of weight
+ * distribution (UltraEP article, "key design", forward-pass paragraph: after
+ * planning, the replicas' expert weights go to the ranks hosting them;
+ * reserved-slot paragraph: the redundant slots are fixed buffers reused
+ * across layers).  For every spare slot x = r*S + s of every instance:
+ *     e = slot_expert[x]; e == -1: empty, nothing copied;
+ *     e outside [-1, E): nothing copied, |= EP_DEV_BAD_ID;
+ *     prev_slot_expert given and prev_slot_expert[x] == e: the slot already
+ *         holds e, nothing copied (only new replicas move);
+ *     else slot_w[x][:] = expert_w[e][:]   (expert_bytes bytes).
+ *
+ *   expert_w         [n_inst][E][expert_bytes] in (per-layer expert weights)
+ *   expert_bytes     bytes of one expert's weights, a multiple of 16
+ *   slot_expert      [n_inst][R][S] int32 in (from ep_plan)
+ *   prev_slot_expert [n_inst][R][S] int32 in, may be NULL
+ *   slot_w           [n_inst][R][S][expert_bytes] out (a cross-layer reused
+ *                    buffer: n_inst = 1, staged again for every layer)
+ * expert_w and slot_w must be 16-byte aligned.
+ */
+ep_status_t ep_stage(const ep_domain_t *dom, int32_t n_inst, const void *expert_w,
+                     int64_t expert_bytes, const int32_t *slot_expert,
+                     const int32_t *prev_slot_expert, void *slot_w, int32_t *dev_status,
+                     void *stream);
+
 /* Static string naming a status code. */
 const char *ep_status_str(ep_status_t status);
 

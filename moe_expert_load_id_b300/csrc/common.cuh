@@ -79,4 +79,10 @@ cudaError_t launch_combine(const void* grouped, int64_t T, int32_t k, int32_t Hd
                            const int32_t* dst_row, const float* weights, void* y,
                            int32_t* dev_status, cudaStream_t s);
 
+// replica weight staging
+cudaError_t launch_stage(const ep_domain_t& d, int32_t n_inst, const void* expert_w,
+                         int64_t expert_bytes, const int32_t* slot_expert,
+                         const int32_t* prev_slot_expert, void* slot_w, int32_t* dev_status,
+                         cudaStream_t s);
+
 }  // namespace ultraep

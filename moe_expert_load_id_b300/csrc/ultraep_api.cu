@@ -208,6 +208,25 @@ ep_status_t ep_combine(const void* grouped, int64_t T, int32_t k, int32_t Hd, in
                                     static_cast<cudaStream_t>(stream)));
 }
 
+ep_status_t ep_stage(const ep_domain_t* dom, int32_t n_inst, const void* expert_w,
+                     int64_t expert_bytes, const int32_t* slot_expert,
+                     const int32_t* prev_slot_expert, void* slot_w, int32_t* dev_status,
+                     void* stream) {
+    if (!domain_ok(dom) || n_inst < 0 || expert_bytes < 0 || expert_bytes % 16 != 0)
+        return EP_ERR_INVAL;
+    const bool any = n_inst > 0 && dom->S > 0 && expert_bytes > 0;
+    if (any && (expert_w == nullptr || slot_w == nullptr || !aligned(expert_w, 16) ||
+                !aligned(slot_w, 16)))
+        return EP_ERR_INVAL;
+    if (!arr_ok(slot_expert, any) || !arr_ok(prev_slot_expert, false) ||
+        !arr_ok(dev_status, false))
+        return EP_ERR_INVAL;
+    if (!any) return EP_OK;
+    return from_cuda(launch_stage(*dom, n_inst, expert_w, expert_bytes, slot_expert,
+                                  prev_slot_expert, slot_w, dev_status,
+                                  static_cast<cudaStream_t>(stream)));
+}
+
 const char* ep_status_str(ep_status_t s) {
     switch (s) {
         case EP_OK: return "EP_OK";

@@ -25,7 +25,7 @@ EP_PLAN_MAX_ITERS = 1 << 16
 EP_COUNT_NOALLOC_SCRATCH_BYTES = 64 << 10
 
 EXPORTS = ("ep_count_workspace_bytes", "ep_count", "ep_count_noalloc", "ep_plan", "ep_reroute",
-           "ep_balance", "ep_permute", "ep_unpermute", "ep_combine", "ep_status_str")
+           "ep_balance", "ep_permute", "ep_unpermute", "ep_combine", "ep_stage", "ep_status_str")
 
 
 class _Domain(ctypes.Structure):
@@ -89,6 +89,8 @@ _lib.ep_unpermute.restype = ctypes.c_int
 _lib.ep_unpermute.argtypes = [_vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp]
 _lib.ep_combine.restype = ctypes.c_int
 _lib.ep_combine.argtypes = [_vp, _i64, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp]
+_lib.ep_stage.restype = ctypes.c_int
+_lib.ep_stage.argtypes = [_DP, _i32, _vp, _i64, _vp, _vp, _vp, _vp, _vp]
 _lib.ep_status_str.restype = ctypes.c_char_p
 _lib.ep_status_str.argtypes = [ctypes.c_int]
 
@@ -202,6 +204,20 @@ def ep_combine(grouped, T, k, dst_row, weights, y, dev_status=None, stream=None)
     _check("ep_combine", _lib.ep_combine(_ptr(grouped), T, k, Hd, n_inst, _ptr(dst_row),
                                          _ptr(weights), _ptr(y), _ptr(dev_status),
                                          _stream(stream)))
+
+
+def ep_stage(dom, expert_w, slot_expert, slot_w, prev_slot_expert=None, dev_status=None,
+             stream=None):
+    """expert_w [E, bytes] or [n_inst, E, bytes] (any dtype, bytes a multiple of
+    16) -> slot_w [.., R, S, bytes]: each filled spare slot gets its expert's
+    weights (slots already holding their expert are skipped when
+    prev_slot_expert is given)."""
+    n_inst = slot_expert.numel() // max(1, dom.R * dom.S) if dom.S else 0
+    E = dom.E
+    nbytes = expert_w.numel() * expert_w.element_size() // max(1, n_inst * E) if n_inst else 0
+    _check("ep_stage", _lib.ep_stage(ctypes.byref(dom.c()), n_inst, _ptr(expert_w), nbytes,
+                                     _ptr(slot_expert), _ptr(prev_slot_expert), _ptr(slot_w),
+                                     _ptr(dev_status), _stream(stream)))
 
 
 # ------------------------------------------------------------------ buffers

@@ -129,3 +129,21 @@ def test_balance_host_rejections_need_no_gpu(lib):
     empty = BalanceOut(*([None] * 13))
     assert lib.ep_balance(ctypes.byref(d), None, 16, 0, 0, ctypes.byref(empty), None, None, 0,
                           None) == 0
+
+
+def test_stage_host_rejections_need_no_gpu(lib):
+    vp = ctypes.c_void_p
+    lib.ep_stage.argtypes = [ctypes.POINTER(Dom), ctypes.c_int32, vp, ctypes.c_int64, vp, vp,
+                             vp, vp, vp]
+    d = Dom(8, 32, 1, 4)
+    fake = vp(0x10000)                    # never dereferenced: every call below fails validation
+    assert lib.ep_stage(ctypes.byref(d), 1, fake, 24, fake, None, fake, None, None) == 1  # 24 % 16
+    assert lib.ep_stage(ctypes.byref(d), 1, vp(0x10008), 32, fake, None, fake, None, None) == 1
+    assert lib.ep_stage(ctypes.byref(d), 1, fake, 32, None, None, fake, None, None) == 1
+    assert lib.ep_stage(ctypes.byref(Dom(8, 30, 1, 4)), 1, fake, 32, fake, None, fake, None,
+                        None) == 1
+    # nothing to copy: no instances, no spare slots, empty experts
+    assert lib.ep_stage(ctypes.byref(d), 0, None, 32, None, None, None, None, None) == 0
+    assert lib.ep_stage(ctypes.byref(Dom(8, 32, 0, 4)), 1, None, 32, None, None, None, None,
+                        None) == 0
+    assert lib.ep_stage(ctypes.byref(d), 1, None, 0, None, None, None, None, None) == 0
