@@ -42,8 +42,8 @@ N_HIDDEN_BUFS = 2  # distinct hidden inputs, alternating by layer (each 1.07 GB 
 # DRAM traffic of one ep_permute launch on this workload, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid for the permute source
 # with this SHA-256; reported as null once the kernel source changes.
-NCU_PERMUTE = {"source_sha256": "cb27c3dd218eca9e59ee127f81b0e4b64e39933004071875696ed72eff51a59e",
-               "bytes_per_launch": 9197400000,
+NCU_PERMUTE = {"source_sha256": "beb6e863723470969d9ab37998812b1a7a254a7ab2b02339f8c2943e50ca16c0",
+               "bytes_per_launch": 9190001600,
                "capture": "profiles/permute_kernel_qwen3-235b-like_T16384.md (x8 tokens)"}
 
 
