@@ -53,6 +53,8 @@ def _load(path):
     L.oracle_plan.restype = ctypes.c_int
     L.oracle_plan.argtypes = [i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                               ctypes.c_int32, i32p, i32p, i32p, i32p, i32p, i32p, i32p]
+    L.oracle_plan_skip.restype = ctypes.c_int
+    L.oracle_plan_skip.argtypes = L.oracle_plan.argtypes
     L.oracle_reroute.restype = None
     L.oracle_reroute.argtypes = [i32p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                  ctypes.c_int32, ctypes.c_int32, i32p, i32p, i32p, i32p,
@@ -93,8 +95,10 @@ def count(ids, R, E):
     return counts, counts_src, int(n_bad)
 
 
-def plan(counts, R, E, S, max_iters=PLAN_MAX_ITERS):
-    """counts: int32 [E].  Returns a dict with the plan outputs."""
+def plan(counts, R, E, S, max_iters=PLAN_MAX_ITERS, variant="base"):
+    """counts: int32 [E].  Returns a dict with the plan outputs.  variant:
+    "base" (the fixed rule) or "skip" (try the next candidate instead of
+    stopping)."""
     counts = _i32(counts)
     H = E // R
     P = R * (H + S)
@@ -105,7 +109,8 @@ def plan(counts, R, E, S, max_iters=PLAN_MAX_ITERS):
     inst_id = np.full(E + R * S, -1, np.int32)
     inst_cum = np.full(E + R * S, -1, np.int32)
     n_iter = ctypes.c_int32(0)
-    st = lib().oracle_plan(_p(counts, ctypes.c_int32), R, E, S, max_iters,
+    fn = {"base": lib().oracle_plan, "skip": lib().oracle_plan_skip}[variant]
+    st = fn(_p(counts, ctypes.c_int32), R, E, S, max_iters,
                            _p(quota, ctypes.c_int32), _p(slot_expert, ctypes.c_int32),
                            _p(rank_load, ctypes.c_int32), _p(inst_ptr, ctypes.c_int32),
                            _p(inst_id, ctypes.c_int32), _p(inst_cum, ctypes.c_int32),

@@ -100,6 +100,36 @@ int64_t oracle_count(const int32_t *ids, int64_t T, int32_t k, int32_t R, int32_
  * inst_ptr[e+1]-1 list the home instance first, then the replicas in
  * ascending p (READING), with inst_cum the inclusive running sum of their
  * quotas.  Returns ORACLE_OK or ORACLE_ITER_LIMIT; *n_iter = moves made.     */
+/* The logical -> physical table of a finished plan: for every expert, its
+ * home instance first, then its replicas by ascending p, with the inclusive
+ * running sum of their quotas (the order reroute's quota-prefix rule uses). */
+static void build_instance_table(int32_t R, int32_t E, int32_t S, const int32_t *quota,
+                                 const int32_t *slot_expert, int32_t *inst_ptr,
+                                 int32_t *inst_id, int32_t *inst_cum)
+{
+    int32_t H = E / R, W = H + S, P = R * W;
+    int32_t m = 0;
+    for (int32_t e = 0; e < E; e++) {
+        int32_t cum = 0;
+        inst_ptr[e] = m;
+        int32_t home_p = (e / H) * W + (e % H);
+        cum += quota[home_p];
+        inst_id[m] = home_p;
+        inst_cum[m] = cum;
+        m++;
+        for (int32_t p = 0; p < P; p++) {
+            int32_t j = p % W;
+            if (j < H) continue;
+            if (slot_expert[(p / W) * S + (j - H)] != e) continue;
+            cum += quota[p];
+            inst_id[m] = p;
+            inst_cum[m] = cum;
+            m++;
+        }
+    }
+    inst_ptr[E] = m;
+}
+
 int oracle_plan(const int32_t *counts, int32_t R, int32_t E, int32_t S, int32_t max_iters,
                 int32_t *quota, int32_t *slot_expert, int32_t *rank_load,
                 int32_t *inst_ptr, int32_t *inst_id, int32_t *inst_cum, int32_t *n_iter)
@@ -180,28 +210,7 @@ int oracle_plan(const int32_t *counts, int32_t R, int32_t E, int32_t S, int32_t 
 
     for (int32_t r = 0; r < R; r++) rank_load[r] = (int32_t)L[r];
 
-    /* logical -> physical table: home first, then replicas by ascending p */
-    int32_t m = 0;
-    for (int32_t e = 0; e < E; e++) {
-        int32_t cum = 0;
-        inst_ptr[e] = m;
-        int32_t home_p = (e / H) * W + (e % H);
-        cum += quota[home_p];
-        inst_id[m] = home_p;
-        inst_cum[m] = cum;
-        m++;
-        for (int32_t p = 0; p < P; p++) {
-            int32_t j = p % W;
-            if (j < H) continue;
-            if (slot_expert[(p / W) * S + (j - H)] != e) continue;
-            cum += quota[p];
-            inst_id[m] = p;
-            inst_cum[m] = cum;
-            m++;
-        }
-    }
-    inst_ptr[E] = m;
-
+    build_instance_table(R, E, S, quota, slot_expert, inst_ptr, inst_id, inst_cum);
     *n_iter = moves;
     free(L);
     return status;
@@ -358,4 +367,120 @@ void oracle_stage(const uint8_t *expert_w, int32_t E, int64_t expert_bytes,
         memcpy(slot_w + x * expert_bytes, expert_w + (int64_t)e * expert_bytes, (size_t)expert_bytes);
         (*n_copied)++;
     }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Planner variant "skip" (a variant of the step-2 rule; the pages leave the
+ * rule open).  The base rule stops as soon as the hottest rank's largest
+ * instance cannot move.  This variant tries the candidates in order and makes
+ * the first move that is possible:
+ *   hot candidates: ranks by load, highest first (lowest rank on ties);
+ *   for each, its instances with quota >= 1 by quota, largest first (lowest
+ *   expert id on ties);
+ *   candidate (h, instance of e) is possible when some rank c != h holds e or
+ *   has a free spare slot and, with cold the least-loaded such rank (lowest
+ *   index on ties), q = min(quota, floor((L[h] - L[cold]) / 2)) >= 1.
+ * The move is the base rule's (cold's instance of e, its lowest free slot if
+ * it does not hold e).  It stops when no candidate is possible, or with
+ * ORACLE_ITER_LIMIT when max_iters moves were made and another is possible.
+ * Every move lowers sum L^2 (q <= (L[h] - L[cold]) / 2), so it ends; while
+ * the base rule's candidate is possible both rules make the same move, so
+ * this plan is the base plan followed by further moves, none of which raises
+ * the maximum load (a move from h to cold leaves both below the old L[h]). */
+int oracle_plan_skip(const int32_t *counts, int32_t R, int32_t E, int32_t S,
+                     int32_t max_iters, int32_t *quota, int32_t *slot_expert,
+                     int32_t *rank_load, int32_t *inst_ptr, int32_t *inst_id,
+                     int32_t *inst_cum, int32_t *n_iter)
+{
+    int32_t H = E / R;
+    int32_t W = H + S;
+    int32_t P = R * W;
+    int64_t *L = (int64_t *)calloc((size_t)R, sizeof(int64_t));
+    char *rank_tried = (char *)calloc((size_t)R, 1);
+    char *inst_tried = (char *)calloc((size_t)W, 1);
+    int status = ORACLE_OK;
+    int32_t moves = 0;
+
+    for (int32_t p = 0; p < P; p++) quota[p] = 0;
+    for (int32_t x = 0; x < R * S; x++) slot_expert[x] = -1;
+    for (int32_t e = 0; e < E; e++) {
+        quota[(e / H) * W + (e % H)] = counts[e];
+        L[e / H] += counts[e];
+    }
+
+    for (;;) {
+        int found = 0;
+        int32_t hot = -1, src_p = -1, src_e = -1, cold = -1;
+        int64_t q = 0;
+        memset(rank_tried, 0, (size_t)R);
+        for (int32_t n = 0; n < R && !found; n++) {
+            /* next hot candidate: highest load among ranks not tried yet */
+            hot = -1;
+            for (int32_t r = 0; r < R; r++)
+                if (!rank_tried[r] && (hot < 0 || L[r] > L[hot])) hot = r;
+            rank_tried[hot] = 1;
+            memset(inst_tried, 0, (size_t)W);
+            for (int32_t nj = 0; nj < W && !found; nj++) {
+                /* next instance of hot: largest quota >= 1 not tried yet */
+                src_p = -1;
+                src_e = -1;
+                int32_t src_j = -1;
+                for (int32_t j = 0; j < W; j++) {
+                    int32_t p = hot * W + j;
+                    int32_t e = (j < H) ? hot * H + j : slot_expert[hot * S + (j - H)];
+                    if (e < 0 || inst_tried[j] || quota[p] < 1) continue;
+                    if (src_p < 0 || quota[p] > quota[src_p] ||
+                        (quota[p] == quota[src_p] && e < src_e)) {
+                        src_p = p;
+                        src_e = e;
+                        src_j = j;
+                    }
+                }
+                if (src_p < 0) break;                 /* hot has nothing left to try */
+                inst_tried[src_j] = 1;
+                /* coldest rank that holds src_e or has a free slot */
+                cold = -1;
+                for (int32_t c = 0; c < R; c++) {
+                    if (c == hot) continue;
+                    int holds = (src_e / H == c);
+                    int has_free = 0;
+                    for (int32_t j = 0; j < S; j++) {
+                        if (slot_expert[c * S + j] == src_e) holds = 1;
+                        if (slot_expert[c * S + j] < 0) has_free = 1;
+                    }
+                    if (!(holds || has_free)) continue;
+                    if (cold < 0 || L[c] < L[cold]) cold = c;
+                }
+                if (cold < 0) continue;
+                int64_t half = (L[hot] - L[cold]) / 2;
+                q = quota[src_p] < half ? quota[src_p] : half;
+                if (q >= 1) found = 1;
+            }
+        }
+        if (!found) break;
+        if (moves == max_iters) { status = ORACLE_ITER_LIMIT; break; }
+
+        int32_t dst_p = -1;
+        if (src_e / H == cold) dst_p = cold * W + (src_e % H);
+        for (int32_t j = 0; j < S && dst_p < 0; j++)
+            if (slot_expert[cold * S + j] == src_e) dst_p = cold * W + H + j;
+        for (int32_t j = 0; j < S && dst_p < 0; j++)
+            if (slot_expert[cold * S + j] < 0) {
+                slot_expert[cold * S + j] = src_e;
+                dst_p = cold * W + H + j;
+            }
+        quota[src_p] -= (int32_t)q;
+        quota[dst_p] += (int32_t)q;
+        L[hot] -= q;
+        L[cold] += q;
+        moves++;
+    }
+
+    for (int32_t r = 0; r < R; r++) rank_load[r] = (int32_t)L[r];
+    build_instance_table(R, E, S, quota, slot_expert, inst_ptr, inst_id, inst_cum);
+    *n_iter = moves;
+    free(L);
+    free(rank_tried);
+    free(inst_tried);
+    return status;
 }

@@ -10,6 +10,7 @@ import pytest
 import oracle
 import test_oracle_combine as combine_pins
 import test_oracle_pins as pins
+import test_oracle_plan_skip as skip_pins
 import test_oracle_stage as stage_pins
 from golden_io import read_sections
 
@@ -58,6 +59,16 @@ MUTANTS = {
     "combine reads row 0 for missing slots": ("if (row < 0) continue;", "if (row < 0) row = 0;"),
     "combine accumulates in double": ("float sum = 0.0f;", "double sum = 0.0;"),
     "combine multiplies after the sum": ("sum = sum + prod;", "sum = sum + x;"),
+    "skip tries the coldest rank first": (
+        "if (!rank_tried[r] && (hot < 0 || L[r] > L[hot])) hot = r;",
+        "if (!rank_tried[r] && (hot < 0 || L[r] < L[hot])) hot = r;"),
+    "skip gives up after the hottest rank": ("for (int32_t n = 0; n < R && !found; n++) {",
+                                             "for (int32_t n = 0; n < 1 && !found; n++) {"),
+    "skip gives up after one instance": ("for (int32_t nj = 0; nj < W && !found; nj++) {",
+                                         "for (int32_t nj = 0; nj < 1 && !found; nj++) {"),
+    "skip tries the smallest instance first": (
+        "if (src_p < 0 || quota[p] > quota[src_p] ||\n                        (quota[p] == quota[src_p] && e < src_e)) {",
+        "if (src_p < 0 || quota[p] < quota[src_p] ||\n                        (quota[p] == quota[src_p] && e < src_e)) {"),
     "stage ignores what a slot holds": ("if (prev != NULL && prev[x] == e) continue;",
                                         "if (prev != NULL && prev[x] == e + E) continue;"),
     "stage clears empty slots": (
@@ -92,6 +103,10 @@ def battery():
                  "test_rows_follow_dst_row_per_token"):
         getattr(combine_pins, name)()
     combine_pins.test_k1_unit_weight_is_the_identity(0)
+    for name in sorted(skip_pins.SKIP):
+        skip_pins.test_skip_hand_examples(name)
+    for seed in range(8):
+        skip_pins.test_skip_prefix_stop_and_bounds(seed)
     stage_pins.test_stage_is_a_gather_of_expert_rows()
     stage_pins.test_empty_invalid_and_unchanged_slots_are_left_alone()
 
@@ -104,9 +119,11 @@ def test_battery_passes_on_the_oracle():
 def test_planted_mistake_is_caught(name, tmp_path):
     old, new = MUTANTS[name]
     src = open(SRC).read()
-    assert src.count(old) == 1, "mutation site not found exactly once"
+    # the first occurrence is the one in the function the mutant names (the
+    # skip variant repeats some lines of the base rule further down the file)
+    assert src.count(old) >= 1, "mutation site not found"
     mutated = tmp_path / "mutant.c"
-    mutated.write_text(src.replace(old, new))
+    mutated.write_text(src.replace(old, new, 1))
     so = tmp_path / "libmutant.so"
     subprocess.run(["gcc", "-O1", "-std=c11", "-ffp-contract=off", "-shared", "-fPIC",
                     str(mutated), "-o", str(so)], check=True)

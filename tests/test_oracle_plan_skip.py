@@ -1,0 +1,103 @@
+"""Pins of the oracle's planner variant "skip" (try the next candidate instead
+of a global stop): hand-worked examples, the prefix property (the base rule's
+moves come first), the stop condition checked from outside, the invariants
+every plan has, and its quality bounds (lower bound <= brute-force optimum <=
+skip's max load <= the base rule's max load).  No GPU needed."""
+import numpy as np
+import pytest
+
+import oracle
+from golden_io import read_sections, as_array
+from plan_checks import instance_expert
+
+SKIP = read_sections("plan_skip_examples.txt")
+
+
+@pytest.mark.parametrize("name", sorted(SKIP))
+def test_skip_hand_examples(name):
+    ex = SKIP[name]
+    variant = "base" if name.endswith("_base_rule") else "skip"
+    pl = oracle.plan(as_array(ex["counts"]), ex["R"], ex["E"], ex["S"], max_iters=ex["max_iters"],
+                     variant=variant)
+    for key in ("quota", "rank_load", "inst_ptr"):
+        assert np.array_equal(pl[key], as_array(ex[key])), key
+    assert np.array_equal(pl["slot_expert"].reshape(-1), as_array(ex["slot_expert"]))
+    m = int(as_array(ex["inst_ptr"])[-1])
+    assert np.array_equal(pl["inst_id"][:m], as_array(ex["inst_id"]))
+    assert np.array_equal(pl["inst_cum"][:m], as_array(ex["inst_cum"]))
+    assert pl["n_iter"] == ex["n_iter"] and pl["status"] == ex["status"]
+
+
+def _random_counts(rng):
+    R = int(rng.choice([2, 3, 4, 8, 16]))
+    H = int(rng.choice([1, 2, 4]))
+    S = int(rng.choice([0, 1, 2]))
+    E = R * H
+    if rng.random() < 0.5:
+        c = rng.integers(0, 40, size=E)
+    else:
+        c = (200.0 / (1 + rng.permutation(E)) ** rng.uniform(0.6, 1.6)).astype(np.int64)
+    return R, E, S, c.astype(np.int32)
+
+
+def _possible_moves(counts, R, E, S, pl):
+    """every (h, p, cold, q >= 1) the skip rule's candidate test accepts"""
+    H, W = E // R, E // R + S
+    ex = instance_expert(E, R, S, pl["slot_expert"])
+    q = pl["quota"]
+    L = pl["rank_load"].astype(np.int64)
+    free = [(ex[c * W + H:(c + 1) * W] < 0).any() for c in range(R)]
+    out = []
+    for h in range(R):
+        for p in range(h * W, (h + 1) * W):
+            e = ex[p]
+            if e < 0 or q[p] < 1:
+                continue
+            elig = [c for c in range(R) if c != h and (free[c] or (ex[c * W:(c + 1) * W] == e).any())]
+            if not elig:
+                continue
+            cold = min(elig, key=lambda c: (L[c], c))
+            m = min(int(q[p]), int((L[h] - L[cold]) // 2))
+            if m >= 1:
+                out.append((h, p, cold, m))
+    return out
+
+
+@pytest.mark.parametrize("seed", range(30))
+def test_skip_prefix_stop_and_bounds(seed):
+    rng = np.random.default_rng(seed)
+    R, E, S, c = _random_counts(rng)
+    base = oracle.plan(c, R, E, S)
+    skip = oracle.plan(c, R, E, S, variant="skip")
+    assert skip["status"] == 0 and base["status"] == 0
+    # prefix: capped at the base rule's move count, skip is in the base rule's state
+    capped = oracle.plan(c, R, E, S, max_iters=base["n_iter"], variant="skip")
+    for key in ("quota", "slot_expert", "rank_load", "inst_ptr"):
+        assert np.array_equal(capped[key], base[key]), key
+    assert skip["n_iter"] >= base["n_iter"]
+    assert capped["status"] == (2 if skip["n_iter"] > base["n_iter"] else 0)
+    # stop condition: at the end no candidate can move
+    assert _possible_moves(c, R, E, S, skip) == []
+    # conservation, loads, and the bounds
+    H, W = E // R, E // R + S
+    ex = instance_expert(E, R, S, skip["slot_expert"])
+    for e in range(E):
+        assert skip["quota"][ex == e].sum() == c[e]
+    assert (skip["quota"] >= 0).all()
+    assert np.array_equal(skip["rank_load"], skip["quota"].reshape(R, W).sum(1))
+    assert skip["rank_load"].max() <= base["rank_load"].max()
+    from moe_expert_load_id_b300 import quality as Q
+    assert Q.lower_bound(c.astype(np.int64), R, S) <= skip["rank_load"].max()
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_skip_against_brute_force(seed):
+    from oracle import bruteforce
+    rng = np.random.default_rng(100 + seed)
+    R, H, S = int(rng.integers(2, 4)), int(rng.integers(1, 3)), 1
+    E = R * H
+    c = rng.integers(0, 9, size=E).astype(np.int32)
+    opt = bruteforce.optimum(c, R, S)
+    skip = oracle.plan(c, R, E, S, variant="skip")
+    base = oracle.plan(c, R, E, S)
+    assert opt <= skip["rank_load"].max() <= base["rank_load"].max()
