@@ -53,8 +53,10 @@ def _load(path):
     L.oracle_plan.restype = ctypes.c_int
     L.oracle_plan.argtypes = [i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
                               ctypes.c_int32, i32p, i32p, i32p, i32p, i32p, i32p, i32p]
-    L.oracle_plan_skip.restype = ctypes.c_int
-    L.oracle_plan_skip.argtypes = L.oracle_plan.argtypes
+    L.oracle_plan_variant.restype = ctypes.c_int
+    L.oracle_plan_variant.argtypes = [i32p, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                                      ctypes.c_int32, ctypes.c_int32, i32p, i32p, i32p, i32p,
+                                      i32p, i32p, i32p]
     L.oracle_reroute.restype = None
     L.oracle_reroute.argtypes = [i32p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                  ctypes.c_int32, ctypes.c_int32, i32p, i32p, i32p, i32p,
@@ -95,10 +97,15 @@ def count(ids, R, E):
     return counts, counts_src, int(n_bad)
 
 
+# planner variants: None = the base rule's own function; otherwise the flags of
+# oracle_plan_variant (1: try the next candidate instead of stopping, 2: release
+# replica slots whose quota reaches 0)
+PLAN_VARIANTS = {"base": None, "base_flags": 0, "skip": 1, "release": 2, "skip+release": 3}
+
+
 def plan(counts, R, E, S, max_iters=PLAN_MAX_ITERS, variant="base"):
-    """counts: int32 [E].  Returns a dict with the plan outputs.  variant:
-    "base" (the fixed rule) or "skip" (try the next candidate instead of
-    stopping)."""
+    """counts: int32 [E].  Returns a dict with the plan outputs.  variant: a key
+    of PLAN_VARIANTS."""
     counts = _i32(counts)
     H = E // R
     P = R * (H + S)
@@ -109,8 +116,14 @@ def plan(counts, R, E, S, max_iters=PLAN_MAX_ITERS, variant="base"):
     inst_id = np.full(E + R * S, -1, np.int32)
     inst_cum = np.full(E + R * S, -1, np.int32)
     n_iter = ctypes.c_int32(0)
-    fn = {"base": lib().oracle_plan, "skip": lib().oracle_plan_skip}[variant]
-    st = fn(_p(counts, ctypes.c_int32), R, E, S, max_iters,
+    flags = PLAN_VARIANTS[variant]
+    if flags is None:
+        fn = lib().oracle_plan
+        args = (_p(counts, ctypes.c_int32), R, E, S, max_iters)
+    else:
+        fn = lib().oracle_plan_variant
+        args = (_p(counts, ctypes.c_int32), R, E, S, max_iters, flags)
+    st = fn(*args,
                            _p(quota, ctypes.c_int32), _p(slot_expert, ctypes.c_int32),
                            _p(rank_load, ctypes.c_int32), _p(inst_ptr, ctypes.c_int32),
                            _p(inst_id, ctypes.c_int32), _p(inst_cum, ctypes.c_int32),

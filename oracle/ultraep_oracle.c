@@ -370,27 +370,34 @@ void oracle_stage(const uint8_t *expert_w, int32_t E, int64_t expert_bytes,
 }
 
 /* ------------------------------------------------------------------------ */
-/* Planner variant "skip" (a variant of the step-2 rule; the pages leave the
- * rule open).  The base rule stops as soon as the hottest rank's largest
- * instance cannot move.  This variant tries the candidates in order and makes
- * the first move that is possible:
- *   hot candidates: ranks by load, highest first (lowest rank on ties);
- *   for each, its instances with quota >= 1 by quota, largest first (lowest
- *   expert id on ties);
- *   candidate (h, instance of e) is possible when some rank c != h holds e or
- *   has a free spare slot and, with cold the least-loaded such rank (lowest
- *   index on ties), q = min(quota, floor((L[h] - L[cold]) / 2)) >= 1.
+/* Planner variants (variants of the step-2 rule; the pages leave the rule
+ * open).  flags:
+ *   ORACLE_PLAN_SKIP: the base rule stops as soon as the hottest rank's
+ *   largest instance cannot move; this variant tries the candidates in order
+ *   and makes the first move that is possible:
+ *     hot candidates: ranks by load, highest first (lowest rank on ties);
+ *     for each, its instances with quota >= 1 by quota, largest first (lowest
+ *     expert id on ties);
+ *     candidate (h, instance of e) is possible when some rank c != h holds e
+ *     or has a free spare slot and, with cold the least-loaded such rank
+ *     (lowest index on ties), q = min(quota, floor((L[h] - L[cold]) / 2)) >= 1.
+ *   ORACLE_PLAN_RELEASE: a replica (spare-slot instance) whose quota a move
+ *   takes to 0 is released: the slot becomes empty (-1) and its rank no longer
+ *   holds the expert, so later moves may fill it.
+ * Without SKIP only the first candidate is tried (the base rule's choice).
  * The move is the base rule's (cold's instance of e, its lowest free slot if
  * it does not hold e).  It stops when no candidate is possible, or with
  * ORACLE_ITER_LIMIT when max_iters moves were made and another is possible.
- * Every move lowers sum L^2 (q <= (L[h] - L[cold]) / 2), so it ends; while
- * the base rule's candidate is possible both rules make the same move, so
- * this plan is the base plan followed by further moves, none of which raises
+ * Every move lowers sum L^2 (q <= (L[h] - L[cold]) / 2), so it ends.  With
+ * SKIP, while the base rule's candidate is possible both make the same move,
+ * so the plan is the base plan followed by further moves, none of which raises
  * the maximum load (a move from h to cold leaves both below the old L[h]). */
-int oracle_plan_skip(const int32_t *counts, int32_t R, int32_t E, int32_t S,
-                     int32_t max_iters, int32_t *quota, int32_t *slot_expert,
-                     int32_t *rank_load, int32_t *inst_ptr, int32_t *inst_id,
-                     int32_t *inst_cum, int32_t *n_iter)
+#define ORACLE_PLAN_SKIP 1
+#define ORACLE_PLAN_RELEASE 2
+int oracle_plan_variant(const int32_t *counts, int32_t R, int32_t E, int32_t S,
+                        int32_t max_iters, int32_t flags, int32_t *quota, int32_t *slot_expert,
+                        int32_t *rank_load, int32_t *inst_ptr, int32_t *inst_id,
+                        int32_t *inst_cum, int32_t *n_iter)
 {
     int32_t H = E / R;
     int32_t W = H + S;
@@ -413,14 +420,16 @@ int oracle_plan_skip(const int32_t *counts, int32_t R, int32_t E, int32_t S,
         int32_t hot = -1, src_p = -1, src_e = -1, cold = -1;
         int64_t q = 0;
         memset(rank_tried, 0, (size_t)R);
-        for (int32_t n = 0; n < R && !found; n++) {
+        int32_t n_ranks = (flags & ORACLE_PLAN_SKIP) ? R : 1;
+        int32_t n_insts = (flags & ORACLE_PLAN_SKIP) ? W : 1;
+        for (int32_t n = 0; n < n_ranks && !found; n++) {
             /* next hot candidate: highest load among ranks not tried yet */
             hot = -1;
             for (int32_t r = 0; r < R; r++)
                 if (!rank_tried[r] && (hot < 0 || L[r] > L[hot])) hot = r;
             rank_tried[hot] = 1;
             memset(inst_tried, 0, (size_t)W);
-            for (int32_t nj = 0; nj < W && !found; nj++) {
+            for (int32_t nj = 0; nj < n_insts && !found; nj++) {
                 /* next instance of hot: largest quota >= 1 not tried yet */
                 src_p = -1;
                 src_e = -1;
@@ -473,6 +482,8 @@ int oracle_plan_skip(const int32_t *counts, int32_t R, int32_t E, int32_t S,
         quota[dst_p] += (int32_t)q;
         L[hot] -= q;
         L[cold] += q;
+        if ((flags & ORACLE_PLAN_RELEASE) && src_p % W >= H && quota[src_p] == 0)
+            slot_expert[hot * S + (src_p % W - H)] = -1;
         moves++;
     }
 

@@ -10,7 +10,7 @@ import pytest
 import oracle
 import test_oracle_combine as combine_pins
 import test_oracle_pins as pins
-import test_oracle_plan_skip as skip_pins
+import test_oracle_plan_variants as skip_pins
 import test_oracle_stage as stage_pins
 from golden_io import read_sections
 
@@ -62,13 +62,18 @@ MUTANTS = {
     "skip tries the coldest rank first": (
         "if (!rank_tried[r] && (hot < 0 || L[r] > L[hot])) hot = r;",
         "if (!rank_tried[r] && (hot < 0 || L[r] < L[hot])) hot = r;"),
-    "skip gives up after the hottest rank": ("for (int32_t n = 0; n < R && !found; n++) {",
-                                             "for (int32_t n = 0; n < 1 && !found; n++) {"),
-    "skip gives up after one instance": ("for (int32_t nj = 0; nj < W && !found; nj++) {",
-                                         "for (int32_t nj = 0; nj < 1 && !found; nj++) {"),
+    "skip gives up after the hottest rank": ("int32_t n_ranks = (flags & ORACLE_PLAN_SKIP) ? R : 1;",
+                                             "int32_t n_ranks = (flags & ORACLE_PLAN_SKIP) ? 1 : 1;"),
+    "skip gives up after one instance": ("int32_t n_insts = (flags & ORACLE_PLAN_SKIP) ? W : 1;",
+                                         "int32_t n_insts = (flags & ORACLE_PLAN_SKIP) ? 1 : 1;"),
     "skip tries the smallest instance first": (
         "if (src_p < 0 || quota[p] > quota[src_p] ||\n                        (quota[p] == quota[src_p] && e < src_e)) {",
         "if (src_p < 0 || quota[p] < quota[src_p] ||\n                        (quota[p] == quota[src_p] && e < src_e)) {"),
+    "release never frees a slot": ("if ((flags & ORACLE_PLAN_RELEASE) && src_p % W >= H && quota[src_p] == 0)",
+                                   "if ((flags & ORACLE_PLAN_RELEASE) && src_p % W >= H && quota[src_p] < 0)"),
+    "release frees replicas that still hold quota": (
+        "if ((flags & ORACLE_PLAN_RELEASE) && src_p % W >= H && quota[src_p] == 0)",
+        "if ((flags & ORACLE_PLAN_RELEASE) && src_p % W >= H && quota[src_p] >= 0)"),
     "stage ignores what a slot holds": ("if (prev != NULL && prev[x] == e) continue;",
                                         "if (prev != NULL && prev[x] == e + E) continue;"),
     "stage clears empty slots": (
@@ -106,7 +111,8 @@ def battery():
     for name in sorted(skip_pins.SKIP):
         skip_pins.test_skip_hand_examples(name)
     for seed in range(8):
-        skip_pins.test_skip_prefix_stop_and_bounds(seed)
+        skip_pins.test_skip_prefix_stop_and_bounds(seed, "skip")
+        skip_pins.test_skip_prefix_stop_and_bounds(seed, "skip+release")
     stage_pins.test_stage_is_a_gather_of_expert_rows()
     stage_pins.test_empty_invalid_and_unchanged_slots_are_left_alone()
 

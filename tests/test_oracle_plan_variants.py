@@ -1,8 +1,10 @@
-"""Pins of the oracle's planner variant "skip" (try the next candidate instead
-of a global stop): hand-worked examples, the prefix property (the base rule's
-moves come first), the stop condition checked from outside, the invariants
-every plan has, and its quality bounds (lower bound <= brute-force optimum <=
-skip's max load <= the base rule's max load).  No GPU needed."""
+"""Pins of the oracle's planner variants: "skip" (try the next candidate
+instead of a global stop) and "release" (free a replica slot whose quota
+reaches 0): hand-worked examples, the flag-free variant function against the
+base rule's own, the prefix property (the base rule's moves come first), the
+stop condition checked from outside, the invariants every plan has, no empty
+replica under release, and the quality bounds (lower bound <= brute-force
+optimum <= skip's max load <= the base rule's max load).  No GPU needed."""
 import numpy as np
 import pytest
 
@@ -13,10 +15,16 @@ from plan_checks import instance_expert
 SKIP = read_sections("plan_skip_examples.txt")
 
 
+def _variant_of(name):
+    if name.endswith("_base_rule"):
+        return "base"
+    return "skip+release" if name.endswith("_skip_release") else "skip"
+
+
 @pytest.mark.parametrize("name", sorted(SKIP))
 def test_skip_hand_examples(name):
     ex = SKIP[name]
-    variant = "base" if name.endswith("_base_rule") else "skip"
+    variant = _variant_of(name)
     pl = oracle.plan(as_array(ex["counts"]), ex["R"], ex["E"], ex["S"], max_iters=ex["max_iters"],
                      variant=variant)
     for key in ("quota", "rank_load", "inst_ptr"):
@@ -63,15 +71,27 @@ def _possible_moves(counts, R, E, S, pl):
     return out
 
 
+@pytest.mark.parametrize("seed", range(20))
+def test_variant_function_without_flags_is_the_base_rule(seed):
+    rng = np.random.default_rng(500 + seed)
+    R, E, S, c = _random_counts(rng)
+    a = oracle.plan(c, R, E, S)
+    b = oracle.plan(c, R, E, S, variant="base_flags")
+    for key in ("quota", "slot_expert", "rank_load", "inst_ptr", "inst_id", "inst_cum",
+                "n_iter", "status"):
+        assert np.array_equal(a[key], b[key]), key
+
+
+@pytest.mark.parametrize("variant", ["skip", "skip+release"])
 @pytest.mark.parametrize("seed", range(30))
-def test_skip_prefix_stop_and_bounds(seed):
+def test_skip_prefix_stop_and_bounds(seed, variant):
     rng = np.random.default_rng(seed)
     R, E, S, c = _random_counts(rng)
     base = oracle.plan(c, R, E, S)
-    skip = oracle.plan(c, R, E, S, variant="skip")
+    skip = oracle.plan(c, R, E, S, variant=variant)
     assert skip["status"] == 0 and base["status"] == 0
     # prefix: capped at the base rule's move count, skip is in the base rule's state
-    capped = oracle.plan(c, R, E, S, max_iters=base["n_iter"], variant="skip")
+    capped = oracle.plan(c, R, E, S, max_iters=base["n_iter"], variant=variant)
     for key in ("quota", "slot_expert", "rank_load", "inst_ptr"):
         assert np.array_equal(capped[key], base[key]), key
     assert skip["n_iter"] >= base["n_iter"]
@@ -84,6 +104,9 @@ def test_skip_prefix_stop_and_bounds(seed):
     for e in range(E):
         assert skip["quota"][ex == e].sum() == c[e]
     assert (skip["quota"] >= 0).all()
+    if variant == "skip+release":                       # no replica is left empty
+        spare = skip["quota"].reshape(R, W)[:, H:].reshape(-1)
+        assert (spare[skip["slot_expert"].reshape(-1) >= 0] > 0).all()
     assert np.array_equal(skip["rank_load"], skip["quota"].reshape(R, W).sum(1))
     assert skip["rank_load"].max() <= base["rank_load"].max()
     from moe_expert_load_id_b300 import quality as Q
@@ -101,3 +124,21 @@ def test_skip_against_brute_force(seed):
     skip = oracle.plan(c, R, E, S, variant="skip")
     base = oracle.plan(c, R, E, S)
     assert opt <= skip["rank_load"].max() <= base["rank_load"].max()
+
+
+def test_base_rule_never_empties_a_replica():
+    # under the base rule (a replica is created holding half a gap, and loads only
+    # converge afterwards) no replica's quota was seen to reach 0 on 3000 random
+    # instances, so "release" changes nothing there; under "skip" it can
+    # (release_ex2 above)
+    rng = np.random.default_rng(2024)
+    for _ in range(3000):
+        R, E, S, c = _random_counts(rng)
+        if S == 0:
+            continue
+        for variant in ("base", "release"):
+            pl = oracle.plan(c, R, E, S, variant=variant)
+            H, W = E // R, E // R + S
+            spare = pl["quota"].reshape(R, W)[:, H:].reshape(-1)
+            filled = pl["slot_expert"].reshape(-1) >= 0
+            assert (spare[filled] > 0).all()
