@@ -377,6 +377,21 @@ def quality_report(U, w, ids, pipe, microbatch, device):
            "before": Q.summarize(before_r), "ultraep_rule": Q.summarize(after_r),
            "lower_bound": Q.summarize(lb_r),
            "plan_n_iter": Q.summarize(pipe.n_iter.cpu().numpy())}
+    # the planner variants (ep_plan_ex) on the same counts, all layers in one launch
+    vb = U.Buffers(dom, 1, w.layers, device=device)
+    vb.counts.copy_(pipe.counts)
+    for name, flags in (("skip", U.EP_PLAN_SKIP),
+                        ("skip_release", U.EP_PLAN_SKIP | U.EP_PLAN_RELEASE)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        vb.plan(flags=flags)
+        e0.record()
+        vb.plan(flags=flags)
+        e1.record()
+        torch.cuda.synchronize(device)
+        loads = vb.rank_load.cpu().numpy()
+        rep[f"variant_{name}"] = Q.summarize([Q.imbalance(loads[l]) for l in range(w.layers)])
+        rep[f"variant_{name}_n_iter"] = Q.summarize(vb.n_iter.cpu().numpy())
+        rep[f"variant_{name}_us_batched"] = round(e0.elapsed_time(e1) * 1000.0, 2)
     if hist:
         rep["eplb_style_history_W1"] = Q.summarize(e1_r)
         rep[f"eplb_style_history_W{len(hist)}"] = Q.summarize(ea_r)

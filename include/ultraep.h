@@ -174,6 +174,27 @@ ep_status_t ep_plan(const ep_domain_t *dom, const int32_t *counts, int32_t n_ins
                     int32_t *n_iter, int32_t *inst_status, void *stream);
 
 /*
+ * ep_plan_ex -- ep_plan with variants of the rule (the pages leave the rule
+ * open; these are the variants this library compares with it).  flags:
+ *   EP_PLAN_SKIP: when the hottest rank's largest instance cannot move, try
+ *     its next instances and then the next-hottest ranks (ranks by load,
+ *     highest first; instances with quota >= 1 by quota, largest first; the
+ *     base rule's ties) and make the first move that can be made; stop when
+ *     none can.  The plan is the base plan followed by further moves, none of
+ *     which raises the maximum load.
+ *   EP_PLAN_RELEASE: a spare-slot instance that a move leaves at quota 0 frees
+ *     its slot (slot_expert -1; the rank no longer holds the expert).
+ * flags = 0 is ep_plan.  Other bits: EP_ERR_INVAL.  Arguments otherwise as
+ * ep_plan.
+ */
+#define EP_PLAN_SKIP 1
+#define EP_PLAN_RELEASE 2
+ep_status_t ep_plan_ex(const ep_domain_t *dom, const int32_t *counts, int32_t n_inst,
+                       int32_t max_iters, int32_t flags, int32_t *quota, int32_t *slot_expert,
+                       int32_t *rank_load, int32_t *inst_ptr, int32_t *inst_id,
+                       int32_t *inst_cum, int32_t *n_iter, int32_t *inst_status, void *stream);
+
+/*
  * ep_reroute -- split every logical expert's slots among its instances
  * (UltraEP article, "key design", forward-pass paragraph: reroute divides the
  * tokens of one logical expert among its replicas; EPLB tutorial, dispatch:

@@ -6,7 +6,7 @@ seeded synthetic inputs and ``quality`` holds the host-side plan-quality
 metrics.  The binding's names are re-exported lazily so that importing the
 workload or quality helpers does not need the compiled library.
 """
-_BINDING_NAMES = ("ep_count", "ep_plan", "ep_reroute", "ep_balance", "ep_permute", "ep_unpermute",
+_BINDING_NAMES = ("ep_count", "ep_plan", "ep_plan_ex", "ep_reroute", "ep_balance", "ep_permute", "ep_unpermute",
                   "ep_combine", "ep_stage",
                   "ep_count_workspace_bytes", "ep_status_str", "Domain", "EpError")
 

@@ -54,7 +54,7 @@ cudaError_t launch_count_noalloc(const ep_domain_t& d, const int32_t* ids, int64
 
 // plan
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
-                        int32_t max_iters, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
+                        int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
                         int32_t* inst_ptr, int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter,
                         int32_t* inst_status, cudaStream_t s, bool pdl = false);
 

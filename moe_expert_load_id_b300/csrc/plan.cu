@@ -49,10 +49,10 @@ template <int WB>
 struct RankRegs {
     int q[WB];
     int x[WB];
-    int load;   // -1: the rank does not exist
-    int used;   // filled spare slots
-    int bq;     // largest quota among its instances
-    int bx;     // that instance: expert << 5 | j (lowest expert on ties)
+    int load;      // -1: the rank does not exist
+    unsigned occ;  // bit s: spare slot s holds an expert
+    int bq;        // largest quota among its instances
+    int bx;        // that instance: expert << 5 | j (lowest expert on ties)
 
     __device__ __forceinline__ void best(int W) {
         bq = -1;
@@ -65,24 +65,47 @@ struct RankRegs {
             bx = take ? cx : bx;
         }
     }
+    // the largest instance with quota >= 1 whose local index is not in excl
+    // (the skip variant's next candidate); bq = -1 when there is none
+    __device__ __forceinline__ void best_excl(int W, unsigned excl, int& cq, int& cxo) const {
+        cq = -1;
+        cxo = INT_MAX;
+#pragma unroll
+        for (int j = 0; j < WB; ++j) {
+            const int cx = (x[j] << 5) | j;
+            const bool ok = j < W && x[j] >= 0 && q[j] >= 1 && !((excl >> j) & 1u);
+            const bool take = ok && (q[j] > cq || (q[j] == cq && cx < cxo));
+            cq = take ? q[j] : cq;
+            cxo = take ? cx : cxo;
+        }
+    }
     __device__ __forceinline__ bool holds(int e) const {
         bool h = false;
 #pragma unroll
         for (int j = 0; j < WB; ++j) h |= (x[j] == e);
         return h;
     }
+    __device__ __forceinline__ bool has_free(int S) const {
+        return occ != ((S >= 32) ? ~0u : ((1u << S) - 1u));
+    }
     // (the rank's load is updated by the move loop itself, ahead of these)
-    // hot side: the owner lane (mine) removes mv from its instance j
-    __device__ __forceinline__ void take(int j, bool mine, int mv) {
+    // hot side: the owner lane (mine) removes mv from its instance j; with
+    // release, a spare-slot instance left at quota 0 frees its slot
+    __device__ __forceinline__ void take(int j, bool mine, int mv, int H, bool release) {
 #pragma unroll
-        for (int jj = 0; jj < WB; ++jj) q[jj] -= (mine && jj == j) ? mv : 0;
+        for (int jj = 0; jj < WB; ++jj) {
+            const bool from = mine && jj == j;
+            q[jj] -= from ? mv : 0;
+            const bool freed = release && from && jj >= H && q[jj] == 0;
+            x[jj] = freed ? -1 : x[jj];
+            occ &= freed ? ~(1u << (jj - H)) : ~0u;
+        }
     }
     // cold side: the owner lane adds mv to its instance of e, filling the
-    // lowest free spare slot (local index H + used) when it does not hold e
-    // yet.  Only one instance grew, so the largest instance is updated in
-    // place.
+    // lowest free spare slot when it does not hold e yet.  Only one instance
+    // grew, so the largest instance is updated in place.
     __device__ __forceinline__ void give(int e, bool held, bool mine, int H, int mv) {
-        const int jn = held ? -1 : H + used;
+        const int jn = held ? -1 : H + __ffs(~occ) - 1;
         int nq = 0, nj = 0;
 #pragma unroll
         for (int jj = 0; jj < WB; ++jj) {
@@ -92,7 +115,7 @@ struct RankRegs {
             nq = to ? q[jj] : nq;
             nj = to ? jj : nj;
         }
-        used += (mine && !held) ? 1 : 0;
+        occ |= (mine && !held) ? (1u << (jn - H)) : 0u;
         const int cx = (e << 5) | nj;
         const bool better = mine && (nq > bq || (nq == bq && cx < bx));
         bq = better ? nq : bq;
@@ -124,40 +147,37 @@ __device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB
 // The loop is software-pipelined: as soon as the amount is known the two
 // loads change and the next move's argmax is issued; the instance bookkeeping
 // of the current move (take, give, largest instance) overlaps it.
+// flags (warp-uniform): EP_PLAN_SKIP -- when the hottest rank's largest
+// instance cannot move, try its next instances, then the next-hottest ranks,
+// and make the first move that can be made; EP_PLAN_RELEASE -- a spare-slot
+// instance a move empties frees its slot.
 template <int WB, bool kTwo, bool kPacked>
 __device__ __forceinline__ void plan_moves(RankRegs<WB>& A, RankRegs<WB>& B, int lane, int H,
-                                           int S, int W, int max_iters, int& iters,
-                                           int& status) {
+                                           int S, int W, int R, int max_iters, int flags,
+                                           int& iters, int& status) {
     const bool hasA = A.load >= 0, hasB = kTwo && B.load >= 0;
     const int ra = lane, rb = lane + 32;
-    int hot, Lmax;
-    argmax_rank<kTwo, kPacked>(A.load, B.load, hasA, hasB, lane, hot, Lmax);
-    while (true) {
-        const bool hotB = kTwo && hot >= 32;
-        const int hl = hot & 31;
+    const bool skip = (flags & EP_PLAN_SKIP) != 0;
+    const bool release = (flags & EP_PLAN_RELEASE) != 0;
 
-        // 2. hot's largest-quota instance (lowest expert id on ties)
-        const int qmax = __shfl_sync(kFull, hotB ? B.bq : A.bq, hl);
-        const int bx = __shfl_sync(kFull, hotB ? B.bx : A.bx, hl);
-        const int e = bx >> 5, src_j = bx & 31;
-
-        // 3. eligible: other ranks that hold e or have a free spare slot
-        const bool holdA = A.holds(e);
-        const bool holdB = kTwo && B.holds(e);
-        const bool elA = hasA && ra != hot && (holdA || A.used < S);
-        const bool elB = hasB && rb != hot && (holdB || B.used < S);
-
-        // 4. coldest eligible rank, lowest index on ties
-        int cold, Lmin;
+    // candidate (hot, expert e with quota qsrc): the coldest eligible rank and
+    // the amount; mv <= 0 when no move is possible
+    auto evaluate = [&](int hot, int Lhot, int e, int qsrc, int& cold, bool& holdA,
+                        bool& holdB) -> int {
+        holdA = A.holds(e);
+        holdB = kTwo && B.holds(e);
+        const bool elA = hasA && ra != hot && (holdA || A.has_free(S));
+        const bool elB = hasB && rb != hot && (holdB || B.has_free(S));
+        int Lmin;
         if (kPacked) {
             const unsigned ca = elA ? ((unsigned)A.load << 6) | (unsigned)ra : 0xffffffffu;
             const unsigned cb = elB ? ((unsigned)B.load << 6) | (unsigned)rb : 0xffffffffu;
             const unsigned k = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
-            if (k == 0xffffffffu) break;  // slots ran out
+            if (k == 0xffffffffu) return 0;  // no eligible rank
             cold = (int)(k & 63u);
             Lmin = (int)(k >> 6);
         } else {
-            if (!__any_sync(kFull, elA || elB)) break;  // slots ran out
+            if (!__any_sync(kFull, elA || elB)) return 0;
             const int ca = elA ? A.load : INT_MAX;
             const int cb = elB ? B.load : INT_MAX;
             Lmin = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
@@ -165,16 +185,62 @@ __device__ __forceinline__ void plan_moves(RankRegs<WB>& A, RankRegs<WB>& B, int
             const unsigned b1 = kTwo ? __ballot_sync(kFull, elB && cb == Lmin) : 0u;
             cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
         }
-        const bool coldB = kTwo && cold >= 32;
-        const int cl = cold & 31;
+        return min(qsrc, (Lhot - Lmin) >> 1);
+    };
 
-        // 5. amount, 6. safety cap
-        const int mv = min(qmax, (Lmax - Lmin) >> 1);
-        if (mv <= 0) break;
+    int hot, Lmax;
+    argmax_rank<kTwo, kPacked>(A.load, B.load, hasA, hasB, lane, hot, Lmax);
+    while (true) {
+        // 2. hot's largest-quota instance (lowest expert id on ties)
+        bool hotB = kTwo && hot >= 32;
+        int hl = hot & 31;
+        int qmax = __shfl_sync(kFull, hotB ? B.bq : A.bq, hl);
+        int bx = __shfl_sync(kFull, hotB ? B.bx : A.bx, hl);
+        int e = bx >> 5, src_j = bx & 31;
+
+        // 3-5. coldest eligible rank and the amount
+        int cold = 0;
+        bool holdA = false, holdB = false;
+        int mv = evaluate(hot, Lmax, e, qmax, cold, holdA, holdB);
+        if (mv <= 0) {
+            if (!skip) break;  // the base rule's global stop
+            // skip: hot's next instances, then the next-hottest ranks
+            uint64_t rtried = 1ull << hot;
+            unsigned itried = 1u << src_j;
+            int ranks_tried = 1;
+            while (mv <= 0) {
+                int cq, cx;
+                if (hotB) B.best_excl(W, itried, cq, cx); else A.best_excl(W, itried, cq, cx);
+                cq = __shfl_sync(kFull, cq, hl);
+                cx = __shfl_sync(kFull, cx, hl);
+                if (cq >= 1) {
+                    e = cx >> 5;
+                    src_j = cx & 31;
+                    itried |= 1u << src_j;
+                    qmax = cq;
+                    mv = evaluate(hot, Lmax, e, qmax, cold, holdA, holdB);
+                    continue;
+                }
+                if (ranks_tried == R) break;  // every candidate tried
+                // the hottest rank not tried yet (lowest index on ties)
+                const bool tA = (rtried >> ra) & 1ull, tB = (rtried >> rb) & 1ull;
+                argmax_rank<kTwo, kPacked>(tA ? -1 : A.load, tB ? -1 : B.load, hasA && !tA,
+                                           hasB && !tB, lane, hot, Lmax);
+                rtried |= 1ull << hot;
+                ++ranks_tried;
+                hotB = kTwo && hot >= 32;
+                hl = hot & 31;
+                itried = 0u;
+            }
+            if (mv <= 0) break;  // no candidate can move
+        }
+        // 6. safety cap
         if (iters == max_iters) {
             status = EP_ERR_ITER_LIMIT;
             break;
         }
+        const bool coldB = kTwo && cold >= 32;
+        const int cl = cold & 31;
 
         // 7. move.  Loads first, then the next move's argmax ...
         A.load += (ra == cold ? mv : 0) - (ra == hot ? mv : 0);
@@ -184,7 +250,8 @@ __device__ __forceinline__ void plan_moves(RankRegs<WB>& A, RankRegs<WB>& B, int
         // ... while hot's owner lane takes, cold's owner lane gives, and hot's
         // half refreshes its largest instance (only the half holding each of
         // them is touched)
-        if (hotB) B.take(src_j, lane == hl, mv); else A.take(src_j, lane == hl, mv);
+        if (hotB) B.take(src_j, lane == hl, mv, H, release);
+        else A.take(src_j, lane == hl, mv, H, release);
         if (coldB) B.give(e, holdB, lane == cl, H, mv); else A.give(e, holdA, lane == cl, H, mv);
         if (hotB) B.best(W); else A.best(W);
         hot = nhot;
@@ -206,7 +273,7 @@ __device__ __forceinline__ void init_rank(RankRegs<WB>& X, int rk, int R, int H,
         sum += (unsigned)X.q[j];
     }
     X.load = has ? (int)sum : -1;
-    X.used = 0;
+    X.occ = 0u;
     X.best(W);
 }
 
@@ -233,6 +300,7 @@ __device__ __forceinline__ void store_rank(const RankRegs<WB>& X, int rk, int R,
 template <int WB, bool kTwo>
 __global__ void __launch_bounds__(kPlanWarps * 32, 1)
 plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S, int max_iters,
+            int flags,
             int32_t* __restrict__ quota_out, int32_t* __restrict__ slot_out,
             int32_t* __restrict__ load_out, int32_t* __restrict__ ptr_out,
             int32_t* __restrict__ id_out, int32_t* __restrict__ cum_out,
@@ -273,9 +341,9 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     int iters = 0;
     if (status == EP_OK) {
         if (tot < kPackLimit)
-            plan_moves<WB, kTwo, true>(A, B, lane, H, S, W, max_iters, iters, status);
+            plan_moves<WB, kTwo, true>(A, B, lane, H, S, W, R, max_iters, flags, iters, status);
         else
-            plan_moves<WB, kTwo, false>(A, B, lane, H, S, W, max_iters, iters, status);
+            plan_moves<WB, kTwo, false>(A, B, lane, H, S, W, R, max_iters, flags, iters, status);
     }
 
     // ---- outputs: quota, spare slots and loads straight from registers; the
@@ -341,7 +409,7 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
 
 template <int WB, bool kTwo>
 cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
-                           int32_t max_iters, int32_t* quota, int32_t* slot_expert,
+                           int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
                            int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                            int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
                            cudaStream_t s, bool pdl) {
@@ -363,21 +431,21 @@ cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t 
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, plan_kernel<WB, kTwo>, counts, (int)n_inst, (int)d.R,
-                              (int)d.E, (int)d.S, (int)max_iters, quota, slot_expert, rank_load,
+                              (int)d.E, (int)d.S, (int)max_iters, (int)flags, quota, slot_expert, rank_load,
                               inst_ptr, inst_id, inst_cum, n_iter, inst_status);
 }
 
 template <int WB>
 cudaError_t launch_plan_r(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
-                          int32_t max_iters, int32_t* quota, int32_t* slot_expert,
+                          int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
                           int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                           int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
                           cudaStream_t s, bool pdl) {
     if (d.R > 32)
-        return launch_plan_wb<WB, true>(d, counts, n_inst, max_iters, quota, slot_expert,
+        return launch_plan_wb<WB, true>(d, counts, n_inst, max_iters, flags, quota, slot_expert,
                                         rank_load, inst_ptr, inst_id, inst_cum, n_iter,
                                         inst_status, s, pdl);
-    return launch_plan_wb<WB, false>(d, counts, n_inst, max_iters, quota, slot_expert,
+    return launch_plan_wb<WB, false>(d, counts, n_inst, max_iters, flags, quota, slot_expert,
                                      rank_load, inst_ptr, inst_id, inst_cum, n_iter,
                                      inst_status, s, pdl);
 }
@@ -385,7 +453,7 @@ cudaError_t launch_plan_r(const ep_domain_t& d, const int32_t* counts, int32_t n
 }  // namespace
 
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
-                        int32_t max_iters, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
+                        int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
                         int32_t* inst_ptr, int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter,
                         int32_t* inst_status, cudaStream_t s, bool pdl) {
     if (n_inst == 0) return cudaSuccess;
@@ -393,7 +461,7 @@ cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_i
     const int W = d.E / d.R + d.S;
 #define EP_PLAN_WB(wb)                                                                       \
     if (W <= wb)                                                                             \
-        return launch_plan_r<wb>(d, counts, n_inst, max_iters, quota, slot_expert, rank_load, \
+        return launch_plan_r<wb>(d, counts, n_inst, max_iters, flags, quota, slot_expert, rank_load, \
                                  inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl);
     EP_PLAN_WB(2)
     EP_PLAN_WB(3)
@@ -402,7 +470,7 @@ cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_i
     EP_PLAN_WB(8)
     EP_PLAN_WB(16)
 #undef EP_PLAN_WB
-    return launch_plan_r<32>(d, counts, n_inst, max_iters, quota, slot_expert, rank_load,
+    return launch_plan_r<32>(d, counts, n_inst, max_iters, flags, quota, slot_expert, rank_load,
                              inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl);
 }
 

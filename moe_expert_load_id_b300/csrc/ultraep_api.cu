@@ -109,8 +109,26 @@ ep_status_t ep_plan(const ep_domain_t* dom, const int32_t* counts, int32_t n_ins
         return EP_ERR_INVAL;
     if (!any) return EP_OK;
     if (max_iters <= 0) max_iters = EP_PLAN_MAX_ITERS;
-    return from_cuda(launch_plan(*dom, counts, n_inst, max_iters, quota, slot_expert, rank_load, inst_ptr,
+    return from_cuda(launch_plan(*dom, counts, n_inst, max_iters, 0, quota, slot_expert, rank_load, inst_ptr,
                                  inst_id, inst_cum, n_iter, inst_status,
+                                 static_cast<cudaStream_t>(stream)));
+}
+
+ep_status_t ep_plan_ex(const ep_domain_t* dom, const int32_t* counts, int32_t n_inst,
+                       int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
+                       int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
+                       int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status, void* stream) {
+    if (!domain_ok(dom) || n_inst < 0 || (flags & ~(EP_PLAN_SKIP | EP_PLAN_RELEASE)) != 0)
+        return EP_ERR_INVAL;
+    const bool any = n_inst > 0;
+    if (!arr_ok(counts, any) || !arr_ok(quota, any) || !arr_ok(slot_expert, any && dom->S > 0) ||
+        !arr_ok(rank_load, any) || !arr_ok(inst_ptr, any) || !arr_ok(inst_id, any) ||
+        !arr_ok(inst_cum, any) || !arr_ok(n_iter, any) || !arr_ok(inst_status, any))
+        return EP_ERR_INVAL;
+    if (!any) return EP_OK;
+    if (max_iters <= 0) max_iters = EP_PLAN_MAX_ITERS;
+    return from_cuda(launch_plan(*dom, counts, n_inst, max_iters, flags, quota, slot_expert,
+                                 rank_load, inst_ptr, inst_id, inst_cum, n_iter, inst_status,
                                  static_cast<cudaStream_t>(stream)));
 }
 
@@ -157,7 +175,7 @@ ep_status_t ep_balance(const ep_domain_t* dom, const int32_t* topk_ids, int64_t 
     cudaError_t err = launch_count(*dom, topk_ids, T, n_inst, out->counts, out->counts_src,
                                    dev_status, workspace, s);
     if (err != cudaSuccess) return EP_ERR_CUDA;
-    err = launch_plan(*dom, out->counts, n_inst, max_iters, out->quota, out->slot_expert,
+    err = launch_plan(*dom, out->counts, n_inst, max_iters, 0, out->quota, out->slot_expert,
                       out->rank_load, out->inst_ptr, out->inst_id, out->inst_cum, out->n_iter,
                       out->inst_status, s, /*pdl=*/true);
     if (err != cudaSuccess) return EP_ERR_CUDA;

@@ -22,9 +22,11 @@ _lib = ctypes.CDLL(_LIB_PATH)
 EP_OK, EP_ERR_INVAL, EP_ERR_ITER_LIMIT, EP_ERR_BAD_ID, EP_ERR_WORKSPACE, EP_ERR_CUDA = range(6)
 EP_DEV_BAD_ID, EP_DEV_QUOTA_OVERFLOW, EP_DEV_ROW_RANGE, EP_DEV_COPY_TIMEOUT = 1, 2, 4, 8
 EP_PLAN_MAX_ITERS = 1 << 16
+EP_PLAN_SKIP, EP_PLAN_RELEASE = 1, 2
 EP_COUNT_NOALLOC_SCRATCH_BYTES = 64 << 10
 
-EXPORTS = ("ep_count_workspace_bytes", "ep_count", "ep_count_noalloc", "ep_plan", "ep_reroute",
+EXPORTS = ("ep_count_workspace_bytes", "ep_count", "ep_count_noalloc", "ep_plan", "ep_plan_ex",
+           "ep_reroute",
            "ep_balance", "ep_permute", "ep_unpermute", "ep_combine", "ep_stage", "ep_status_str")
 
 
@@ -70,6 +72,9 @@ _lib.ep_count_noalloc.restype = ctypes.c_int
 _lib.ep_count_noalloc.argtypes = [_DP, _vp, _i64, _i32, _vp, _vp, _vp, _vp]
 _lib.ep_plan.restype = ctypes.c_int
 _lib.ep_plan.argtypes = [_DP, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
+_lib.ep_plan_ex.restype = ctypes.c_int
+_lib.ep_plan_ex.argtypes = [_DP, _vp, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                            _vp]
 _lib.ep_reroute.restype = ctypes.c_int
 _lib.ep_reroute.argtypes = [_DP, _vp, _i64, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]
 
@@ -150,6 +155,16 @@ def ep_plan(dom, counts, quota, slot_expert, rank_load, inst_ptr, inst_id, inst_
                                    _ptr(slot_expert), _ptr(rank_load), _ptr(inst_ptr),
                                    _ptr(inst_id), _ptr(inst_cum), _ptr(n_iter),
                                    _ptr(inst_status), _stream(stream)))
+
+
+def ep_plan_ex(dom, counts, flags, quota, slot_expert, rank_load, inst_ptr, inst_id, inst_cum,
+               n_iter, inst_status, max_iters=0, stream=None):
+    """ep_plan with rule variants: flags = EP_PLAN_SKIP | EP_PLAN_RELEASE (0: ep_plan)."""
+    n_inst = counts.numel() // dom.E
+    _check("ep_plan_ex", _lib.ep_plan_ex(ctypes.byref(dom.c()), _ptr(counts), n_inst, max_iters,
+                                         flags, _ptr(quota), _ptr(slot_expert), _ptr(rank_load),
+                                         _ptr(inst_ptr), _ptr(inst_id), _ptr(inst_cum),
+                                         _ptr(n_iter), _ptr(inst_status), _stream(stream)))
 
 
 def ep_reroute(dom, topk_ids, counts_src, quota, inst_ptr, inst_id, inst_cum, dst_row, src_slot,
@@ -253,7 +268,12 @@ class Buffers:
         ep_count(self.dom, topk_ids, self.counts, self.counts_src, self.dev_status,
                  self.workspace, stream)
 
-    def plan(self, max_iters=0, stream=None):
+    def plan(self, max_iters=0, stream=None, flags=0):
+        if flags:
+            ep_plan_ex(self.dom, self.counts, flags, self.quota, self.slot_expert,
+                       self.rank_load, self.inst_ptr, self.inst_id, self.inst_cum, self.n_iter,
+                       self.inst_status, max_iters, stream)
+            return
         ep_plan(self.dom, self.counts, self.quota, self.slot_expert, self.rank_load,
                 self.inst_ptr, self.inst_id, self.inst_cum, self.n_iter, self.inst_status,
                 max_iters, stream)

@@ -12,7 +12,7 @@ def dom_of(R, E, S, k):
 
 
 def gpu_run(dom, ids_np, hidden_u16=None, src_slot=True, max_iters=0, unpermute=True,
-            fused=False):
+            fused=False, flags=0):
     """ids_np [n_inst, T, k] int32 (host).  Returns host numpy views of every output.
     fused: count -> plan -> reroute through the single ep_balance call."""
     n_inst, T, k = ids_np.shape
@@ -24,7 +24,7 @@ def gpu_run(dom, ids_np, hidden_u16=None, src_slot=True, max_iters=0, unpermute=
         b.balance_fused(ids, max_iters=max_iters)
     else:
         b.count(ids)
-        b.plan(max_iters=max_iters)
+        b.plan(max_iters=max_iters, flags=flags)
         b.reroute(ids)
     out = {}
     if hidden_u16 is not None:
@@ -47,7 +47,8 @@ def gpu_run(dom, ids_np, hidden_u16=None, src_slot=True, max_iters=0, unpermute=
     return out
 
 
-def oracle_run(R, E, S, ids_np, hidden_u16=None, max_iters=oracle.PLAN_MAX_ITERS):
+def oracle_run(R, E, S, ids_np, hidden_u16=None, max_iters=oracle.PLAN_MAX_ITERS,
+               variant="base"):
     """Per instance oracle outputs, same layout as gpu_run."""
     n_inst, T, k = ids_np.shape
     res = {key: [] for key in ("counts", "counts_src", "n_bad", "quota", "slot_expert",
@@ -56,7 +57,7 @@ def oracle_run(R, E, S, ids_np, hidden_u16=None, max_iters=oracle.PLAN_MAX_ITERS
                                "y")}
     for g in range(n_inst):
         c, cs, nb = oracle.count(ids_np[g], R, E)
-        pl = oracle.plan(c, R, E, S, max_iters=max_iters)
+        pl = oracle.plan(c, R, E, S, max_iters=max_iters, variant=variant)
         dst, src, off = oracle.reroute(ids_np[g], R, E, S, pl)
         res["counts"].append(c)
         res["counts_src"].append(cs)

@@ -147,3 +147,14 @@ def test_stage_host_rejections_need_no_gpu(lib):
     assert lib.ep_stage(ctypes.byref(Dom(8, 32, 0, 4)), 1, None, 32, None, None, None, None,
                         None) == 0
     assert lib.ep_stage(ctypes.byref(d), 1, None, 0, None, None, None, None, None) == 0
+
+
+def test_plan_ex_rejects_unknown_flags(lib):
+    vp = ctypes.c_void_p
+    lib.ep_plan_ex.argtypes = [ctypes.POINTER(Dom), vp, ctypes.c_int32, ctypes.c_int32,
+                               ctypes.c_int32] + [vp] * 9
+    d = Dom(8, 32, 1, 4)
+    fake = vp(0x10000)                    # never dereferenced: every call below fails validation
+    assert lib.ep_plan_ex(ctypes.byref(d), fake, 1, 0, 4, *([fake] * 8), None) == 1
+    assert lib.ep_plan_ex(ctypes.byref(d), fake, 1, 0, -1, *([fake] * 8), None) == 1
+    assert lib.ep_plan_ex(ctypes.byref(d), None, 0, 0, 3, *([None] * 8), None) == 0
