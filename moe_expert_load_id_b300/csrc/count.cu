@@ -28,9 +28,16 @@ namespace {
 
 namespace cg = cooperative_groups;
 
-constexpr int kCountThreads = 512;
+// block size and 16-byte loads in flight per thread (build-time tunables)
+#ifndef EP_COUNT_THREADS
+#define EP_COUNT_THREADS 256
+#endif
+#ifndef EP_COUNT_VEC
+#define EP_COUNT_VEC 2
+#endif
+constexpr int kCountThreads = EP_COUNT_THREADS;
 constexpr int kCountWarps = kCountThreads / 32;
-constexpr int kVec = 2;                         // 16-byte loads in flight per thread
+constexpr int kVec = EP_COUNT_VEC;
 constexpr int kTargetBlocks = 2 * 148;          // two blocks per B300 SM
 constexpr int kMinChunk = kCountThreads * 4;    // at least one 16-byte load per thread
 constexpr int kMaxChunksPerRank = 8;            // portable cluster size
@@ -51,12 +58,30 @@ __host__ __device__ inline size_t count_smem_bytes(int E) {
     return sizeof(int32_t) * ((size_t)h + E);
 }
 
+// 16-byte id load: streaming (evict-first), or (EP_COUNT_LOAD_HINT = 1)
+// through the non-coherent path with no L1 allocation and a 256-byte L2
+// prefetch hint (a build-time tunable)
+#ifndef EP_COUNT_LOAD_HINT
+#define EP_COUNT_LOAD_HINT 0
+#endif
+__device__ __forceinline__ int4 load_ids(const int4* p) {
+#if EP_COUNT_LOAD_HINT
+    int4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.s32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+#else
+    return __ldcs(p);
+#endif
+}
+
 __device__ __forceinline__ void count_one(int v, int E, int32_t* hist, int C, int col, int& bad) {
     if ((unsigned)v < (unsigned)E) atomicAdd(&hist[v * C + col], 1);
     else bad = 1;
 }
 
-__global__ void __launch_bounds__(kCountThreads, 4)
+__global__ void __launch_bounds__(kCountThreads, 2048 / kCountThreads)
 count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int cps,
              int32_t* __restrict__ counts, int32_t* __restrict__ counts_src,
              int32_t* dev_status, uint32_t* inst_ticket) {
@@ -108,7 +133,7 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {
             const int64_t vi = v0 + u * 32 + lane;
-            w[u] = (vi < n4) ? __ldcs(body + vi) : make_int4(0, 0, 0, 0);
+            w[u] = (vi < n4) ? load_ids(body + vi) : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
         for (int u = 0; u < kVec; ++u) {

@@ -30,6 +30,11 @@
 // ids are read once from memory (kept in registers between the histogram and
 // the assignment phase of a chunk); dst_row is written with coalesced
 // streaming stores; the optional src_slot inverse is a scattered store.
+//
+// (A design with lane-private counters, each lane owning a contiguous run of
+// slots, two shared-memory atomics per slot and one warp scan per expert
+// pair, executed as many instructions per slot as this one at half the
+// occupancy, and was slower in every configuration measured.)
 #include <climits>
 #include <type_traits>
 
@@ -73,110 +78,29 @@ __device__ __forceinline__ int upper_bound(const int32_t* a, int lo, int hi, int
     return lo;
 }
 
-// One block per (instance, source rank); the rank's slots are processed in
-// chunks of kThreads * kItems.  kThreads = 1024 when few blocks run (one
-// instance: the whole rank is one chunk) and E <= 512; else 256, four blocks
-// per SM (measured faster for batched calls than 512 x 2).
+// Plan tables in shared memory:
+//   off[P+1]  first row of each instance (exclusive prefix of quota over p)
+//   ptr[E+1]  CSR row pointers of the instance lists, clamped to [0, M]
+//   bcum[M]   inclusive cumulative quota of each list entry (INT_MIN if unused)
+//   bdel[M]   row minus within-expert rank, for the ranks of that entry
+//   base[E]   += slots of e on source ranks below r
+// base must be zero, and a block barrier passed, before the call; the block
+// of source rank 0 also writes inst_offset.  The caller puts a barrier
+// between this and any read of the tables.
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads, 1024 / kThreads)
-reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
-               const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
-               const int32_t* __restrict__ inst_ptr, const int32_t* __restrict__ inst_id,
-               const int32_t* __restrict__ inst_cum, int32_t* __restrict__ dst_row,
-               int32_t* __restrict__ src_slot, int32_t* __restrict__ inst_offset,
-               int32_t* dev_status, int early) {
+__device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst, int r,
+                                            const int32_t* __restrict__ counts_src,
+                                            const int32_t* __restrict__ quota,
+                                            const int32_t* __restrict__ inst_ptr,
+                                            const int32_t* __restrict__ inst_id,
+                                            const int32_t* __restrict__ inst_cum,
+                                            int32_t* __restrict__ inst_offset, int32_t* off,
+                                            int32_t* ptr, int32_t* bcum, int32_t* bdel,
+                                            int32_t* base, int32_t* warp_tot) {
     constexpr int kWarps = kThreads / 32;
-    constexpr int kChunk = kThreads * kItems;
     constexpr int kIpt = (2048 + kThreads - 1) / kThreads;  // P <= 2048 quota per thread
-    extern __shared__ __align__(16) int32_t sm[];
-    __shared__ int32_t warp_tot[kWarps];
-    __shared__ int32_t flags;
-
-    const RrLayout lay = rr_layout(R, E, S, kWarps);
-    const int P = lay.P, M = lay.M;
-    int32_t* off = sm;              // [P+1] first row of each instance
-    int32_t* ptr = off + (P + 1);   // [E+1] CSR row pointers (clamped)
-    int32_t* bcum = ptr + (E + 1);  // [M]   inclusive cumulative quota
-    int32_t* bdel = bcum + M;       // [M]   row - within-expert rank
-    int32_t* base = bdel + M;       // [E]   within-expert rank of the chunk's first slot
-    int32_t* wx0 = base + E;        // [kWarps][E] per-warp counts, then each warp's first rank
-    int32_t* wdb = wx0 + kWarps * E;  // [kWarps][E] row of that first rank
-    uint16_t* wlim = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(sm) + lay.lim_off);
-                                    // [kWarps][E] ranks left in its instance (capped)
-
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int inst = blockIdx.x / R, r = blockIdx.x % R;
     const int32_t* qg = quota + (int64_t)inst * P;
-
-    // ---- this block's slots (source rank r).  Out-of-range ids are flagged
-    // at load time; slots past the end load as -1.
-    // (32-bit division: T < 2^31 since T*k < 2^31)
-    const int Tr = ((int)T + R - 1) / R;
-    const int64_t N = T * k;
-    const int64_t s0 = min(T, (int64_t)r * Tr) * k, s1 = min(T, (int64_t)(r + 1) * Tr) * k;
-    const int32_t* idi = ids + (int64_t)inst * N;
-    int my_flags = 0;
-    int ev[kItems];
-    const int lbase = warp * 32 * kItems + lane;  // chunk-local index of item 0
-    auto load_chunk = [&](int64_t cs) {
-        const int nc = (int)min((int64_t)kChunk, s1 - cs);
-        const int32_t* src = idi + cs;
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int li = lbase + it * 32;
-            const int v = (li < nc) ? __ldcs(src + li) : -1;
-            if (li < nc && (unsigned)v >= (unsigned)E) my_flags |= EP_DEV_BAD_ID;
-            ev[it] = v;
-        }
-    };
-    // ---- shared tables that phase A needs: zero them first
-    if (tid == 0) flags = 0;
-    for (int x = tid; x < (2 * kWarps + 1) * E; x += kThreads) base[x] = 0;  // base, wx0, wdb
-    __syncthreads();
-
-    int32_t* wrow = wx0 + warp * E;
-    const unsigned lt = lanemask_lt();
-    // phase A: per-warp histogram and ranks inside the warp; ev becomes
-    // e | rank << 10 (-1: no valid id).  The lanes holding the same id find
-    // each other through the warp's mask row (the wdb row, idle until phase
-    // B): each ORs its lane bit into mask[e]; after a warp barrier mask[e] is
-    // the group.  The group's lowest lane (leader) advances the warp's running
-    // count of e and clears mask[e] for the next step.
-    auto phase_a = [&]() {
-        uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * E;
-#pragma unroll
-        for (int it = 0; it < kItems; ++it) {
-            const int e = ev[it];
-            const bool valid = (unsigned)e < (unsigned)E;
-            if (valid) atomicOr(&mrow[e], 1u << lane);
-            __syncwarp();
-            const unsigned g = valid ? mrow[e] : 0u;
-            const int leader = __ffs(g) - 1;
-            __syncwarp();
-            int old = 0;
-            if (valid && lane == leader) {
-                old = wrow[e];
-                wrow[e] = old + __popc(g);
-                mrow[e] = 0u;
-            }
-            __syncwarp();  // the clear lands before the next step's ORs
-            old = __shfl_sync(kFull, old, leader & 31);
-            ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
-        }
-    };
-    // early (ep_balance): this grid is a programmatic dependent of ep_plan and
-    // the ids were complete before ep_count started, so the first chunk's ids
-    // are loaded and ranked before waiting for the plan.  Otherwise the wait
-    // comes first (a plain launch returns from it at once).
-    if (!early) pdl_wait();
-    if (s0 < s1) {
-        load_chunk(s0);
-        phase_a();
-    }
-    if (early) pdl_wait();
-    pdl_trigger();
-
-    // ---- prologue: plan tables
     int qv[kIpt];
     int qlocal = 0;
 #pragma unroll
@@ -260,6 +184,113 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         int32_t* og = inst_offset + (int64_t)inst * (P + 1);
         for (int p = tid; p <= P; p += kThreads) og[p] = off[p];
     }
+
+}
+
+// One block per (instance, source rank); the rank's slots are processed in
+// chunks of kThreads * kItems.  kThreads = 1024 when few blocks run (one
+// instance: the whole rank is one chunk) and E <= 512; else 256, four blocks
+// per SM (measured faster for batched calls than 512 x 2).
+template <int kThreads>
+__global__ void __launch_bounds__(kThreads, 1024 / kThreads)
+reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
+               const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
+               const int32_t* __restrict__ inst_ptr, const int32_t* __restrict__ inst_id,
+               const int32_t* __restrict__ inst_cum, int32_t* __restrict__ dst_row,
+               int32_t* __restrict__ src_slot, int32_t* __restrict__ inst_offset,
+               int32_t* dev_status, int early) {
+    constexpr int kWarps = kThreads / 32;
+    constexpr int kChunk = kThreads * kItems;
+    extern __shared__ __align__(16) int32_t sm[];
+    __shared__ int32_t warp_tot[kWarps];
+    __shared__ int32_t flags;
+
+    const RrLayout lay = rr_layout(R, E, S, kWarps);
+    const int P = lay.P, M = lay.M;
+    int32_t* off = sm;              // [P+1] first row of each instance
+    int32_t* ptr = off + (P + 1);   // [E+1] CSR row pointers (clamped)
+    int32_t* bcum = ptr + (E + 1);  // [M]   inclusive cumulative quota
+    int32_t* bdel = bcum + M;       // [M]   row - within-expert rank
+    int32_t* base = bdel + M;       // [E]   within-expert rank of the chunk's first slot
+    int32_t* wx0 = base + E;        // [kWarps][E] per-warp counts, then each warp's first rank
+    int32_t* wdb = wx0 + kWarps * E;  // [kWarps][E] row of that first rank
+    uint16_t* wlim = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(sm) + lay.lim_off);
+                                    // [kWarps][E] ranks left in its instance (capped)
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int inst = blockIdx.x / R, r = blockIdx.x % R;
+
+    // ---- this block's slots (source rank r).  Out-of-range ids are flagged
+    // at load time; slots past the end load as -1.
+    // (32-bit division: T < 2^31 since T*k < 2^31)
+    const int Tr = ((int)T + R - 1) / R;
+    const int64_t N = T * k;
+    const int64_t s0 = min(T, (int64_t)r * Tr) * k, s1 = min(T, (int64_t)(r + 1) * Tr) * k;
+    const int32_t* idi = ids + (int64_t)inst * N;
+    int my_flags = 0;
+    int ev[kItems];
+    const int lbase = warp * 32 * kItems + lane;  // chunk-local index of item 0
+    auto load_chunk = [&](int64_t cs) {
+        const int nc = (int)min((int64_t)kChunk, s1 - cs);
+        const int32_t* src = idi + cs;
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int li = lbase + it * 32;
+            const int v = (li < nc) ? __ldcs(src + li) : -1;
+            if (li < nc && (unsigned)v >= (unsigned)E) my_flags |= EP_DEV_BAD_ID;
+            ev[it] = v;
+        }
+    };
+    // ---- shared tables that phase A needs: zero them first
+    if (tid == 0) flags = 0;
+    for (int x = tid; x < (2 * kWarps + 1) * E; x += kThreads) base[x] = 0;  // base, wx0, wdb
+    __syncthreads();
+
+    int32_t* wrow = wx0 + warp * E;
+    const unsigned lt = lanemask_lt();
+    // phase A: per-warp histogram and ranks inside the warp; ev becomes
+    // e | rank << 10 (-1: no valid id).  The lanes holding the same id find
+    // each other through the warp's mask row (the wdb row, idle until phase
+    // B): each ORs its lane bit into mask[e]; after a warp barrier mask[e] is
+    // the group.  The group's lowest lane (leader) advances the warp's running
+    // count of e and clears mask[e] for the next step.
+    auto phase_a = [&]() {
+        uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * E;
+#pragma unroll
+        for (int it = 0; it < kItems; ++it) {
+            const int e = ev[it];
+            const bool valid = (unsigned)e < (unsigned)E;
+            if (valid) atomicOr(&mrow[e], 1u << lane);
+            __syncwarp();
+            const unsigned g = valid ? mrow[e] : 0u;
+            const int leader = __ffs(g) - 1;
+            __syncwarp();
+            int old = 0;
+            if (valid && lane == leader) {
+                old = wrow[e];
+                wrow[e] = old + __popc(g);
+                mrow[e] = 0u;
+            }
+            __syncwarp();  // the clear lands before the next step's ORs
+            old = __shfl_sync(kFull, old, leader & 31);
+            ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
+        }
+    };
+    // early (ep_balance): this grid is a programmatic dependent of ep_plan and
+    // the ids were complete before ep_count started, so the first chunk's ids
+    // are loaded and ranked before waiting for the plan.  Otherwise the wait
+    // comes first (a plain launch returns from it at once).
+    if (!early) pdl_wait();
+    if (s0 < s1) {
+        load_chunk(s0);
+        phase_a();
+    }
+    if (early) pdl_wait();
+    pdl_trigger();
+
+    // ---- prologue: plan tables
+    plan_tables<kThreads>(R, E, P, M, inst, r, counts_src, quota, inst_ptr, inst_id, inst_cum,
+                          inst_offset, off, ptr, bcum, bdel, base, warp_tot);
     // (the barrier before phase B orders the writes above before any read of
     // bcum / bdel)
 
@@ -406,6 +437,7 @@ cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T
                               (int)d.E, (int)d.S, counts_src, quota, inst_ptr, inst_id, inst_cum,
                               dst_row, src_slot, inst_offset, dev_status, pdl ? 1 : 0);
 }
+
 
 }  // namespace
 

@@ -122,6 +122,15 @@ CASES = [
     ("bulk_row_1KiB",      8,  4, 1, 4,  333,   2,      512,  "zipf"),
     ("bulk_row_3_segments", 4, 2, 1, 3,  97,    1,      8200, "zipf"),
     ("bulk_rows_bad_ids",  8,  4, 2, 4,  250,   3,      1024, "bad"),
+    # reroute kernels: E = 256 (ids held as bytes cannot mark an invalid id),
+    # E in (256, 512] (the mask kernel, one wide block per rank), a rank in
+    # several rounds of lane runs, many blocks (short runs, four warps) with
+    # invalid ids, and with ranks that do not start on a 16-byte boundary
+    ("E256_bad_ids",       8,  32, 0, 8, 3001,  2,      8,   "bad"),
+    ("E320_mask_kernel",   16, 20, 2, 8, 3000,  1,      8,   "zipf"),
+    ("runs_many_rounds",   2,  8, 1, 8,  20000, 1,      8,   "zipf"),
+    ("runs_batched_bad",   8,  4, 1, 4,  3001,  40,     8,   "bad"),
+    ("runs_batched_unaligned", 8, 4, 1, 3, 1001, 40,    8,   "zipf"),
 ]
 
 
