@@ -41,6 +41,9 @@ constexpr int kVec = EP_COUNT_VEC;
 constexpr int kTargetBlocks = 2 * 148;          // two blocks per B300 SM
 constexpr int kMinChunk = kCountThreads * 4;    // at least one 16-byte load per thread
 constexpr int kMaxChunksPerRank = 8;            // portable cluster size
+#ifndef EP_COUNT_MIN_CHUNKS
+#define EP_COUNT_MIN_CHUNKS 1                   // chunks per rank at least (build-time tunable)
+#endif
 
 // columns of the lane-column histogram: 16 (lanes l and l+16 share a column,
 // at most a 2-way same-address collision) while E*16 ints fit 32 KB.  Four
@@ -246,6 +249,7 @@ int count_chunks_per_rank(const ep_domain_t& d, int64_t T, int32_t n_inst) {
     int64_t cap = slots_per_rank / kMinChunk;
     if (cap < 1) cap = 1;
     if (cap > kMaxChunksPerRank) cap = kMaxChunksPerRank;
+    if (cps < EP_COUNT_MIN_CHUNKS) cps = EP_COUNT_MIN_CHUNKS;
     if (cps > cap) cps = cap;
     if (cps < 1) cps = 1;
     return (int)cps;

@@ -102,10 +102,13 @@ struct RankRegs {
         }
     }
     // cold side: the owner lane adds mv to its instance of e, filling the
-    // lowest free spare slot when it does not hold e yet.  Only one instance
-    // grew, so the largest instance is updated in place.
+    // lowest free spare slot when it does not hold e yet (without released
+    // slots the filled ones are a prefix, so that is the count of filled
+    // slots).  Only one instance grew, so the largest instance is updated in
+    // place.
+    template <bool kHoles>
     __device__ __forceinline__ void give(int e, bool held, bool mine, int H, int mv) {
-        const int jn = held ? -1 : H + __ffs(~occ) - 1;
+        const int jn = held ? -1 : H + (kHoles ? __ffs(~occ) - 1 : __popc(occ));
         int nq = 0, nj = 0;
 #pragma unroll
         for (int jj = 0; jj < WB; ++jj) {
@@ -147,18 +150,19 @@ __device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB
 // The loop is software-pipelined: as soon as the amount is known the two
 // loads change and the next move's argmax is issued; the instance bookkeeping
 // of the current move (take, give, largest instance) overlaps it.
-// flags (warp-uniform): EP_PLAN_SKIP -- when the hottest rank's largest
+// flags (warp-uniform; kFlags: compiled in at all, so that the base rule's
+// loop carries none of it): EP_PLAN_SKIP -- when the hottest rank's largest
 // instance cannot move, try its next instances, then the next-hottest ranks,
 // and make the first move that can be made; EP_PLAN_RELEASE -- a spare-slot
 // instance a move empties frees its slot.
-template <int WB, bool kTwo, bool kPacked>
+template <int WB, bool kTwo, bool kPacked, bool kFlags>
 __device__ __forceinline__ void plan_moves(RankRegs<WB>& A, RankRegs<WB>& B, int lane, int H,
                                            int S, int W, int R, int max_iters, int flags,
                                            int& iters, int& status) {
     const bool hasA = A.load >= 0, hasB = kTwo && B.load >= 0;
     const int ra = lane, rb = lane + 32;
-    const bool skip = (flags & EP_PLAN_SKIP) != 0;
-    const bool release = (flags & EP_PLAN_RELEASE) != 0;
+    const bool skip = kFlags && (flags & EP_PLAN_SKIP) != 0;
+    const bool release = kFlags && (flags & EP_PLAN_RELEASE) != 0;
 
     // candidate (hot, expert e with quota qsrc): the coldest eligible rank and
     // the amount; mv <= 0 when no move is possible
@@ -252,7 +256,8 @@ __device__ __forceinline__ void plan_moves(RankRegs<WB>& A, RankRegs<WB>& B, int
         // them is touched)
         if (hotB) B.take(src_j, lane == hl, mv, H, release);
         else A.take(src_j, lane == hl, mv, H, release);
-        if (coldB) B.give(e, holdB, lane == cl, H, mv); else A.give(e, holdA, lane == cl, H, mv);
+        if (coldB) B.template give<kFlags>(e, holdB, lane == cl, H, mv);
+        else A.template give<kFlags>(e, holdA, lane == cl, H, mv);
         if (hotB) B.best(W); else A.best(W);
         hot = nhot;
         Lmax = nLmax;
@@ -297,7 +302,7 @@ __device__ __forceinline__ void store_rank(const RankRegs<WB>& X, int rk, int R,
     lo[rk] = X.load;
 }
 
-template <int WB, bool kTwo>
+template <int WB, bool kTwo, bool kFlags>
 __global__ void __launch_bounds__(kPlanWarps * 32, 1)
 plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S, int max_iters,
             int flags,
@@ -341,9 +346,11 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     int iters = 0;
     if (status == EP_OK) {
         if (tot < kPackLimit)
-            plan_moves<WB, kTwo, true>(A, B, lane, H, S, W, R, max_iters, flags, iters, status);
+            plan_moves<WB, kTwo, true, kFlags>(A, B, lane, H, S, W, R, max_iters, flags, iters,
+                                               status);
         else
-            plan_moves<WB, kTwo, false>(A, B, lane, H, S, W, R, max_iters, flags, iters, status);
+            plan_moves<WB, kTwo, false, kFlags>(A, B, lane, H, S, W, R, max_iters, flags, iters,
+                                                status);
     }
 
     // ---- outputs: quota, spare slots and loads straight from registers; the
@@ -407,15 +414,15 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     }
 }
 
-template <int WB, bool kTwo>
-cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
+template <int WB, bool kTwo, bool kFlags>
+cudaError_t launch_plan_k(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
                            int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
                            int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                            int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
                            cudaStream_t s, bool pdl) {
     const size_t smem = kPlanWarps * plan_warp_bytes(d.R, d.E, d.S);
     if (smem > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(plan_kernel<WB, kTwo>,
+        cudaError_t err = cudaFuncSetAttribute(plan_kernel<WB, kTwo, kFlags>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)smem);
         if (err != cudaSuccess) return err;
@@ -430,9 +437,25 @@ cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, plan_kernel<WB, kTwo>, counts, (int)n_inst, (int)d.R,
+    return cudaLaunchKernelEx(&cfg, plan_kernel<WB, kTwo, kFlags>, counts, (int)n_inst, (int)d.R,
                               (int)d.E, (int)d.S, (int)max_iters, (int)flags, quota, slot_expert, rank_load,
                               inst_ptr, inst_id, inst_cum, n_iter, inst_status);
+}
+
+// the flag-free base rule gets its own kernel
+template <int WB, bool kTwo>
+cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
+                           int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
+                           int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
+                           int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
+                           cudaStream_t s, bool pdl) {
+    if (flags != 0)
+        return launch_plan_k<WB, kTwo, true>(d, counts, n_inst, max_iters, flags, quota,
+                                             slot_expert, rank_load, inst_ptr, inst_id, inst_cum,
+                                             n_iter, inst_status, s, pdl);
+    return launch_plan_k<WB, kTwo, false>(d, counts, n_inst, max_iters, flags, quota, slot_expert,
+                                          rank_load, inst_ptr, inst_id, inst_cum, n_iter,
+                                          inst_status, s, pdl);
 }
 
 template <int WB>

@@ -43,7 +43,15 @@
 namespace ultraep {
 namespace {
 
-constexpr int kItems = 16;  // 32-slot steps per warp per chunk (ids held in registers)
+// 32-slot steps per warp per chunk (ids held in registers), blocks per SM of
+// the many-block launches (build-time tunables)
+#ifndef EP_REROUTE_ITEMS
+#define EP_REROUTE_ITEMS 16
+#endif
+#ifndef EP_REROUTE_BLOCKS_PER_SM
+#define EP_REROUTE_BLOCKS_PER_SM 4
+#endif
+constexpr int kItems = EP_REROUTE_ITEMS;
 
 struct RrLayout {
     int P, M;        // instances, CSR capacity
@@ -192,7 +200,7 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
 // instance: the whole rank is one chunk) and E <= 512; else 256, four blocks
 // per SM (measured faster for batched calls than 512 x 2).
 template <int kThreads>
-__global__ void __launch_bounds__(kThreads, 1024 / kThreads)
+__global__ void __launch_bounds__(kThreads, kThreads == 256 ? EP_REROUTE_BLOCKS_PER_SM : 1024 / kThreads)
 reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
                const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
                const int32_t* __restrict__ inst_ptr, const int32_t* __restrict__ inst_id,

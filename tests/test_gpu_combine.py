@@ -109,3 +109,40 @@ def test_combine_full_size_layer_sample():
                           wts[0][torch.from_numpy(toks).cuda()].cpu().numpy())
     got = y[0][torch.from_numpy(toks).cuda()].view(torch.int16).cpu().numpy().view(np.uint16)
     assert np.array_equal(got, want)
+
+
+def _fused_differs_case(n_tok, seed):
+    """k = 2 tokens whose combine depends on the product being rounded before the
+    sum: with a fused multiply-add the bf16 result would differ.  Found by a
+    seeded search on the CPU (float64 holds a product of two floats exactly)."""
+    rng = np.random.default_rng(seed)
+    rows, ws = [], []
+    while len(rows) < n_tok:
+        a = rng.standard_normal(2).astype(np.float32)
+        xb = (a.view(np.uint32) >> 16).astype(np.uint16)
+        x = (xb.astype(np.uint32) << 16).view(np.float32)
+        w = rng.standard_normal(2).astype(np.float32)
+        sep = np.float32(np.float32(w[0] * x[0]) + np.float32(w[1] * x[1]))
+        fused = np.float32(np.float64(w[1]) * np.float64(x[1]) + np.float64(np.float32(w[0] * x[0])))
+        bs = int(np.array([sep], np.float32).view(np.uint32)[0])
+        bfz = int(np.array([fused], np.float32).view(np.uint32)[0])
+        to_bf = lambda u: (u >> 16) + (1 if ((u & 0xFFFF) > 0x8000 or ((u & 0xFFFF) == 0x8000 and (u >> 16) & 1)) else 0)
+        if to_bf(bs) != to_bf(bfz):
+            rows.append(xb)
+            ws.append(w)
+    T, k = n_tok, 2
+    grouped = np.zeros((1, T * k, 8), np.uint16)
+    for t_, xb in enumerate(rows):
+        grouped[0, 2 * t_, :] = xb[0]
+        grouped[0, 2 * t_ + 1, :] = xb[1]
+    dst = np.arange(T * k, dtype=np.int32)[None]
+    w = np.stack(ws).astype(np.float32)[None]
+    return grouped, dst, w
+
+
+def test_combine_rounds_products_before_sums():
+    grouped, dst, w = _fused_differs_case(64, 5)
+    got, st = _gpu_combine(grouped, dst, w, 64, 2)
+    assert st == 0
+    want = oracle.combine(grouped[0], 64, 2, dst[0], w[0])
+    assert np.array_equal(got[0], want)
