@@ -235,12 +235,18 @@ def batched_report(U, w, ids, pipe, stream, device, peak, reps=5, warm=2):
     too little to fill HBM, while the whole microbatch moves about 400 MB."""
     L = w.layers
     b = U.Buffers(pipe.dom, w.T, L, device=device)
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)   # 2x L2
+    # L2 flush: write 256 MB (2x L2), then read another 256 MB, so that the timed
+    # launch starts with L2 holding only clean lines of neither its inputs nor
+    # its outputs (a write-only flush leaves ~126 MB of dirty lines whose
+    # write-back would land inside the timed launch)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    flush_r = torch.ones(64 << 20, dtype=torch.int32, device=device)
     names = ("count", "plan", "reroute")
     acc = {n: [] for n in names}
     for rep in range(warm + reps):
         for n in names:
             flush.zero_()
+            flush_r.sum()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             if n == "count":
@@ -262,7 +268,7 @@ def batched_report(U, w, ids, pipe, stream, device, peak, reps=5, warm=2):
     reroute_bytes = L * 8 * w.N
     gbs = lambda by, t: by / (t * 1e-6) / 1e9
     return {"launch": f"one launch per step over all {w.layers} layers (n_inst={L}), "
-                      "L2 flushed before each launch",
+                      "L2 flushed before each launch (256 MB written, then 256 MB read)",
             "count": {"us": round(us["count"], 2), "bytes": count_bytes,
                       "gbs": round(gbs(count_bytes, us["count"]), 1),
                       "frac": round(gbs(count_bytes, us["count"]) / peak, 4)},

@@ -49,8 +49,11 @@ constexpr int kMaxChunksPerRank = 8;            // portable cluster size
 // at most a 2-way same-address collision) while E*16 ints fit 32 KB.  Four
 // blocks per SM with two 16-byte loads per thread measured faster than three
 // blocks with four loads and 32 columns.
+#ifndef EP_COUNT_COLS
+#define EP_COUNT_COLS 16                        // lane columns at most (build-time tunable)
+#endif
 __host__ __device__ inline int count_cols(int E) {
-    int C = 16;
+    int C = EP_COUNT_COLS;
     while (C > 1 && E * C > 8192) C >>= 1;
     return C;
 }
