@@ -33,8 +33,8 @@
 //
 // (A design with lane-private counters, each lane owning a contiguous run of
 // slots, two shared-memory atomics per slot and one warp scan per expert
-// pair, executed as many instructions per slot as this one at half the
-// occupancy, and was slower in every configuration measured.)
+// pair, was slower in every configuration measured, also with a path free of
+// per-slot tests for full aligned runs.)
 #include <climits>
 #include <type_traits>
 
@@ -119,6 +119,79 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
     }
     const int32_t* pg = inst_ptr + (int64_t)inst * (E + 1);
     for (int e = tid; e <= E; e += kThreads) ptr[e] = min(max(pg[e], 0), M);
+    // the list entries: cumulative quota, and for now the instance (-1 when
+    // unused or out of range); every load here and below is independent, so
+    // the prologue waits for memory once
+    {
+        const int nM = min(max(__ldg(pg + E), 0), M);
+        const int32_t* ig = inst_id + (int64_t)inst * M;
+        const int32_t* cg = inst_cum + (int64_t)inst * M;
+        for (int m = tid; m < M; m += kThreads) {
+            int cum = INT_MIN, p = -1;
+            if (m < nM) {
+                const int pm = ig[m], cm = cg[m];
+                if (pm >= 0 && pm < P) {
+                    p = pm;
+                    cum = cm;
+                }
+            }
+            bcum[m] = cum;
+            bdel[m] = p;
+        }
+    }
+    // per-expert slots on earlier source ranks.  With E a multiple of 4 and
+    // the rows 16-byte aligned, thread (g, q) sums the int4 column q
+    // (experts 4q .. 4q+3) over rows g, g+G, ... < r (G = threads / (E/4)),
+    // eight loads in flight; otherwise thread (g, e) sums column e the same
+    // way (G = threads / E).  The partial sums meet in base[] by atomics.
+    {
+        const int32_t* cs = counts_src + (int64_t)inst * R * E;
+        const int Q = E >> 2;
+        if ((E & 3) == 0 && Q <= kThreads && (reinterpret_cast<uintptr_t>(cs) & 15u) == 0) {
+            const int G = kThreads / Q;
+            const int q = tid % Q, g = tid / Q;
+            if (g < G) {
+                int4 t = make_int4(0, 0, 0, 0);
+                for (int r0 = g; r0 < r; r0 += 8 * G) {
+                    int4 v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int rr = r0 + u * G;
+                        v[u] = (rr < r) ? __ldg(reinterpret_cast<const int4*>(cs + (int64_t)rr * E) + q)
+                                        : make_int4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        t.x += v[u].x;
+                        t.y += v[u].y;
+                        t.z += v[u].z;
+                        t.w += v[u].w;
+                    }
+                }
+                if (t.x != 0) atomicAdd(&base[4 * q], t.x);
+                if (t.y != 0) atomicAdd(&base[4 * q + 1], t.y);
+                if (t.z != 0) atomicAdd(&base[4 * q + 2], t.z);
+                if (t.w != 0) atomicAdd(&base[4 * q + 3], t.w);
+            }
+        } else {
+            const int G = (E <= kThreads) ? kThreads / E : 1;
+            for (int x = tid; x < G * E; x += kThreads) {
+                const int e = x % E, g = x / E;
+                int t = 0;
+                for (int r0 = g; r0 < r; r0 += 8 * G) {
+                    int v[8];
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) {
+                        const int rr = r0 + u * G;
+                        v[u] = (rr < r) ? cs[(int64_t)rr * E + e] : 0;
+                    }
+#pragma unroll
+                    for (int u = 0; u < 8; ++u) t += v[u];
+                }
+                if (t != 0) atomicAdd(&base[e], t);
+            }
+        }
+    }
     // inst_offset: exclusive prefix of quota over p
     int qx = qlocal;
 #pragma unroll
@@ -137,28 +210,6 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
         }
         if (lane < kWarps) warp_tot[lane] = w;  // inclusive over warps
     }
-    // per-expert slots on earlier source ranks: thread (g, e) sums rows
-    // g, g+G, ... < r of column e (G = threads / E), loads eight at a time,
-    // then adds its partial into base[e]
-    {
-        const int32_t* cs = counts_src + (int64_t)inst * R * E;
-        const int G = (E <= kThreads) ? kThreads / E : 1;
-        for (int x = tid; x < G * E; x += kThreads) {
-            const int e = x % E, g = x / E;
-            int t = 0;
-            for (int r0 = g; r0 < r; r0 += 8 * G) {
-                int v[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int rr = r0 + u * G;
-                    v[u] = (rr < r) ? cs[(int64_t)rr * E + e] : 0;
-                }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) t += v[u];
-            }
-            if (t != 0) atomicAdd(&base[e], t);
-        }
-    }
     __syncthreads();
     {
         int run = qx - qlocal + (warp > 0 ? warp_tot[warp - 1] : 0);
@@ -171,28 +222,16 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
         if (tid == kThreads - 1) off[P] = warp_tot[kWarps - 1];
     }
     __syncthreads();
-    {
-        const int nM = ptr[E];
-        const int32_t* ig = inst_id + (int64_t)inst * M;
-        const int32_t* cg = inst_cum + (int64_t)inst * M;
-        for (int m = tid; m < M; m += kThreads) {
-            int cum = INT_MIN, del = 0;
-            if (m < nM) {
-                const int p = ig[m];
-                if (p >= 0 && p < P) {
-                    cum = cg[m];
-                    del = off[p] - (cum - qg[p]);
-                }
-            }
-            bcum[m] = cum;
-            bdel[m] = del;
-        }
+    // row minus within-expert rank of each entry: off[p] - (cum - quota[p]),
+    // with quota[p] = off[p+1] - off[p] (each thread revisits its own entries)
+    for (int m = tid; m < M; m += kThreads) {
+        const int p = bdel[m];
+        bdel[m] = (p >= 0) ? off[p] - (bcum[m] - (off[p + 1] - off[p])) : 0;
     }
     if (r == 0) {
         int32_t* og = inst_offset + (int64_t)inst * (P + 1);
         for (int p = tid; p <= P; p += kThreads) og[p] = off[p];
     }
-
 }
 
 // One block per (instance, source rank); the rank's slots are processed in
@@ -445,6 +484,7 @@ cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T
                               (int)d.E, (int)d.S, counts_src, quota, inst_ptr, inst_id, inst_cum,
                               dst_row, src_slot, inst_offset, dev_status, pdl ? 1 : 0);
 }
+
 
 
 }  // namespace

@@ -312,6 +312,16 @@ def test_full_size_batched_count_and_reroute():
     G().compare(w.R, w.E, w.S, out, orc, check_rows=False)
 
 
+def test_full_size_layer_without_src_slot():
+    # one Qwen3-235B-like layer per launch, as the benchmark's step makes it
+    # (no src_slot output)
+    w = W.WORKLOADS["qwen3-235b"]
+    ids = W.topk_ids(w, 7, 2, device="cuda").cpu().numpy()[None]
+    out = G().gpu_run(U.Domain(w.R, w.E, w.S, w.k), ids, src_slot=False)
+    orc = G().oracle_run(w.R, w.E, w.S, ids)
+    G().compare(w.R, w.E, w.S, out, orc, check_rows=False)
+
+
 @pytest.mark.parametrize("R,S,tpr,s", [(8, 4, 8192, 1.6), (64, 4, 512, 0.6), (32, 2, 2048, 1.0)])
 def test_stress_points(R, S, tpr, s):
     w = W.stress(R, S, tpr, s)
