@@ -481,7 +481,9 @@ def run_ultraep(args, rank, world, local):
                               frac=round(gbs(count_bytes, split["count"]) / peak, 4))
     breakdown["reroute"].update(gbs=round(gbs(reroute_bytes, split["reroute"]), 1),
                                 frac=round(gbs(reroute_bytes, split["reroute"]) / peak, 4))
-    breakdown["plan"].update(n_iter_mean=float(pipe.n_iter.float().mean().item()))
+    n_iter_mean = float(pipe.n_iter.float().mean().item())
+    breakdown["plan"].update(n_iter_mean=n_iter_mean,
+                             us_per_move=round(split["plan"] / max(n_iter_mean, 1.0), 3))
     breakdown["note"] = ("one extra step, outside the timed region, with the four calls made "
                          "separately and an event between each")
 
@@ -531,8 +533,12 @@ def run_ultraep(args, rank, world, local):
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_baseline:
-        cpu = cpu_baseline_sample(w, ids[:args.cpu_layers].cpu().numpy(),
-                                  W.bf16_bits(hiddens[0]))
+        hbits = W.bf16_bits(hiddens[0])
+        cpu = cpu_baseline_sample(w, ids[:args.cpu_layers].cpu().numpy(), hbits)
+        n_thr = min(os.cpu_count() or 1, 16)
+        cpu["nproc"] = os.cpu_count()
+        cpu["cpu_model"] = cpu_model()
+        cpu["all_cores"] = cpu_baseline_threads(w, ids[:n_thr].cpu().numpy(), hbits, n_thr)
 
     line = {"metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 3),
@@ -584,6 +590,92 @@ def cpu_baseline_sample(w, ids_layers, hidden_bits, perm_fraction=8):
                       f"x{perm_fraction}; single-threaded C"}
 
 
+def run_stress_sweep(args):
+    """The stress grid (R in {8,16,32,64}, E = 4R, S in {1,2,4}, k = 8, Zipf
+    s in {0.6,1.0,1.6}) at 2048 tokens per rank, 8 layers each: per layer the
+    planner alone (separate call), the ep_balance call and ep_permute (hidden
+    4096 bf16), with moves per layer and max/mean load before and after."""
+    from moe_expert_load_id_b300 import ultraep as U
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    stream = torch.cuda.current_stream(device)
+    grid = W.STRESS_GRID
+    rows = []
+    for R in grid["R"]:
+        for S in grid["S"]:
+            for sk in grid["s"]:
+                w = dataclasses.replace(W.stress(R, S, 2048, sk), layers=8)
+                ids, hiddens = make_inputs(w, 0, device)
+                pipe = LayerPipeline(U, w, device)
+                L = w.layers
+                pipe.step(ids, hiddens, stream)
+                ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
+                pipe.step(ids, hiddens, stream, ev)
+                sev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(L)]
+                pipe.step_split(ids, hiddens, stream, sev)
+                torch.cuda.synchronize(device)
+                mean = lambda f: float(np.mean([f(l) for l in range(L)]))
+                counts = pipe.counts.cpu().numpy().astype(np.int64)
+                after = pipe.rank_load.cpu().numpy()
+                rows.append({
+                    "R": R, "E": w.E, "S": S, "zipf_s": sk, "T": w.T,
+                    "plan_us": round(mean(lambda l: sev[l][1].elapsed_time(sev[l][2]) * 1000), 2),
+                    "balance_us": round(mean(lambda l: ev[l][0].elapsed_time(ev[l][1]) * 1000), 2),
+                    "permute_us": round(mean(lambda l: ev[l][1].elapsed_time(ev[l][2]) * 1000), 2),
+                    "moves": round(float(pipe.n_iter.float().mean().item()), 1),
+                    "before": round(float(np.median([Q.imbalance(Q.home_load(counts[l], R))
+                                                     for l in range(L)])), 4),
+                    "after": round(float(np.median([Q.imbalance(after[l]) for l in range(L)])), 4),
+                    "status": int(pipe.dev_status.item())})
+                del pipe, ids, hiddens
+                torch.cuda.empty_cache()
+    return {"stress_sweep": rows, "unit": "us per layer (means over 8 layers)",
+            "config": "stress grid at 2048 tokens per rank, k=8, hidden 4096 bf16, 8 layers "
+                      "per point; plan_us = ep_plan as its own call, balance_us = the ep_balance "
+                      "call, permute_us = ep_permute"}
+
+
+def cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def cpu_baseline_threads(w, ids_layers, hidden_bits, threads, perm_fraction=32):
+    """The same oracle on `threads` host threads at once, one layer each (its C
+    calls release the GIL): wall-clock throughput of the whole host.  count +
+    plan + reroute run on every sampled layer in parallel, then permute on the
+    first 1/perm_fraction of each layer's rows in parallel (its wall time scaled
+    up by perm_fraction)."""
+    from concurrent.futures import ThreadPoolExecutor
+    import oracle
+    oracle.lib()
+
+    def cpr(ids):
+        c, _, _ = oracle.count(ids, w.R, w.E)
+        pl = oracle.plan(c, w.R, w.E, w.S)
+        return oracle.reroute(ids, w.R, w.E, w.S, pl)
+
+    with ThreadPoolExecutor(threads) as ex:
+        t0 = time.perf_counter()
+        routes = list(ex.map(cpr, ids_layers))
+        t1 = time.perf_counter()
+        list(ex.map(lambda r: oracle.permute(hidden_bits, w.k, r[1][:int(r[2][-1]) // perm_fraction],
+                                             int(r[2][-1]) // perm_fraction), routes))
+        t2 = time.perf_counter()
+    n = len(ids_layers)
+    value = ((t1 - t0) + (t2 - t1) * perm_fraction) / n * 1e6
+    return {"value": round(value, 1), "unit": UNIT, "threads": threads,
+            "sample": f"{n} layers at once, one per thread: count+plan+reroute on the whole "
+                      f"layer, permute on 1/{perm_fraction} of the rows scaled x{perm_fraction}; "
+                      f"wall clock divided by the layers"}
+
+
 def run_reference(args, rank, world):
     if rank != 0:
         return None
@@ -625,6 +717,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--stress-sweep", action="store_true",
+                    help="instead of the benchmark: planner, ep_balance and ep_permute per layer "
+                         "over the stress grid")
     ap.add_argument("--no-extras", dest="extras", action="store_false",
                     help="skip the batched count/plan/reroute and unpermute timings")
     args = ap.parse_args()
@@ -636,7 +731,9 @@ def main():
         w = dataclasses.replace(w, T=args.tokens or w.T, layers=args.layers or w.layers)
     args.w = w
     rank, world, local = dist_init()
-    if args.impl == "reference":
+    if args.stress_sweep:
+        line = run_stress_sweep(args) if rank == 0 else None
+    elif args.impl == "reference":
         line = run_reference(args, rank, world)
     else:
         line = run_ultraep(args, rank, world, local)

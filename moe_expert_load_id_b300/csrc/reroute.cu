@@ -252,6 +252,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     __shared__ int32_t warp_tot[kWarps];
     __shared__ int32_t flags;
 
+    static_assert(kItems % 4 == 0, "phase C takes four steps at a time");
     const RrLayout lay = rr_layout(R, E, S, kWarps);
     const int P = lay.P, M = lay.M;
     int32_t* off = sm;              // [P+1] first row of each instance
@@ -417,28 +418,51 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         int32_t* dst = dsti + cs;
         auto phase_c = [&](auto full_tag) {
             constexpr bool kFullChunk = decltype(full_tag)::value;
+            // four steps at a time: their rows first (no branch), then the rare
+            // search for ranks past the instance of the warp's first rank
 #pragma unroll
-            for (int it = 0; it < kItems; ++it) {
-                const int li = lbase + it * 32;
-                if (kFullChunk || li < nc) {
-                    const int v = ev[it];
+            for (int it0 = 0; it0 < kItems; it0 += 4) {
+                int d[4];
+                unsigned slow = 0u;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int it = it0 + j;
+                    const int li = lbase + it * 32;
+                    const int v = (kFullChunk || li < nc) ? ev[it] : -1;
                     const bool has = v >= 0;
                     const int e = has ? (v & 1023) : 0;
                     const int rr = v >> 10;
-                    int d = dbrow[e] + rr;
-                    if (has && rr >= (int)limrow[e]) {
-                        const int x = wrow[e] + rr;
-                        const int end = ptr[e + 1];
-                        const int m = upper_bound(bcum, ptr[e], end, x);
-                        d = (m < end) ? x + bdel[m < M ? m : M - 1] : -1;
+                    d[j] = dbrow[e] + rr;
+                    slow |= (has && rr >= (int)limrow[e]) ? (1u << j) : 0u;
+                }
+                if (slow) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        if ((slow >> j) & 1u) {
+                            const int v = ev[it0 + j];
+                            const int e = v & 1023, rr = v >> 10;
+                            const int x = wrow[e] + rr;
+                            const int end = ptr[e + 1];
+                            const int m = upper_bound(bcum, ptr[e], end, x);
+                            d[j] = (m < end) ? x + bdel[m < M ? m : M - 1] : -1;
+                        }
                     }
-                    if (has && (unsigned)d >= (unsigned)N) {
-                        d = -1;
-                        my_flags |= EP_DEV_QUOTA_OVERFLOW;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int it = it0 + j;
+                    const int li = lbase + it * 32;
+                    if (kFullChunk || li < nc) {
+                        const bool has = ev[it] >= 0;
+                        int dd = d[j];
+                        if (has && (unsigned)dd >= (unsigned)N) {
+                            dd = -1;
+                            my_flags |= EP_DEV_QUOTA_OVERFLOW;
+                        }
+                        dd = has ? dd : -1;
+                        __stcs(dst + li, dd);
+                        if (srci != nullptr && dd >= 0) srci[dd] = (int32_t)(cs + li);
                     }
-                    d = has ? d : -1;
-                    __stcs(dst + li, d);
-                    if (srci != nullptr && d >= 0) srci[d] = (int32_t)(cs + li);
                 }
             }
         };
