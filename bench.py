@@ -140,6 +140,12 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def whole_job_us_per_layer(max_ms, steps, layers, world):
+    """The metric over all ranks: every rank runs `steps` steps of `layers`
+    layers (its own microbatch); the slowest rank's time over all layers run."""
+    return max_ms * 1000.0 / (steps * layers * world)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
@@ -438,7 +444,7 @@ def run_ultraep(args, rank, world, local):
     total_ms = step_ev[0].elapsed_time(step_ev[-1])
     total_ms = max_over_ranks(total_ms, world, device)
     ms_per_step = total_ms / args.steps
-    value = total_ms * 1000.0 / (args.steps * L * world)
+    value = whole_job_us_per_layer(total_ms, args.steps, L, world)
 
     per = {"balance": [], "permute": []}
     for k in range(args.steps):
