@@ -52,14 +52,22 @@ namespace {
 #define EP_REROUTE_BLOCKS_PER_SM 4
 #endif
 constexpr int kItems = EP_REROUTE_ITEMS;
+// Where a chunk's ids (and then their ranks) live: registers, or shared
+// memory, which frees kItems registers per thread.  Measured: the one-layer
+// launch (1024-thread blocks) 22.5 us with shared memory against 24.6, the
+// batched launch (256-thread blocks) 407.5 us with registers against 411.7
+// (five blocks per SM) to 421.9 (four).
+template <int kThreads>
+constexpr bool ev_in_smem() { return kThreads == 1024; }
 
 struct RrLayout {
     int P, M;        // instances, CSR capacity
     size_t lim_off;  // byte offset of the uint16 table wlim
+    size_t ev_off;   // byte offset of the ids of a chunk (when in shared memory)
     size_t bytes;
 };
 
-__host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps) {
+__host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps, bool ev_smem) {
     RrLayout l;
     l.P = R * (E / R + S);
     l.M = E + R * S;
@@ -68,6 +76,8 @@ __host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps) {
     l.lim_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
                                    2 * (size_t)warps * E);
     l.bytes = l.lim_off + sizeof(uint16_t) * (size_t)warps * E;
+    l.ev_off = (l.bytes + 15) & ~(size_t)15;
+    if (ev_smem) l.bytes = l.ev_off + sizeof(int32_t) * (size_t)kItems * warps * 32;
     return l;
 }
 
@@ -253,7 +263,8 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     __shared__ int32_t flags;
 
     static_assert(kItems % 4 == 0, "phase C takes four steps at a time");
-    const RrLayout lay = rr_layout(R, E, S, kWarps);
+    constexpr bool kEvSmem = ev_in_smem<kThreads>();
+    const RrLayout lay = rr_layout(R, E, S, kWarps, kEvSmem);
     const int P = lay.P, M = lay.M;
     int32_t* off = sm;              // [P+1] first row of each instance
     int32_t* ptr = off + (P + 1);   // [E+1] CSR row pointers (clamped)
@@ -276,7 +287,18 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     const int64_t s0 = min(T, (int64_t)r * Tr) * k, s1 = min(T, (int64_t)(r + 1) * Tr) * k;
     const int32_t* idi = ids + (int64_t)inst * N;
     int my_flags = 0;
-    int ev[kItems];
+    // item it of this thread: a register, or word it * kThreads + tid of the
+    // chunk's shared array (consecutive threads, consecutive banks)
+    int evr[kEvSmem ? 1 : kItems] = {};
+    int* evs = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(sm) + lay.ev_off) + threadIdx.x;
+    auto ev_get = [&](int it) -> int {
+        if constexpr (kEvSmem) return evs[it * kThreads];
+        else return evr[it];
+    };
+    auto ev_set = [&](int it, int v) {
+        if constexpr (kEvSmem) evs[it * kThreads] = v;
+        else evr[it] = v;
+    };
     const int lbase = warp * 32 * kItems + lane;  // chunk-local index of item 0
     auto load_chunk = [&](int64_t cs) {
         const int nc = (int)min((int64_t)kChunk, s1 - cs);
@@ -286,7 +308,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             const int li = lbase + it * 32;
             const int v = (li < nc) ? __ldcs(src + li) : -1;
             if (li < nc && (unsigned)v >= (unsigned)E) my_flags |= EP_DEV_BAD_ID;
-            ev[it] = v;
+            ev_set(it, v);
         }
     };
     // ---- shared tables that phase A needs: zero them first
@@ -306,7 +328,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * E;
 #pragma unroll
         for (int it = 0; it < kItems; ++it) {
-            const int e = ev[it];
+            const int e = ev_get(it);
             const bool valid = (unsigned)e < (unsigned)E;
             if (valid) atomicOr(&mrow[e], 1u << lane);
             __syncwarp();
@@ -321,7 +343,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             }
             __syncwarp();  // the clear lands before the next step's ORs
             old = __shfl_sync(kFull, old, leader & 31);
-            ev[it] = valid ? (e | ((old + __popc(g & lt)) << 10)) : -1;
+            ev_set(it, valid ? (e | ((old + __popc(g & lt)) << 10)) : -1);
         }
     };
     // early (ep_balance): this grid is a programmatic dependent of ep_plan and
@@ -428,7 +450,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
                 for (int j = 0; j < 4; ++j) {
                     const int it = it0 + j;
                     const int li = lbase + it * 32;
-                    const int v = (kFullChunk || li < nc) ? ev[it] : -1;
+                    const int v = (kFullChunk || li < nc) ? ev_get(it) : -1;
                     const bool has = v >= 0;
                     const int e = has ? (v & 1023) : 0;
                     const int rr = v >> 10;
@@ -439,7 +461,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         if ((slow >> j) & 1u) {
-                            const int v = ev[it0 + j];
+                            const int v = ev_get(it0 + j);
                             const int e = v & 1023, rr = v >> 10;
                             const int x = wrow[e] + rr;
                             const int end = ptr[e + 1];
@@ -453,7 +475,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
                     const int it = it0 + j;
                     const int li = lbase + it * 32;
                     if (kFullChunk || li < nc) {
-                        const bool has = ev[it] >= 0;
+                        const bool has = ev_get(it) >= 0;
                         int dd = d[j];
                         if (has && (unsigned)dd >= (unsigned)N) {
                             dd = -1;
@@ -487,7 +509,7 @@ cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T
                              const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
                              int32_t* inst_offset, int32_t* dev_status, cudaStream_t s,
                              bool pdl) {
-    const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32);
+    const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32, ev_in_smem<kThreads>());
     if (lay.bytes > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
