@@ -57,8 +57,11 @@ constexpr int kItems = EP_REROUTE_ITEMS;
 // launch (1024-thread blocks) 22.5 us with shared memory against 24.6, the
 // batched launch (256-thread blocks) 407.5 us with registers against 411.7
 // (five blocks per SM) to 421.9 (four).
+#ifndef EP_REROUTE_EV_SMEM_NARROW
+#define EP_REROUTE_EV_SMEM_NARROW 0  // build-time tunable: also for 256-thread blocks
+#endif
 template <int kThreads>
-constexpr bool ev_in_smem() { return kThreads == 1024; }
+constexpr bool ev_in_smem() { return kThreads == 1024 || EP_REROUTE_EV_SMEM_NARROW; }
 
 struct RrLayout {
     int P, M;        // instances, CSR capacity
@@ -322,8 +325,9 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     // e | rank << 10 (-1: no valid id).  The lanes holding the same id find
     // each other through the warp's mask row (the wdb row, idle until phase
     // B): each ORs its lane bit into mask[e]; after a warp barrier mask[e] is
-    // the group.  The group's lowest lane (leader) advances the warp's running
-    // count of e and clears mask[e] for the next step.
+    // the group.  Every lane of the group reads the warp's running count of e;
+    // after a second barrier the group's lowest lane (leader) advances it and
+    // clears mask[e] for the next step.
     auto phase_a = [&]() {
         uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * E;
 #pragma unroll
@@ -332,18 +336,18 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             const bool valid = (unsigned)e < (unsigned)E;
             if (valid) atomicOr(&mrow[e], 1u << lane);
             __syncwarp();
+            // every lane of the group reads the group and the running count
+            // itself (no shuffle from the leader), both loads at once
             const unsigned g = valid ? mrow[e] : 0u;
-            const int leader = __ffs(g) - 1;
-            __syncwarp();
-            int old = 0;
-            if (valid && lane == leader) {
-                old = wrow[e];
+            const int old = valid ? wrow[e] : 0;
+            const unsigned below = g & lt;
+            __syncwarp();  // every read of mrow[e] and wrow[e] is done
+            if (valid && below == 0u) {  // the group's lowest lane
                 wrow[e] = old + __popc(g);
                 mrow[e] = 0u;
             }
             __syncwarp();  // the clear lands before the next step's ORs
-            old = __shfl_sync(kFull, old, leader & 31);
-            ev_set(it, valid ? (e | ((old + __popc(g & lt)) << 10)) : -1);
+            ev_set(it, valid ? (e | ((old + __popc(below)) << 10)) : -1);
         }
     };
     // early (ep_balance): this grid is a programmatic dependent of ep_plan and
@@ -543,8 +547,12 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
                            bool pdl) {
     if (n_inst == 0) return cudaSuccess;
     const int64_t blocks = (int64_t)n_inst * d.R;
-    const int sms = device_info().sms;
-    if (blocks >= 2 * (int64_t)sms || d.E > 512)
+    const DeviceInfo di = device_info();
+    const int sms = di.sms;
+    // wide blocks only when their tables (and the chunk's ids) fit in shared memory
+    const bool wide_fits =
+        rr_layout(d.R, d.E, d.S, 1024 / 32, ev_in_smem<1024>()).bytes + 1024 <= di.smem_optin;
+    if (blocks >= 2 * (int64_t)sms || d.E > 512 || !wide_fits)
         return launch_reroute_t<256>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
                                       inst_cum, dst_row, src_slot, inst_offset, dev_status, s, pdl);
     return launch_reroute_t<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,

@@ -128,6 +128,7 @@ CASES = [
     # invalid ids, and with ranks that do not start on a 16-byte boundary
     ("E256_bad_ids",       8,  32, 0, 8, 3001,  2,      8,   "bad"),
     ("E320_mask_kernel",   16, 20, 2, 8, 3000,  1,      8,   "zipf"),
+    ("E512_one_layer",     16, 32, 0, 8, 3000,  1,      8,   "zipf"),   # wide blocks do not fit
     ("runs_many_rounds",   2,  8, 1, 8,  20000, 1,      8,   "zipf"),
     ("runs_batched_bad",   8,  4, 1, 4,  3001,  40,     8,   "bad"),
     ("runs_batched_unaligned", 8, 4, 1, 3, 1001, 40,    8,   "zipf"),
