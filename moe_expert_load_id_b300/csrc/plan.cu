@@ -11,7 +11,10 @@
 // least-loaded eligible rank, q = min(quota, floor(gap/2)), global stop).
 //
 // One warp per (layer, microbatch) instance.  The moves form one serial
-// chain, so the design goal is the shortest dependent path per move:
+// chain, so the design goal is the shortest dependent path per move.  Two
+// move loops implement the rule: plan_moves on registers (below) and, for the
+// flag-free rule with more than four instances per rank, plan_moves_table on
+// a shared-memory table (see there).  The register loop:
 //   - lane l owns ranks l and l+32 and keeps, in registers, each rank's load,
 //     its instances (quota and expert, unrolled over a compile-time bound WB on
 //     H+S) and its largest instance;
@@ -24,8 +27,8 @@
 //     touches no shared memory at all;
 //   - every lane runs the same branch-free update on its own registers (a
 //     no-op unless it owns hot or cold), so the warp never diverges.
-// Shared memory is used only after the loop, to build the logical->physical
-// CSR table.
+// The register loop uses shared memory only after the loop, to build the
+// logical->physical CSR table.
 #include <climits>
 
 #include "common.cuh"
@@ -265,6 +268,112 @@ __device__ __forceinline__ void plan_moves(RankRegs<WB>& A, RankRegs<WB>& B, int
     }
 }
 
+
+// The base rule on a shared-memory table (the flag-free kernel): the warp's
+// instance quotas q[P] (rank-major, W per rank), the experts of the spare
+// slots slot[R*S] (-1: empty) and, per expert, the mask of ranks holding it;
+// the loads stay in registers (lane l: ranks l and l+32).  Per move the hot
+// rank's largest instance is one warp reduction over its W instances (lane j:
+// instance j), eligibility is one 64-bit mask (holders of e | ranks with a
+// free slot), and the bookkeeping is a few single-lane stores, so nothing in a
+// move grows with the instances per rank.  Same rule, same ties, same outputs
+// as plan_moves with no flags; the tables are exactly the epilogue's.
+template <bool kTwo, bool kPacked>
+__device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint64_t* holder,
+                                                 int& loadA, int& loadB, int lane, int H, int S,
+                                                 int W, int R, int max_iters, int& iters,
+                                                 int& status) {
+    const bool hasA = loadA >= 0, hasB = kTwo && loadB >= 0;
+    const int ra = lane, rb = lane + 32;
+    const uint64_t exist = (R >= 64) ? ~0ull : ((1ull << R) - 1ull);
+    uint64_t freem = S > 0 ? exist : 0ull;  // ranks with a free spare slot (warp-uniform)
+    int hot, Lmax;
+    argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, hot, Lmax);
+    while (true) {
+        // 2. hot's largest-quota instance, lowest expert on ties (lane j:
+        // instance j; every rank has its H >= 1 home instances)
+        int qj = -1;
+        unsigned cxj = 0xffffffffu;
+        if (lane < W) {
+            const int xj = lane < H ? hot * H + lane : slot[hot * S + (lane - H)];
+            if (xj >= 0) {
+                qj = q[hot * W + lane];
+                cxj = ((unsigned)xj << 5) | (unsigned)lane;
+            }
+        }
+        const int qmax = __reduce_max_sync(kFull, qj);
+        const unsigned cx = __reduce_min_sync(kFull, qj == qmax ? cxj : 0xffffffffu);
+        const int e = (int)(cx >> 5), src_j = (int)(cx & 31u);
+
+        // 3-5. eligible ranks: the others that hold e or have a free slot;
+        // the coldest of them (lowest rank on ties) and the amount
+        const uint64_t hm = holder[e];
+        const uint64_t el = (hm | freem) & exist & ~(1ull << hot);
+        if (el == 0ull) break;  // no rank is eligible
+        const bool elA = hasA && ((el >> ra) & 1ull);
+        const bool elB = hasB && ((el >> rb) & 1ull);
+        int cold, Lmin;
+        if (kPacked) {
+            const unsigned ca = elA ? ((unsigned)loadA << 6) | (unsigned)ra : 0xffffffffu;
+            const unsigned cb = elB ? ((unsigned)loadB << 6) | (unsigned)rb : 0xffffffffu;
+            const unsigned kk = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            cold = (int)(kk & 63u);
+            Lmin = (int)(kk >> 6);
+        } else {
+            const int ca = elA ? loadA : INT_MAX;
+            const int cb = elB ? loadB : INT_MAX;
+            Lmin = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            const unsigned b0 = __ballot_sync(kFull, elA && ca == Lmin);
+            const unsigned b1 = kTwo ? __ballot_sync(kFull, elB && cb == Lmin) : 0u;
+            cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+        }
+        const int mv = min(qmax, (Lmax - Lmin) >> 1);
+        if (mv <= 0) break;  // the global stop
+        // 6. safety cap
+        if (iters == max_iters) {
+            status = EP_ERR_ITER_LIMIT;
+            break;
+        }
+        // 7. move.  Loads first, then the next move's argmax ...
+        loadA += (ra == cold ? mv : 0) - (ra == hot ? mv : 0);
+        if (kTwo) loadB += (rb == cold ? mv : 0) - (rb == hot ? mv : 0);
+        int nhot, nLmax;
+        argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, nhot, nLmax);
+        // ... and the tables: cold's instance of e is its home, a spare slot
+        // already holding e, or its lowest free spare slot (filled now)
+        const bool held = (hm >> cold) & 1ull;
+        int dj;
+        unsigned freeb = 0u;  // cold's free spare slots (bit s)
+        if (held && e / H == cold) {
+            dj = e - cold * H;
+        } else {
+            const int sv = (lane < S) ? slot[cold * S + lane] : 0;
+            const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
+            freeb = __ballot_sync(kFull, lane < S && sv < 0);
+            const unsigned pick = held ? hit : freeb;  // nonzero: cold is eligible
+            if (pick == 0u) {                          // (never; keeps every index in range)
+                status = EP_ERR_INVAL;
+                break;
+            }
+            dj = H + __ffs(pick) - 1;
+        }
+        __syncwarp();  // every read of this move's table entries is done
+        if (lane == 0) {
+            q[hot * W + src_j] -= mv;
+            q[cold * W + dj] += mv;
+            if (!held) {
+                slot[cold * S + (dj - H)] = e;
+                holder[e] = hm | (1ull << cold);
+            }
+        }
+        if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
+        __syncwarp();  // the stores land before the next move reads the table
+        hot = nhot;
+        Lmax = nLmax;
+        ++iters;
+    }
+}
+
 template <int WB>
 __device__ __forceinline__ void init_rank(RankRegs<WB>& X, int rk, int R, int H, int W,
                                           const int32_t* cnt) {
@@ -338,23 +447,6 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
         if (bad || tot > (long long)INT_MAX) status = EP_ERR_INVAL;
     }
 
-    // registers of ranks lane (A) and lane+32 (B)
-    RankRegs<WB> A, B;
-    init_rank(A, lane, R, H, W, cnt);
-    init_rank(B, lane + 32, R, H, W, cnt);
-
-    int iters = 0;
-    if (status == EP_OK) {
-        if (tot < kPackLimit)
-            plan_moves<WB, kTwo, true, kFlags>(A, B, lane, H, S, W, R, max_iters, flags, iters,
-                                               status);
-        else
-            plan_moves<WB, kTwo, false, kFlags>(A, B, lane, H, S, W, R, max_iters, flags, iters,
-                                                status);
-    }
-
-    // ---- outputs: quota, spare slots and loads straight from registers; the
-    // CSR is built from a shared-memory copy
     unsigned char* base = smem + (size_t)warp * plan_warp_bytes(R, E, S);
     int32_t* q = reinterpret_cast<int32_t*>(base);
     int32_t* slot = reinterpret_cast<int32_t*>(base + align16((size_t)P * 4));
@@ -362,10 +454,65 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
                                                    align16((size_t)R * S * 4));
     int32_t* qo = quota_out + (int64_t)g * P;
     int32_t* so = slot_out + (int64_t)g * R * S;
-    for (int e = lane; e < E; e += 32) holder[e] = 1ull << (e / H);
-    __syncwarp();
-    store_rank(A, lane, R, H, S, W, q, slot, holder, qo, so, load_out + (int64_t)g * R);
-    store_rank(B, lane + 32, R, H, S, W, q, slot, holder, qo, so, load_out + (int64_t)g * R);
+    int32_t* lo = load_out + (int64_t)g * R;
+    int iters = 0;
+    // the base rule with more than four instances per rank runs on the
+    // shared-memory table (its moves cost the same whatever W; measured 0.48 us
+    // per move at W = 6 against 0.70 on registers); up to four, and for the
+    // variants, the register loop (0.46 us per move at W = 3 against 0.47)
+    if constexpr (!kFlags && WB > 4) {
+        // ---- the base rule on the shared-memory table
+        for (int p = lane; p < P; p += 32) {
+            const int r = p / W, j = p - r * W;
+            q[p] = j < H ? cnt[r * H + j] : 0;
+        }
+        for (int x = lane; x < R * S; x += 32) slot[x] = -1;
+        for (int e = lane; e < E; e += 32) holder[e] = 1ull << (e / H);
+        int loadA = -1, loadB = -1;
+        if (lane < R) {
+            unsigned sum = 0;
+            for (int j = 0; j < H; ++j) sum += (unsigned)cnt[lane * H + j];
+            loadA = (int)sum;
+        }
+        if (kTwo && lane + 32 < R) {
+            unsigned sum = 0;
+            for (int j = 0; j < H; ++j) sum += (unsigned)cnt[(lane + 32) * H + j];
+            loadB = (int)sum;
+        }
+        __syncwarp();
+        if (status == EP_OK) {
+            if (tot < kPackLimit)
+                plan_moves_table<kTwo, true>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
+                                             max_iters, iters, status);
+            else
+                plan_moves_table<kTwo, false>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
+                                              max_iters, iters, status);
+        }
+        __syncwarp();
+        for (int p = lane; p < P; p += 32) qo[p] = q[p];
+        for (int x = lane; x < R * S; x += 32) so[x] = slot[x];
+        if (lane < R) lo[lane] = loadA;
+        if (kTwo && lane + 32 < R) lo[lane + 32] = loadB;
+    } else {
+        // ---- registers: ranks lane (A) and lane+32 (B)
+        RankRegs<WB> A, B;
+        init_rank(A, lane, R, H, W, cnt);
+        init_rank(B, lane + 32, R, H, W, cnt);
+        if (status == EP_OK) {
+            if (tot < kPackLimit)
+                plan_moves<WB, kTwo, true, kFlags>(A, B, lane, H, S, W, R, max_iters, flags,
+                                                   iters, status);
+            else
+                plan_moves<WB, kTwo, false, kFlags>(A, B, lane, H, S, W, R, max_iters, flags,
+                                                    iters, status);
+        }
+        // outputs: quota, spare slots and loads straight from registers; the CSR
+        // is built from a shared-memory copy
+        for (int e = lane; e < E; e += 32) holder[e] = 1ull << (e / H);
+        __syncwarp();
+        store_rank(A, lane, R, H, S, W, q, slot, holder, qo, so, lo);
+        store_rank(B, lane + 32, R, H, S, W, q, slot, holder, qo, so, lo);
+    }
     __syncwarp();
 
     // logical -> physical CSR: home first, then replicas by ascending rank (= ascending p)
