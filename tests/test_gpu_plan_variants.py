@@ -125,3 +125,40 @@ def test_full_size_layer_skip():
     _same(got, 0, want)
     base = oracle.plan(c, w.R, w.E, w.S)
     assert want["rank_load"].max() <= base["rank_load"].max()
+
+
+# The flag-free rule with more than four instances per rank runs the planner's
+# shared-memory table loop; these shapes (W = H + S from 5 to 12, one and two
+# ranks per lane, both key widths) pin it to the oracle on random counts and
+# under caps.
+TABLE_SHAPES = [(3, 4, 1), (8, 4, 2), (33, 2, 3), (64, 4, 4), (64, 8, 4), (16, 4, 8)]
+
+
+@pytest.mark.parametrize("shape", TABLE_SHAPES, ids=[f"R{r}H{h}S{s}" for r, h, s in TABLE_SHAPES])
+def test_base_rule_table_loop(shape):
+    R, H, S = shape
+    E = R * H
+    rng = np.random.default_rng(R * 100 + H * 10 + S)
+    c = np.stack([(400.0 / (1 + rng.permutation(E)) ** rng.uniform(0.5, 1.6)).astype(np.int32)
+                  for _ in range(16)])
+    got = _gpu_plan(R, E, S, c, 0)
+    for g in range(c.shape[0]):
+        _same(got, g, oracle.plan(c[g], R, E, S))
+    # caps: the state after exactly `cap` moves, flagged
+    full = min(int(oracle.plan(c[g], R, E, S)["n_iter"]) for g in range(c.shape[0]))
+    for cap in (1, max(1, full // 2)):
+        got = _gpu_plan(R, E, S, c, 0, cap)
+        for g in range(c.shape[0]):
+            _same(got, g, oracle.plan(c[g], R, E, S, max_iters=cap))
+
+
+def test_base_rule_table_loop_wide_keys():
+    # totals of 2^25 and more take the planner's unpacked reductions
+    R, H, S = 64, 4, 2
+    E = R * H
+    rng = np.random.default_rng(5)
+    c = (rng.random((4, E)) ** 3 * 2.0e6).astype(np.int32)
+    assert (c.sum(1) >= (1 << 25)).all()
+    got = _gpu_plan(R, E, S, c, 0)
+    for g in range(c.shape[0]):
+        _same(got, g, oracle.plan(c[g], R, E, S))
