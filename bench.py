@@ -37,7 +37,8 @@ from moe_expert_load_id_b300 import quality as Q  # noqa: E402
 WORKLOAD = "qwen3-235b"
 METRIC = "µs per MoE layer (count+plan+reroute+permute) at EP64"
 UNIT = "us/layer"
-N_HIDDEN_BUFS = 2  # distinct hidden inputs, alternating by layer (each 1.07 GB > L2)
+N_HIDDEN_BUFS = 2  # distinct hidden inputs (each 1.07 GB > L2): the first half of the
+                   # layers reads buffer 0, the second half buffer 1
 
 # DRAM traffic of one ep_permute launch on this workload, from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum), valid for the permute source
@@ -220,14 +221,21 @@ class LayerPipeline:
         U.ep_permute(hidden_l, d.k, self.dst_row, self.grouped, self.dev_status, stream)
         ev[4].record(stream)
 
-    def step(self, ids, hiddens, stream, events=None):
+    def hidden_of(self, l, hiddens):
+        return hiddens[l * len(hiddens) // self.w.layers]
+
+    def step(self, ids, hiddens, stream, events=None, ready=None):
+        """ready: optional {layer: event} the stream waits for before that layer
+        (inputs still being copied in)."""
         for l in range(self.w.layers):
-            self.layer(l, ids[l:l + 1], hiddens[l % len(hiddens)][None], stream,
+            if ready is not None and l in ready:
+                stream.wait_event(ready[l])
+            self.layer(l, ids[l:l + 1], self.hidden_of(l, hiddens)[None], stream,
                        None if events is None else events[l])
 
     def step_split(self, ids, hiddens, stream, events):
         for l in range(self.w.layers):
-            self.layer_split(l, ids[l:l + 1], hiddens[l % len(hiddens)][None], stream, events[l])
+            self.layer_split(l, ids[l:l + 1], self.hidden_of(l, hiddens)[None], stream, events[l])
 
     def results(self):
         """The step's result the host reads back: per-layer plan outcome."""
@@ -504,11 +512,26 @@ def run_ultraep(args, rank, world, local):
         h2d = ids_h.numel() * 4 + sum(h.numel() * 2 for h in hid_h)
         d2h = sum(t.numel() * t.element_size() for t in res_h)
 
+        # the inputs of each half of the layers are copied in on a second
+        # stream, the first half's before the step starts and the second
+        # half's while the first half runs; the next step's copies wait for
+        # this step's layers (they overwrite the same device buffers)
+        copy_stream = torch.cuda.Stream(device)
+        half = max(1, L // 2)
+
         def e2e_step():
-            ids_d.copy_(ids_h, non_blocking=True)
-            for d_, h_ in zip(hid_d, hid_h):
-                d_.copy_(h_, non_blocking=True)
-            pipe.step(ids_d, hid_d, stream)
+            copy_stream.wait_stream(stream)
+            with torch.cuda.stream(copy_stream):
+                hid_d[0].copy_(hid_h[0], non_blocking=True)
+                ids_d[:half].copy_(ids_h[:half], non_blocking=True)
+                first = torch.cuda.Event()
+                first.record(copy_stream)
+                for d_, h_ in zip(hid_d[1:], hid_h[1:]):
+                    d_.copy_(h_, non_blocking=True)
+                ids_d[half:].copy_(ids_h[half:], non_blocking=True)
+                second = torch.cuda.Event()
+                second.record(copy_stream)
+            pipe.step(ids_d, hid_d, stream, ready={0: first, half: second})
             for h_, d_ in zip(res_h, pipe.results()):
                 h_.copy_(d_, non_blocking=True)
 
