@@ -224,14 +224,16 @@ class LayerPipeline:
     def hidden_of(self, l, hiddens):
         return hiddens[l * len(hiddens) // self.w.layers]
 
-    def step(self, ids, hiddens, stream, events=None, ready=None):
+    def step(self, ids, hiddens, stream, events=None, ready=None, done=None):
         """ready: optional {layer: event} the stream waits for before that layer
-        (inputs still being copied in)."""
+        (inputs still being copied in); done: {layer: event} recorded after it."""
         for l in range(self.w.layers):
             if ready is not None and l in ready:
                 stream.wait_event(ready[l])
             self.layer(l, ids[l:l + 1], self.hidden_of(l, hiddens)[None], stream,
                        None if events is None else events[l])
+            if done is not None and l in done:
+                done[l].record(stream)
 
     def step_split(self, ids, hiddens, stream, events):
         for l in range(self.w.layers):
@@ -512,26 +514,35 @@ def run_ultraep(args, rank, world, local):
         h2d = ids_h.numel() * 4 + sum(h.numel() * 2 for h in hid_h)
         d2h = sum(t.numel() * t.element_size() for t in res_h)
 
-        # the inputs of each half of the layers are copied in on a second
-        # stream, the first half's before the step starts and the second
-        # half's while the first half runs; the next step's copies wait for
-        # this step's layers (they overwrite the same device buffers)
+        # the inputs are copied in on a second stream, half of the layers' at a
+        # time: a step's first-half inputs as soon as the previous step's
+        # first half of the layers is done with those device buffers, its
+        # second-half inputs once the previous step is done; the layers wait
+        # on events.  Every step's inputs are copied inside the timed region.
         copy_stream = torch.cuda.Stream(device)
         half = max(1, L // 2)
+        free = {}
 
         def e2e_step():
-            copy_stream.wait_stream(stream)
             with torch.cuda.stream(copy_stream):
+                if "first" in free:
+                    copy_stream.wait_event(free["first"])
+                else:
+                    copy_stream.wait_stream(stream)
                 hid_d[0].copy_(hid_h[0], non_blocking=True)
                 ids_d[:half].copy_(ids_h[:half], non_blocking=True)
                 first = torch.cuda.Event()
                 first.record(copy_stream)
+                if "second" in free:
+                    copy_stream.wait_event(free["second"])
                 for d_, h_ in zip(hid_d[1:], hid_h[1:]):
                     d_.copy_(h_, non_blocking=True)
                 ids_d[half:].copy_(ids_h[half:], non_blocking=True)
                 second = torch.cuda.Event()
                 second.record(copy_stream)
-            pipe.step(ids_d, hid_d, stream, ready={0: first, half: second})
+            free["first"], free["second"] = torch.cuda.Event(), torch.cuda.Event()
+            pipe.step(ids_d, hid_d, stream, ready={0: first, half: second},
+                      done={half - 1: free["first"], L - 1: free["second"]})
             for h_, d_ in zip(res_h, pipe.results()):
                 h_.copy_(d_, non_blocking=True)
 
@@ -540,6 +551,7 @@ def run_ultraep(args, rank, world, local):
         barrier(world)
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        copy_stream.wait_event(e0)  # no timed copy starts before the timed region
         for _ in range(args.e2e_steps):
             e2e_step()
         e1.record(stream)
