@@ -12,9 +12,9 @@
 //
 // One warp per (layer, microbatch) instance.  The moves form one serial
 // chain, so the design goal is the shortest dependent path per move.  Two
-// move loops implement the rule: plan_moves on registers (below) and, for the
-// flag-free rule with more than four instances per rank, plan_moves_table on
-// a shared-memory table (see there).  The register loop:
+// move loops implement the rule: plan_moves_table on a shared-memory table
+// (see there) runs the flag-free rule, plan_moves on registers (below) the
+// variants of ep_plan_ex.  The register loop:
 //   - lane l owns ranks l and l+32 and keeps, in registers, each rank's load,
 //     its instances (quota and expert, unrolled over a compile-time bound WB on
 //     H+S) and its largest instance;
@@ -37,6 +37,11 @@ namespace ultraep {
 namespace {
 
 constexpr int kPlanWarps = 4;
+// the flag-free rule runs the shared-memory table loop from this register
+// bound on (build-time tunable; the bounds are 2, 3, 4, 6, 8, 16, 32; 2: always)
+#ifndef EP_PLAN_TABLE_MIN_WB
+#define EP_PLAN_TABLE_MIN_WB 2
+#endif
 constexpr long long kPackLimit = 1ll << 25;  // total below this: loads fit a 6-bit-shifted key
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
@@ -294,10 +299,11 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         // instance j; every rank has its H >= 1 home instances)
         int qj = -1;
         unsigned cxj = 0xffffffffu;
-        if (lane < W) {
+        if (lane < W) {  // the two loads are independent
             const int xj = lane < H ? hot * H + lane : slot[hot * S + (lane - H)];
+            const int qv = q[hot * W + lane];
             if (xj >= 0) {
-                qj = q[hot * W + lane];
+                qj = qv;
                 cxj = ((unsigned)xj << 5) | (unsigned)lane;
             }
         }
@@ -340,34 +346,34 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         int nhot, nLmax;
         argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, nhot, nLmax);
         // ... and the tables: cold's instance of e is its home, a spare slot
-        // already holding e, or its lowest free spare slot (filled now)
+        // already holding e, or its lowest free spare slot (filled now).  The
+        // spare slots are read and voted on unconditionally (no branch), so
+        // this overlaps the argmax above.
+        const int sv = (lane < S) ? slot[cold * S + lane] : 0;
+        const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
+        const unsigned freeb = __ballot_sync(kFull, lane < S && sv < 0);  // cold's free slots
         const bool held = (hm >> cold) & 1ull;
-        int dj;
-        unsigned freeb = 0u;  // cold's free spare slots (bit s)
-        if (held && e / H == cold) {
-            dj = e - cold * H;
-        } else {
-            const int sv = (lane < S) ? slot[cold * S + lane] : 0;
-            const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
-            freeb = __ballot_sync(kFull, lane < S && sv < 0);
-            const unsigned pick = held ? hit : freeb;  // nonzero: cold is eligible
-            if (pick == 0u) {                          // (never; keeps every index in range)
-                status = EP_ERR_INVAL;
-                break;
-            }
-            dj = H + __ffs(pick) - 1;
+        const int ej = e - cold * H;
+        const bool home = (unsigned)ej < (unsigned)H;  // e is one of cold's home experts
+        const unsigned pick = held ? hit : freeb;       // nonzero unless home: cold is eligible
+        if (!home && pick == 0u) {                      // (never; keeps every index in range)
+            status = EP_ERR_INVAL;
+            break;
         }
-        __syncwarp();  // every read of this move's table entries is done
+        const int dj = home ? ej : H + __ffs(pick) - 1;
+        // every read of this move was consumed by the warp's votes and
+        // reductions above; the updates are fire-and-forget shared-memory
+        // additions, no read-modify-write chain
         if (lane == 0) {
-            q[hot * W + src_j] -= mv;
-            q[cold * W + dj] += mv;
+            atomicAdd(&q[hot * W + src_j], -mv);
+            atomicAdd(&q[cold * W + dj], mv);
             if (!held) {
                 slot[cold * S + (dj - H)] = e;
                 holder[e] = hm | (1ull << cold);
             }
         }
         if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
-        __syncwarp();  // the stores land before the next move reads the table
+        __syncwarp();  // the updates land before the next move reads the table
         hot = nhot;
         Lmax = nLmax;
         ++iters;
@@ -456,11 +462,10 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     int32_t* so = slot_out + (int64_t)g * R * S;
     int32_t* lo = load_out + (int64_t)g * R;
     int iters = 0;
-    // the base rule with more than four instances per rank runs on the
-    // shared-memory table (its moves cost the same whatever W; measured 0.48 us
-    // per move at W = 6 against 0.70 on registers); up to four, and for the
-    // variants, the register loop (0.46 us per move at W = 3 against 0.47)
-    if constexpr (!kFlags && WB > 4) {
+    // the base rule runs on the shared-memory table (a move costs the same
+    // whatever W: measured 0.38-0.39 us per move at W = 3 and 6, against 0.46
+    // and 0.70 on registers); the variants run the register loop
+    if constexpr (!kFlags && WB >= EP_PLAN_TABLE_MIN_WB) {
         // ---- the base rule on the shared-memory table
         for (int p = lane; p < P; p += 32) {
             const int r = p / W, j = p - r * W;
