@@ -38,7 +38,10 @@ namespace cg = cooperative_groups;
 constexpr int kCountThreads = EP_COUNT_THREADS;
 constexpr int kCountWarps = kCountThreads / 32;
 constexpr int kVec = EP_COUNT_VEC;
-constexpr int kTargetBlocks = 2 * 148;          // two blocks per B300 SM
+#ifndef EP_COUNT_TARGET_BLOCKS
+#define EP_COUNT_TARGET_BLOCKS (2 * 148)        // blocks a launch aims at (build-time tunable)
+#endif
+constexpr int kTargetBlocks = EP_COUNT_TARGET_BLOCKS;
 constexpr int kMinChunk = kCountThreads * 4;    // at least one 16-byte load per thread
 constexpr int kMaxChunksPerRank = 8;            // portable cluster size
 #ifndef EP_COUNT_MIN_CHUNKS
