@@ -587,7 +587,7 @@ def run_ultraep(args, rank, world, local):
             "dtype": "int32", "payload": "bf16", "data": "synthetic",
             "config": {"workload": f"{args.workload}-like: R={w.R} E={w.E} S={w.S} k={w.k} "
                                    f"T={w.T} layers={w.layers} hidden={w.Hd} bf16, "
-                                   f"Zipf(s={w.s}) popularity re-drawn per microbatch",
+                                   f"{w.popularity_desc()}",
                        "step": "one microbatch through all layers, per layer "
                                "ep_balance (ep_count -> ep_plan -> ep_reroute chained on the "
                                "device) then ep_permute",

@@ -69,6 +69,13 @@ class Workload:
     def domain(self):
         return dict(R=self.R, E=self.E, S=self.S, k=self.k)
 
+    def popularity_desc(self) -> str:
+        if self.popularity == "dirichlet_drift":
+            return (f"popularity 0.5 Dirichlet({self.alpha}) per layer + 0.5 drift between two "
+                    f"Dirichlet({self.alpha}) endpoints over {self.microbatches} microbatches")
+        when = "re-drawn every microbatch" if self.redraw else "fixed per layer"
+        return f"Zipf(s={self.s}) popularity {when}"
+
 
 WORKLOADS = {
     "tiny": Workload("tiny", R=8, E=32, S=1, k=4, T=4096, layers=4, microbatches=1,
