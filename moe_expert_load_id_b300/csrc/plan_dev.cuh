@@ -1,0 +1,257 @@
+// Device code of the planner's flag-free rule: the count checks, the
+// shared-memory table move loop and the logical->physical CSR epilogue (the
+// last also serves the register loop of the rule variants in plan.cu).
+//
+// UltraEP article (m.youleyou.com), "key design" section, control-plane
+// paragraph: the solver fixes the load (quota) every expert instance receives;
+// each exploration step either instantiates a new replica or shifts load; it
+// runs warp-parallel.  The rule itself (hot = argmax load, its largest
+// instance, cold = least-loaded eligible rank, q = min(quota, floor(gap/2)),
+// global stop) is the one documented in ultraep.h.
+#pragma once
+
+#include <climits>
+
+#include "common.cuh"
+
+namespace ultraep {
+
+constexpr long long kPackLimit = 1ll << 25;  // total below this: loads fit a 6-bit-shifted key
+
+__host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
+
+__host__ __device__ inline size_t plan_warp_bytes(int R, int E, int S) {
+    const int P = R * (E / R + S);
+    return align16((size_t)P * 4) + align16((size_t)R * S * 4) + (size_t)E * 8;
+}
+
+// Hottest rank (lowest index on ties) and its load.
+template <bool kTwo, bool kPacked>
+__device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB, int lane,
+                                            int& hot, int& Lmax) {
+    if (kPacked) {
+        const unsigned ka = hasA ? ((unsigned)la << 6) | (unsigned)(63 - lane) : 0u;
+        const unsigned kb = hasB ? ((unsigned)lb << 6) | (unsigned)(31 - lane) : 0u;
+        const unsigned k = __reduce_max_sync(kFull, kTwo ? max(ka, kb) : ka);
+        hot = 63 - (int)(k & 63u);
+        Lmax = (int)(k >> 6);
+    } else {
+        Lmax = __reduce_max_sync(kFull, kTwo ? max(la, lb) : la);
+        const unsigned b0 = __ballot_sync(kFull, la == Lmax);
+        const unsigned b1 = kTwo ? __ballot_sync(kFull, lb == Lmax) : 0u;
+        hot = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+    }
+}
+
+// The base rule on a shared-memory table (the flag-free kernel): the warp's
+// instance quotas q[P] (rank-major, W per rank), the experts of the spare
+// slots slot[R*S] (-1: empty) and, per expert, the mask of ranks holding it;
+// the loads stay in registers (lane l: ranks l and l+32).  Per move the hot
+// rank's largest instance is one warp reduction over its W instances (lane j:
+// instance j), eligibility is one 64-bit mask (holders of e | ranks with a
+// free slot), and the bookkeeping is a few single-lane stores, so nothing in a
+// move grows with the instances per rank.  Same rule, same ties, same outputs
+// as plan_moves with no flags; the tables are exactly the epilogue's.
+template <bool kTwo, bool kPacked>
+__device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint64_t* holder,
+                                                 int& loadA, int& loadB, int lane, int H, int S,
+                                                 int W, int R, int max_iters, int& iters,
+                                                 int& status) {
+    const bool hasA = loadA >= 0, hasB = kTwo && loadB >= 0;
+    const int ra = lane, rb = lane + 32;
+    const uint64_t exist = (R >= 64) ? ~0ull : ((1ull << R) - 1ull);
+    uint64_t freem = S > 0 ? exist : 0ull;  // ranks with a free spare slot (warp-uniform)
+    int hot, Lmax;
+    argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, hot, Lmax);
+    while (true) {
+        // 2. hot's largest-quota instance, lowest expert on ties (lane j:
+        // instance j; every rank has its H >= 1 home instances)
+        int qj = -1;
+        unsigned cxj = 0xffffffffu;
+        if (lane < W) {  // the two loads are independent
+            const int xj = lane < H ? hot * H + lane : slot[hot * S + (lane - H)];
+            const int qv = q[hot * W + lane];
+            if (xj >= 0) {
+                qj = qv;
+                cxj = ((unsigned)xj << 5) | (unsigned)lane;
+            }
+        }
+        const int qmax = __reduce_max_sync(kFull, qj);
+        const unsigned cx = __reduce_min_sync(kFull, qj == qmax ? cxj : 0xffffffffu);
+        const int e = (int)(cx >> 5), src_j = (int)(cx & 31u);
+
+        // 3-5. eligible ranks: the others that hold e or have a free slot;
+        // the coldest of them (lowest rank on ties) and the amount
+        const uint64_t hm = holder[e];
+        const uint64_t el = (hm | freem) & exist & ~(1ull << hot);
+        if (el == 0ull) break;  // no rank is eligible
+        const bool elA = hasA && ((el >> ra) & 1ull);
+        const bool elB = hasB && ((el >> rb) & 1ull);
+        int cold, Lmin;
+        if (kPacked) {
+            const unsigned ca = elA ? ((unsigned)loadA << 6) | (unsigned)ra : 0xffffffffu;
+            const unsigned cb = elB ? ((unsigned)loadB << 6) | (unsigned)rb : 0xffffffffu;
+            const unsigned kk = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            cold = (int)(kk & 63u);
+            Lmin = (int)(kk >> 6);
+        } else {
+            const int ca = elA ? loadA : INT_MAX;
+            const int cb = elB ? loadB : INT_MAX;
+            Lmin = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            const unsigned b0 = __ballot_sync(kFull, elA && ca == Lmin);
+            const unsigned b1 = kTwo ? __ballot_sync(kFull, elB && cb == Lmin) : 0u;
+            cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+        }
+        const int mv = min(qmax, (Lmax - Lmin) >> 1);
+        if (mv <= 0) break;  // the global stop
+        // 6. safety cap
+        if (iters == max_iters) {
+            status = EP_ERR_ITER_LIMIT;
+            break;
+        }
+        // 7. move.  Loads first, then the next move's argmax ...
+        loadA += (ra == cold ? mv : 0) - (ra == hot ? mv : 0);
+        if (kTwo) loadB += (rb == cold ? mv : 0) - (rb == hot ? mv : 0);
+        int nhot, nLmax;
+        argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, nhot, nLmax);
+        // ... and the tables: cold's instance of e is its home, a spare slot
+        // already holding e, or its lowest free spare slot (filled now).  The
+        // spare slots are read and voted on unconditionally (no branch), so
+        // this overlaps the argmax above.
+        const int sv = (lane < S) ? slot[cold * S + lane] : 0;
+        const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
+        const unsigned freeb = __ballot_sync(kFull, lane < S && sv < 0);  // cold's free slots
+        const bool held = (hm >> cold) & 1ull;
+        const int ej = e - cold * H;
+        const bool home = (unsigned)ej < (unsigned)H;  // e is one of cold's home experts
+        const unsigned pick = held ? hit : freeb;       // nonzero unless home: cold is eligible
+        if (!home && pick == 0u) {                      // (never; keeps every index in range)
+            status = EP_ERR_INVAL;
+            break;
+        }
+        const int dj = home ? ej : H + __ffs(pick) - 1;
+        // every read of this move was consumed by the warp's votes and
+        // reductions above; the updates are fire-and-forget shared-memory
+        // additions, no read-modify-write chain
+        if (lane == 0) {
+            atomicAdd(&q[hot * W + src_j], -mv);
+            atomicAdd(&q[cold * W + dj], mv);
+            if (!held) {
+                slot[cold * S + (dj - H)] = e;
+                holder[e] = hm | (1ull << cold);
+            }
+        }
+        if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
+        __syncwarp();  // the updates land before the next move reads the table
+        hot = nhot;
+        Lmax = nLmax;
+        ++iters;
+    }
+}
+
+// Counts must be >= 0 with a total below 2^31; otherwise the instance is
+// rejected (EP_ERR_INVAL).  tot: the warp-uniform total.
+__device__ __forceinline__ int plan_check_counts(const int32_t* cnt, int E, int lane,
+                                                 long long& tot) {
+    bool bad = false;
+    tot = 0;
+    for (int e = lane; e < E; e += 32) {
+        const int v = cnt[e];
+        bad |= v < 0;
+        tot += v;
+    }
+    bad = __any_sync(kFull, bad);
+    for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(kFull, tot, o);
+    return (bad || tot > (long long)INT_MAX) ? EP_ERR_INVAL : EP_OK;
+}
+
+// The flag-free rule for one instance on the shared-memory tables q[P],
+// slot[R*S], holder[E] (plan_warp_bytes): the home placement from cnt, the
+// move loop (only while status is EP_OK), then quota, spare slots and loads to
+// qo / so / lo.  One warp; kTwo: R > 32.
+template <bool kTwo>
+__device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int E, int S,
+                                                 int max_iters, long long tot, int32_t* q,
+                                                 int32_t* slot, uint64_t* holder, int lane,
+                                                 int32_t* qo, int32_t* so, int32_t* lo,
+                                                 int& iters, int& status) {
+    const int H = E / R, W = H + S, P = R * W;
+    for (int p = lane; p < P; p += 32) {
+        const int r = p / W, j = p - r * W;
+        q[p] = j < H ? cnt[r * H + j] : 0;
+    }
+    for (int x = lane; x < R * S; x += 32) slot[x] = -1;
+    for (int e = lane; e < E; e += 32) holder[e] = 1ull << (e / H);
+    int loadA = -1, loadB = -1;
+    if (lane < R) {
+        unsigned sum = 0;
+        for (int j = 0; j < H; ++j) sum += (unsigned)cnt[lane * H + j];
+        loadA = (int)sum;
+    }
+    if (kTwo && lane + 32 < R) {
+        unsigned sum = 0;
+        for (int j = 0; j < H; ++j) sum += (unsigned)cnt[(lane + 32) * H + j];
+        loadB = (int)sum;
+    }
+    __syncwarp();
+    if (status == EP_OK) {
+        if (tot < kPackLimit)
+            plan_moves_table<kTwo, true>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
+                                         max_iters, iters, status);
+        else
+            plan_moves_table<kTwo, false>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
+                                          max_iters, iters, status);
+    }
+    __syncwarp();
+    for (int p = lane; p < P; p += 32) qo[p] = q[p];
+    for (int x = lane; x < R * S; x += 32) so[x] = slot[x];
+    if (lane < R) lo[lane] = loadA;
+    if (kTwo && lane + 32 < R) lo[lane + 32] = loadB;
+}
+
+// Logical -> physical CSR from the tables: for each expert its home instance
+// first, then its replicas by ascending rank (= ascending p), with inclusive
+// cumulative quotas.  One warp; writes po[0..E], io and co.
+__device__ __forceinline__ void plan_csr(const int32_t* q, const int32_t* slot,
+                                         const uint64_t* holder, int R, int E, int S, int lane,
+                                         int32_t* po, int32_t* io, int32_t* co) {
+    const int H = E / R, W = H + S;
+    int run = 0;
+    for (int e0 = 0; e0 < E; e0 += 32) {
+        const int e = e0 + lane;
+        const uint64_t hm = (e < E) ? holder[e] : 0ull;
+        const int n = __popcll(hm);
+        int x = n;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        if (e < E) {
+            int m = run + x - n;
+            po[e] = m;
+            const int home = e / H;
+            const int hp = home * W + (e - home * H);
+            int cum = q[hp];
+            io[m] = hp;
+            co[m] = cum;
+            ++m;
+            uint64_t rest = hm & ~(1ull << home);
+            while (rest) {
+                const int c = __ffsll((long long)rest) - 1;
+                rest &= rest - 1;
+                int j = 0;
+                while (j < S && slot[c * S + j] != e) ++j;
+                const int p = c * W + H + j;
+                cum += q[p];
+                io[m] = p;
+                co[m] = cum;
+                ++m;
+            }
+        }
+        run += __shfl_sync(kFull, x, 31);
+    }
+    if (lane == 0) po[E] = run;
+}
+
+}  // namespace ultraep

@@ -1,7 +1,8 @@
 """ep_balance (count -> plan -> reroute chained with programmatic dependent
 launch) against the CPU oracle and against the three separate calls, bit for
-bit, on seeded inputs; plus back-to-back calls that reuse every buffer on one
-stream, the way a forward pass calls it layer after layer."""
+bit, on seeded inputs; the workspace is left zero.  Plus back-to-back calls
+that reuse every buffer on one stream, the way a forward pass calls it layer
+after layer."""
 import numpy as np
 import pytest
 import torch
@@ -35,7 +36,10 @@ CASES = [
     ("ragged_T",       8,  4, 1, 4,  1001,  3,      False),
     ("invalid_ids",    8,  4, 2, 4,  2000,  2,      True),
     ("R64",            64, 2, 1, 8,  8192,  1,      False),
-    ("many_chunks",    4,  4, 2, 8,  40000, 1,      False),
+    ("R64_full_rank",  64, 2, 1, 8,  131072, 1,     False),   # 16384 slots per source rank
+    ("R64_E256_S2",    64, 4, 2, 8,  20000, 1,      False),
+    ("R64_3_inst",     64, 2, 1, 8,  4096,  3,      False),   # more wide blocks than SMs
+    ("many_chunks",    4,  4, 2, 8,  40000, 1,      False),   # 80000 slots per source rank
     ("max_E_and_k",    64, 16, 16, 32, 1024, 1,     False),
     ("no_spares",      8,  4, 0, 4,  3000,  2,      False),
     ("T_below_R",      8,  2, 1, 3,  5,     1,      False),
@@ -49,6 +53,7 @@ def test_balance_matches_oracle_and_separate_calls(case):
     ids = _zipf_ids(R, E, k, T, n_inst, seed=len(name) * 131 + T, bad=bad)
     dom = G().dom_of(R, E, S, k)
     fused = G().gpu_run(dom, ids, src_slot=True, fused=True)
+    assert not fused["workspace"].any()  # left zero for the next call
     G().compare(R, E, S, fused, G().oracle_run(R, E, S, ids), check_rows=False)
     sep = G().gpu_run(dom, ids, src_slot=True, fused=False)
     for key in ("counts", "counts_src", "quota", "slot_expert", "rank_load", "inst_ptr",
@@ -63,6 +68,37 @@ def test_balance_iteration_cap():
     out = G().gpu_run(dom, ids, max_iters=2, fused=True)
     G().compare(R, R * H, S, out, G().oracle_run(R, R * H, S, ids, max_iters=2), check_rows=False)
     assert (out["inst_status"] == 2).all()
+    assert not out["workspace"].any()
+
+
+def test_balance_cap_above_the_default():
+    R, H, S, k, T = 8, 4, 1, 8, 3000
+    ids = _zipf_ids(R, R * H, k, T, 2, 7)
+    dom = G().dom_of(R, R * H, S, k)
+    cap = (1 << 16) + 1
+    out = G().gpu_run(dom, ids, max_iters=cap, fused=True)
+    G().compare(R, R * H, S, out, G().oracle_run(R, R * H, S, ids, max_iters=cap),
+                check_rows=False)
+
+
+def test_balance_reuses_its_workspace():
+    # the same buffers and workspace through five different instances: every
+    # call must find the workspace zero, so a word left behind would show as a
+    # wrong plan in a later call
+    from moe_expert_load_id_b300 import ultraep as U
+    R, H, S, k, T, n_inst = 16, 4, 1, 8, 6000, 2
+    E = R * H
+    dom = U.Domain(R, E, S, k)
+    b = U.Buffers(dom, T, n_inst, device="cuda")
+    for it in range(5):
+        ids = _zipf_ids(R, E, k, T, n_inst, seed=500 + it)
+        b.balance_fused(torch.from_numpy(ids).cuda())
+        torch.cuda.synchronize()
+        ref = G().oracle_run(R, E, S, ids)
+        assert np.array_equal(b.dst_row.cpu().numpy(), np.stack(ref["dst_row"]))
+        assert np.array_equal(b.quota.cpu().numpy(), np.stack(ref["quota"]))
+        assert not b.workspace.any().item()
+    assert int(b.dev_status.item()) == 0
 
 
 def test_balance_layer_after_layer_reusing_buffers():
