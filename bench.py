@@ -591,8 +591,8 @@ def run_ultraep(args, rank, world, local):
                        "step": "one microbatch through all layers, per layer "
                                "ep_balance (ep_count -> ep_plan -> ep_reroute chained on the "
                                "device) then ep_permute",
-                       "l2": "inputs larger than L2 (1.07 GB hidden per layer, 8.6 GB "
-                             "permute output per layer)",
+                       "l2": f"inputs larger than L2 ({w.T * w.Hd * 2 / 1e9:.2f} GB hidden per "
+                             f"layer, {w.N * w.Hd * 2 / 1e9:.2f} GB permute output per layer)",
                        "parallelism": f"replicas x{world}"},
             "roofline": roofline, "kernels": kernels, "split_breakdown": breakdown,
             "batched": batched,
@@ -755,6 +755,8 @@ def main():
     ap.add_argument("--tokens", type=int, default=0,
                     help="override T (small cases for profiler captures)")
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers")
+    ap.add_argument("--hidden", type=int, default=0,
+                    help="override the hidden size (small cases for profiler captures)")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
@@ -768,8 +770,9 @@ def main():
         ap.error("--warmup must be >= 3")
 
     w = W.WORKLOADS[args.workload]
-    if args.tokens or args.layers:
-        w = dataclasses.replace(w, T=args.tokens or w.T, layers=args.layers or w.layers)
+    if args.tokens or args.layers or args.hidden:
+        w = dataclasses.replace(w, T=args.tokens or w.T, layers=args.layers or w.layers,
+                                Hd=args.hidden or w.Hd)
     args.w = w
     rank, world, local = dist_init()
     if args.stress_sweep:
