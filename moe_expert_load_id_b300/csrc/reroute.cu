@@ -27,9 +27,11 @@
 // next replica) binary search the expert's list, which for a hot expert holds
 // dozens of replicas.
 //
-// ids are read once from memory (kept in registers between the histogram and
-// the assignment phase of a chunk); dst_row is written with coalesced
-// streaming stores; the optional src_slot inverse is a scattered store.
+// ids are read once from memory and kept, with their ranks, between the
+// ranking and the row phase of a chunk: in registers in the 256-thread blocks
+// of batched launches, in shared memory in the 1024-thread blocks of one-layer
+// launches; dst_row is written with coalesced streaming stores; the optional
+// src_slot inverse is a scattered store.
 //
 // (A design with lane-private counters, each lane owning a contiguous run of
 // slots, two shared-memory atomics per slot and one warp scan per expert
