@@ -738,7 +738,8 @@ def run_reference(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "int32", "payload": "bf16",
             "data": "synthetic",
             "config": {"workload": f"{args.workload}-like: R={w.R} E={w.E} S={w.S} k={w.k} "
-                                   f"T={w.T} layers={w.layers} hidden={w.Hd} bf16",
+                                   f"T={w.T} layers={w.layers} hidden={w.Hd} bf16, "
+                                   f"{w.popularity_desc()}",
                        "parallelism": "host cores, 1 thread"},
             "cpu_baseline": cpu,
             "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
