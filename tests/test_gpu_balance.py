@@ -43,6 +43,8 @@ CASES = [
     ("max_E_and_k",    64, 16, 16, 32, 1024, 1,     False),
     ("no_spares",      8,  4, 0, 4,  3000,  2,      False),
     ("T_below_R",      8,  2, 1, 3,  5,     1,      False),
+    ("R1",             1,  4, 1, 2,  500,   1,      False),
+    ("W32",            8,  1, 31, 4, 3000,  2,      False),
 ]
 
 

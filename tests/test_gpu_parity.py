@@ -132,6 +132,10 @@ CASES = [
     ("runs_many_rounds",   2,  8, 1, 8,  20000, 1,      8,   "zipf"),
     ("runs_batched_bad",   8,  4, 1, 4,  3001,  40,     8,   "bad"),
     ("runs_batched_unaligned", 8, 4, 1, 3, 1001, 40,    8,   "zipf"),
+    ("R1_single_rank",     1,  4, 1, 2,  500,   1,      8,   "zipf"),   # no other rank: no move
+    ("R33_second_rank_per_lane", 33, 2, 1, 4, 3000, 1,  8,   "zipf"),   # ragged last rank
+    ("R40_glm_like",       40, 4, 1, 8,  4000,  1,      8,   "zipf"),
+    ("W32_max_instances",  8,  1, 31, 4, 3000,  1,      8,   "zipf"),   # H + S = 32
 ]
 
 
