@@ -158,3 +158,66 @@ def test_plan_ex_rejects_unknown_flags(lib):
     assert lib.ep_plan_ex(ctypes.byref(d), fake, 1, 0, 4, *([fake] * 8), None) == 1
     assert lib.ep_plan_ex(ctypes.byref(d), fake, 1, 0, -1, *([fake] * 8), None) == 1
     assert lib.ep_plan_ex(ctypes.byref(d), None, 0, 0, 3, *([None] * 8), None) == 0
+
+
+def test_reroute_host_rejections_need_no_gpu(lib):
+    vp = ctypes.c_void_p
+    lib.ep_reroute.argtypes = [ctypes.POINTER(Dom), vp, ctypes.c_int64, ctypes.c_int32] + [vp] * 10
+    d = Dom(8, 32, 1, 4)
+    f = vp(0x10000)                       # never dereferenced: every call below fails validation
+    odd = vp(0x10002)
+    #                         ids T   n  counts_src quota ptr id cum dst src off status stream
+    assert lib.ep_reroute(ctypes.byref(Dom(8, 30, 1, 4)), f, 16, 1, f, f, f, f, f, f, None, f,
+                          None, None) == 1                                   # E % R != 0
+    assert lib.ep_reroute(ctypes.byref(d), f, 16, -1, f, f, f, f, f, f, None, f, None,
+                          None) == 1                                         # n_inst < 0
+    assert lib.ep_reroute(ctypes.byref(d), f, 1 << 29, 1, f, f, f, f, f, f, None, f, None,
+                          None) == 1                                         # T*k >= 2^31
+    assert lib.ep_reroute(ctypes.byref(d), f, 16, 1, f, None, f, f, f, f, None, f, None,
+                          None) == 1                                         # no quota
+    assert lib.ep_reroute(ctypes.byref(d), f, 16, 1, f, f, f, f, f, odd, None, f, None,
+                          None) == 1                                         # misaligned dst_row
+    assert lib.ep_reroute(ctypes.byref(d), f, 16, 1, f, f, f, f, f, f, odd, f, None,
+                          None) == 1                                         # misaligned src_slot
+    assert lib.ep_reroute(ctypes.byref(d), f, 16, 1, f, f, f, f, f, f, None, f, odd,
+                          None) == 1                                         # misaligned status
+    assert lib.ep_reroute(ctypes.byref(d), None, 16, 0, *([None] * 10)) == 0  # nothing to do
+
+
+def test_unpermute_and_combine_host_rejections_need_no_gpu(lib):
+    vp = ctypes.c_void_p
+    lib.ep_unpermute.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.c_int32, vp, vp, vp, vp]
+    lib.ep_combine.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                               vp, vp, vp, vp, vp]
+    f = vp(0x10000)                       # never dereferenced: every call below fails validation
+    # unpermute: grouped, T, k, Hd, n_inst, dst_row, y, status, stream
+    assert lib.ep_unpermute(f, 4, 2, 12, 1, f, f, None, None) == 1          # Hd % 8 != 0
+    assert lib.ep_unpermute(f, 4, 0, 16, 1, f, f, None, None) == 1          # k < 1
+    assert lib.ep_unpermute(f, 4, 33, 16, 1, f, f, None, None) == 1         # k > 32
+    assert lib.ep_unpermute(vp(0x10008), 4, 2, 16, 1, f, f, None, None) == 1  # rows not 16-aligned
+    assert lib.ep_unpermute(f, 4, 2, 16, 1, f, None, None, None) == 1       # no output
+    assert lib.ep_unpermute(f, 4, 2, 16, 1, None, f, None, None) == 1       # no dst_row
+    assert lib.ep_unpermute(f, 4, 2, 16, -1, f, f, None, None) == 1         # n_inst < 0
+    assert lib.ep_unpermute(None, 0, 2, 16, 1, None, None, None, None) == 0  # no rows
+    # combine: grouped, T, k, Hd, n_inst, dst_row, weights, y, status, stream
+    assert lib.ep_combine(f, 4, 2, 16, 1, f, None, f, None, None) == 1      # no weights
+    assert lib.ep_combine(f, 4, 2, 16, 1, f, vp(0x10002), f, None, None) == 1  # misaligned weights
+    assert lib.ep_combine(f, 4, 2, 20, 1, f, f, f, None, None) == 1         # Hd % 8 != 0
+    assert lib.ep_combine(f, 4, 2, 16, 1, f, f, vp(0x10004), None, None) == 1  # y not 16-aligned
+    assert lib.ep_combine(None, 4, 2, 16, 0, None, None, None, None, None) == 0  # no instances
+
+
+def test_count_noalloc_host_rejections_need_no_gpu(lib):
+    vp = ctypes.c_void_p
+    lib.ep_count_noalloc.argtypes = [ctypes.POINTER(Dom), vp, ctypes.c_int64, ctypes.c_int32,
+                                     vp, vp, vp, vp]
+    f = vp(0x10000)                       # never dereferenced: every call below fails validation
+    d = Dom(64, 128, 1, 8)
+    assert lib.ep_count_noalloc(ctypes.byref(Dom(8, 30, 1, 4)), f, 16, 1, f, f, None,
+                                None) == 1                                   # bad domain
+    assert lib.ep_count_noalloc(ctypes.byref(d), f, 16, 1, None, f, None, None) == 1  # no counts
+    # more instances than the library's fixed array holds tickets for: refused
+    # before any CUDA call
+    assert lib.ep_count_noalloc(ctypes.byref(d), f, 1, 20000, f, f, None, None) == 4
+    assert lib.ep_count_noalloc(ctypes.byref(d), None, 16, 0, None, None, None, None) == 0
