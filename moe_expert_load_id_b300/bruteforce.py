@@ -1,5 +1,6 @@
-"""Brute-force optimal plan for tiny instances (test infrastructure; a quality
-reference, not a parity target).
+"""Brute-force optimal plan for tiny instances: a plan-quality reference (the
+gap of a planning rule to the best possible maximum rank load), not a parity
+target and not part of the balancing path.
 
 For every replica placement (each spare slot empty or holding one expert its
 rank does not hold yet) the smallest feasible integer maximum rank load is the

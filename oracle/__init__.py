@@ -5,8 +5,7 @@ baseline leg may import this package; the product path never does.  It shares
 no code with the CUDA library and imports nothing from it.
 
 Every function here is argument marshalling around the plain C definitions in
-ultraep_oracle.c, which cite the pages they follow.  The exception is
-`bruteforce`, a separate quality reference for tiny inputs.
+ultraep_oracle.c, which cite the pages they follow.
 """
 import contextlib
 import ctypes

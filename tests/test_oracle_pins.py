@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 import oracle
-from oracle import bruteforce
+from moe_expert_load_id_b300 import bruteforce
 from moe_expert_load_id_b300 import quality as Q
 from moe_expert_load_id_b300 import workload as W
 

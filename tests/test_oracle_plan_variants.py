@@ -115,7 +115,7 @@ def test_skip_prefix_stop_and_bounds(seed, variant):
 
 @pytest.mark.parametrize("seed", range(12))
 def test_skip_against_brute_force(seed):
-    from oracle import bruteforce
+    from moe_expert_load_id_b300 import bruteforce
     rng = np.random.default_rng(100 + seed)
     R, H, S = int(rng.integers(2, 4)), int(rng.integers(1, 3)), 1
     E = R * H
