@@ -36,7 +36,8 @@
  *    (an int32 the caller zeroes; calls OR EP_DEV_* bits into it) and the
  *    per-instance `inst_status` of ep_plan.  Kernels never trap.
  *  - Limits: 1 <= R <= 64, E % R == 0, 1 <= E <= 1024, 0 <= S, H + S <= 32,
- *    1 <= k <= 32, k <= E, 0 <= T, T*k < 2^31, n_inst >= 0.
+ *    1 <= k <= 32, k <= E, 0 <= T, T*k < 2^31, n_inst >= 0, and for the bf16
+ *    row calls 0 <= Hd <= 2^29 (a row of at most 1 GiB).
  */
 #ifndef ULTRAEP_H
 #define ULTRAEP_H
@@ -70,6 +71,13 @@ typedef enum {
 #define EP_DEV_ROW_RANGE 4      /* a dst_row entry was >= T*k; that row was skipped */
 #define EP_DEV_COPY_TIMEOUT 8   /* a row copy did not complete within the kernel's wait
                                    limit; the call stopped early and its output is incomplete */
+#define EP_DEV_COUNTS_MISMATCH 16 /* ep_reroute: counts_src does not hold the per-source-rank
+                                     counts of these ids (e.g. another layer's); every row of
+                                     that instance may be wrong */
+#define EP_DEV_COPY_UNDRAINED 32  /* ep_permute, after EP_DEV_COPY_TIMEOUT: copies into shared
+                                     memory were still pending when the block gave up waiting
+                                     for them and exited; the whole launch's output, and any
+                                     kernel sharing the GPU with it, is suspect */
 
 #define EP_PLAN_MAX_ITERS (1 << 16)
 #define EP_MAX_R 64
@@ -118,8 +126,10 @@ ep_status_t ep_count(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T,
  *  - Returns EP_ERR_WORKSPACE, enqueueing nothing, when the shape needs more
  *    than that (ep_count_workspace_bytes(dom, T, n_inst) is larger).
  *  - The first call on a device, with that device current, looks up the
- *    array's device address (cudaGetSymbolAddress); make that first call
- *    before any stream capture.
+ *    array's device address (cudaGetSymbolAddress) and keeps it for the life
+ *    of the process; make that first call before any stream capture.  After
+ *    cudaDeviceReset on that device the kept address is stale: do not call
+ *    ep_count_noalloc on a device after resetting it.
  *  - All calls on a device share the one array.  Each call clears the part
  *    that must start at zero (the tickets) on `stream` and then launches, so
  *    calls that overlap on the GPU (different streams or threads) race and
@@ -206,7 +216,14 @@ ep_status_t ep_plan_ex(const ep_domain_t *dom, const int32_t *counts, int32_t n_
  * ascending and, inside an instance, by slot index ascending.
  *
  *   topk_ids    [n_inst][T][k]   int32 in
- *   counts_src  [n_inst][R][E]   int32 in  (from ep_count on the same ids)
+ *   counts_src  [n_inst][R][E]   int32 in: ep_count's per-source-rank counts
+ *               of the SAME ids.  They stand in for a per-call workspace: the
+ *               block of source rank r starts its ranks at the prefix of
+ *               counts_src over ranks below r, so no second pass over the ids
+ *               is needed.  After ranking its slots each block checks its own
+ *               row against what it counted; a difference raises
+ *               EP_DEV_COUNTS_MISMATCH, and then dst_row, src_slot and
+ *               inst_offset of that instance must be treated as invalid.
  *   quota, inst_ptr, inst_id, inst_cum   in (from ep_plan)
  *   dst_row     [n_inst][T*k]    int32 out: row of each slot; -1 for a slot
  *                                with an invalid id or beyond its quotas
@@ -214,7 +231,8 @@ ep_status_t ep_plan_ex(const ep_domain_t *dom, const int32_t *counts, int32_t n_
  *                                entries past the last row are not written
  *   inst_offset [n_inst][P+1]    int32 out: first row of every instance
  *                                (exclusive prefix sum of quota)
- *   dev_status  int32            out: |= EP_DEV_BAD_ID, EP_DEV_QUOTA_OVERFLOW
+ *   dev_status  int32            out: |= EP_DEV_BAD_ID, EP_DEV_QUOTA_OVERFLOW,
+ *                                EP_DEV_COUNTS_MISMATCH
  */
 ep_status_t ep_reroute(const ep_domain_t *dom, const int32_t *topk_ids, int64_t T, int32_t n_inst,
                        const int32_t *counts_src, const int32_t *quota, const int32_t *inst_ptr,
@@ -273,7 +291,10 @@ ep_status_t ep_balance(const ep_domain_t *dom, const int32_t *topk_ids, int64_t 
  *   out     [n_inst][T*k][Hd] bf16 out; rows nobody maps to are not written
  *   dev_status int32          out: |= EP_DEV_ROW_RANGE for a dst_row >= T*k;
  *                             |= EP_DEV_COPY_TIMEOUT if a bulk row copy did not
- *                             complete within the kernel's bounded wait
+ *                             complete within the kernel's bounded wait (the
+ *                             output is then incomplete); |= EP_DEV_COPY_UNDRAINED
+ *                             if, after that, copies were still pending when the
+ *                             block exited
  *
  * Rows of 1 KiB or more move through shared memory with TMA bulk copies
  * (one global->shared copy per row, k shared->global copies); shorter rows

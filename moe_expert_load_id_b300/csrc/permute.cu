@@ -259,15 +259,20 @@ permute_tma_kernel(const char* __restrict__ hidden, int64_t n_tok, int64_t T, in
         }
         __syncwarp();
     }
+    // After a timeout no further load is issued (the loop above stops before
+    // its next issue_load); the loads already in flight are waited for, again
+    // with a bound, before the block's shared memory is released.  If one of
+    // them does not complete either, the block still exits and says so.
+    int undrained = 0;
     if (lane == 0) {
         bulk_wait_all();
-        // after a timeout, let the loads still in flight land (bounded) before
-        // the block's shared memory is released
         for (int64_t x = i; x < issued; ++x)
-            mbar_wait(&bar[x % kStages], (uint32_t)((x / kStages) & 1));
+            if (!mbar_wait(&bar[x % kStages], (uint32_t)((x / kStages) & 1))) undrained = 1;
     }
     const bool to = __shfl_sync(kFull, timed_out, 0) != 0;
-    const int flags = (__any_sync(kFull, range_err) ? EP_DEV_ROW_RANGE : 0) | (to ? EP_DEV_COPY_TIMEOUT : 0);
+    const bool ud = __shfl_sync(kFull, undrained, 0) != 0;
+    const int flags = (__any_sync(kFull, range_err) ? EP_DEV_ROW_RANGE : 0) |
+                      (to ? EP_DEV_COPY_TIMEOUT : 0) | (ud ? EP_DEV_COPY_UNDRAINED : 0);
     if (lane == 0 && flags) raise_flag(dev_status, flags);
 }
 

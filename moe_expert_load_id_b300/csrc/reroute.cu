@@ -89,9 +89,10 @@ __host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps, bo
         l.Es = l.El = E;
     }
     // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wx0[warps][Es] wdb[warps][Es]
+    //        want[E]
     // uint16: wlim[warps][El]
     l.lim_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
-                                   2 * (size_t)warps * l.Es);
+                                   2 * (size_t)warps * l.Es + E);
     l.bytes = l.lim_off + sizeof(uint16_t) * (size_t)warps * l.El;
     l.ev_off = (l.bytes + 15) & ~(size_t)15;
     if (ev_smem) l.bytes = l.ev_off + sizeof(int32_t) * (size_t)kItems * warps * 32;
@@ -119,6 +120,9 @@ __device__ __forceinline__ int upper_bound(const int32_t* a, int lo, int hi, int
 //   bcum[M]   inclusive cumulative quota of each list entry (INT_MIN if unused)
 //   bdel[M]   row minus within-expert rank, for the ranks of that entry
 //   base[E]   += slots of e on source ranks below r
+//   want[E]   base[e] + counts_src[r][e]: the running base after the block's
+//             last chunk when counts_src describes these ids (not built when
+//             want is null)
 // base must be zero, and a block barrier passed, before the call; the block
 // of source rank 0 also writes inst_offset.  The caller puts a barrier
 // between this and any read of the tables.
@@ -131,7 +135,7 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
                                             const int32_t* __restrict__ inst_cum,
                                             int32_t* __restrict__ inst_offset, int32_t* off,
                                             int32_t* ptr, int32_t* bcum, int32_t* bdel,
-                                            int32_t* base, int32_t* warp_tot) {
+                                            int32_t* base, int32_t* want, int32_t* warp_tot) {
     constexpr int kWarps = kThreads / 32;
     constexpr int kIpt = (2048 + kThreads - 1) / kThreads;  // P <= 2048 quota per thread
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -166,6 +170,10 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
             bdel[m] = p;
         }
     }
+    // this rank's own row of counts_src, for the check after the last chunk
+    const int32_t* own = counts_src + ((int64_t)inst * R + r) * E;
+    if (want != nullptr)
+        for (int e = tid; e < E; e += kThreads) want[e] = __ldg(own + e);
     // per-expert slots on earlier source ranks.  With E a multiple of 4 and
     // the rows 16-byte aligned, thread (g, q) sums the int4 column q
     // (experts 4q .. 4q+3) over rows g, g+G, ... < r (G = threads / (E/4)),
@@ -249,6 +257,9 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
         if (tid == kThreads - 1) off[P] = warp_tot[kWarps - 1];
     }
     __syncthreads();
+    // each thread adds the prefix to the want[] entries it loaded itself
+    if (want != nullptr)
+        for (int e = tid; e < E; e += kThreads) want[e] += base[e];
     // row minus within-expert rank of each entry: off[p] - (cum - quota[p]),
     // with quota[p] = off[p+1] - off[p] (each thread revisits its own entries)
     for (int m = tid; m < M; m += kThreads) {
@@ -291,6 +302,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     const int Es = lay.Es, El = lay.El;
     int32_t* wx0 = base + E;        // [kWarps][Es] per-warp counts, then each warp's first rank
     int32_t* wdb = wx0 + kWarps * Es;  // [kWarps][Es] row of that first rank
+    int32_t* want = wdb + kWarps * Es;  // [E] expected base after the last chunk
     uint16_t* wlim = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(sm) + lay.lim_off);
                                     // [kWarps][El] ranks left in its instance (capped)
 
@@ -379,7 +391,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 
     // ---- prologue: plan tables
     plan_tables<kThreads>(R, E, P, M, inst, r, counts_src, quota, inst_ptr, inst_id, inst_cum,
-                          inst_offset, off, ptr, bcum, bdel, base, warp_tot);
+                          inst_offset, off, ptr, bcum, bdel, base, want, warp_tot);
     // (the barrier before phase B orders the writes above before any read of
     // bcum / bdel)
 
@@ -559,6 +571,12 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         }
         __syncwarp();
     }
+    // every slot of the rank has been ranked: base[e] - (slots of e on earlier
+    // ranks) is this rank's own count of e, which must equal counts_src[r][e]
+    // (the within-expert ranks above started from the counts_src prefix)
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads)
+        if (base[e] != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
     if (my_flags) atomicOr(&flags, my_flags);
     __syncthreads();
     if (tid == 0 && flags) raise_flag(dev_status, flags);

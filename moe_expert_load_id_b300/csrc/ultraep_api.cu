@@ -51,7 +51,7 @@ ep_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? EP_OK : EP_ERR_
 bool rows_ok(int64_t T, int32_t k, int32_t Hd, int32_t n_inst) {
     if (n_inst < 0 || Hd < 0 || Hd % 8 != 0) return false;
     if (k < 1 || k > EP_MAX_K || !slots_ok(T, k)) return false;
-    if ((int64_t)Hd * 2 / 16 >= (int64_t(1) << 31)) return false;
+    if (Hd > (1 << 29)) return false;  // row bytes (2*Hd) stay an int
     return true;
 }
 

@@ -21,6 +21,7 @@ _lib = ctypes.CDLL(_LIB_PATH)
 
 EP_OK, EP_ERR_INVAL, EP_ERR_ITER_LIMIT, EP_ERR_BAD_ID, EP_ERR_WORKSPACE, EP_ERR_CUDA = range(6)
 EP_DEV_BAD_ID, EP_DEV_QUOTA_OVERFLOW, EP_DEV_ROW_RANGE, EP_DEV_COPY_TIMEOUT = 1, 2, 4, 8
+EP_DEV_COUNTS_MISMATCH, EP_DEV_COPY_UNDRAINED = 16, 32
 EP_PLAN_MAX_ITERS = 1 << 16
 EP_PLAN_SKIP, EP_PLAN_RELEASE = 1, 2
 EP_COUNT_NOALLOC_SCRATCH_BYTES = 64 << 10

@@ -1,10 +1,77 @@
 """Shared helpers of the GPU parity tests: run the CUDA path through the C ABI
-and the oracle on the same seeded inputs, and compare them."""
+and the oracle on the same seeded inputs, and compare them.
+
+Every output buffer the tests hand to the library is allocated through a
+``Guard``: 4 KiB past its end hold a fixed byte pattern, and ``Guard.check``
+asserts after the calls that no kernel wrote there.  compute-sanitizer is not
+available on the GPU machines these tests run on; the guard tails are how the
+tests see a write past the end of an output."""
+import math
+
 import numpy as np
 import torch
 
 import oracle
 from moe_expert_load_id_b300 import ultraep as U
+
+GUARD_BYTES = 4096
+_PATTERN = ((np.arange(GUARD_BYTES, dtype=np.uint32) * 37 + 0xA5) & 0xFF).astype(np.uint8)
+
+
+class Guard:
+    """Allocates output tensors with a guard tail and checks the tails later."""
+
+    def __init__(self, device="cuda"):
+        self.device = device
+        self.items = []
+        self.pattern = torch.from_numpy(_PATTERN).to(device)
+
+    def alloc(self, name, shape, dtype, fill=None):
+        n = math.prod(shape)
+        esize = torch.empty((), dtype=dtype).element_size()
+        extra = GUARD_BYTES // esize
+        base = torch.empty(n + extra, dtype=dtype, device=self.device)
+        raw = base.view(torch.uint8)
+        raw[n * esize:].copy_(self.pattern)
+        t = base[:n].view(shape)
+        if fill is not None:
+            t.fill_(fill)
+        self.items.append((name, raw, n * esize))
+        return t
+
+    def check(self):
+        torch.cuda.synchronize()
+        for name, raw, off in self.items:
+            tail = raw[off:]
+            if not torch.equal(tail, self.pattern):
+                bad = int((tail != self.pattern).nonzero()[0].item())
+                raise AssertionError(f"{name}: write past the end (guard byte {bad} changed)")
+
+
+def guarded_buffers(dom, T, n_inst=1, Hd=0, src_slot=False, guard=None, device="cuda"):
+    """U.Buffers whose every output (and the count workspace) carries a guard tail."""
+    g = guard if guard is not None else Guard(device)
+    b = U.Buffers(dom, T, n_inst, Hd=0, device=device, src_slot=False)
+    i32 = torch.int32
+    N = T * dom.k
+    specs = {"counts": ((n_inst, dom.E), None), "counts_src": ((n_inst, dom.R, dom.E), None),
+             "dev_status": ((1,), 0), "quota": ((n_inst, dom.P), None),
+             "slot_expert": ((n_inst, dom.R, dom.S), None), "rank_load": ((n_inst, dom.R), None),
+             "inst_ptr": ((n_inst, dom.E + 1), None),
+             "inst_id": ((n_inst, dom.E + dom.R * dom.S), -1),
+             "inst_cum": ((n_inst, dom.E + dom.R * dom.S), -1), "n_iter": ((n_inst,), None),
+             "inst_status": ((n_inst,), None), "dst_row": ((n_inst, N), None),
+             "inst_offset": ((n_inst, dom.P + 1), None)}
+    for name, (shape, fill) in specs.items():
+        setattr(b, name, g.alloc(name, shape, i32, fill))
+    b.workspace = g.alloc("workspace", tuple(b.workspace.shape), i32, 0)
+    if src_slot:
+        b.src_slot = g.alloc("src_slot", (n_inst, N), i32, -1)
+    if Hd:
+        b.Hd = Hd
+        b.grouped = g.alloc("grouped", (n_inst, N, Hd), torch.bfloat16)
+    b.guard = g
+    return b
 
 
 def dom_of(R, E, S, k):
@@ -19,7 +86,7 @@ def gpu_run(dom, ids_np, hidden_u16=None, src_slot=True, max_iters=0, unpermute=
     dev = "cuda"
     ids = torch.from_numpy(np.ascontiguousarray(ids_np, dtype=np.int32)).to(dev)
     Hd = 0 if hidden_u16 is None else hidden_u16.shape[-1]
-    b = U.Buffers(dom, T, n_inst, Hd=Hd, device=dev, src_slot=src_slot)
+    b = guarded_buffers(dom, T, n_inst, Hd=Hd, src_slot=src_slot, device=dev)
     if fused:
         b.balance_fused(ids, max_iters=max_iters)
     else:
@@ -33,11 +100,11 @@ def gpu_run(dom, ids_np, hidden_u16=None, src_slot=True, max_iters=0, unpermute=
         b.grouped.zero_()
         b.permute(hid)
         if unpermute:
-            y = torch.empty((n_inst, T, k, Hd), dtype=torch.bfloat16, device=dev)
+            y = b.guard.alloc("y", (n_inst, T, k, Hd), torch.bfloat16)
             U.ep_unpermute(b.grouped, T, k, b.dst_row, y, b.dev_status)
             out["y"] = y.view(torch.int16).cpu().numpy().view(np.uint16)
         out["grouped"] = b.grouped.view(torch.int16).cpu().numpy().view(np.uint16)
-    torch.cuda.synchronize()
+    b.guard.check()
     for name in ("counts", "counts_src", "quota", "slot_expert", "rank_load", "inst_ptr",
                  "inst_id", "inst_cum", "n_iter", "inst_status", "dst_row", "inst_offset",
                  "dev_status", "workspace"):

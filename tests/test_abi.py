@@ -208,6 +208,23 @@ def test_unpermute_and_combine_host_rejections_need_no_gpu(lib):
     assert lib.ep_combine(None, 4, 2, 16, 0, None, None, None, None, None) == 0  # no instances
 
 
+def test_row_calls_reject_rows_past_one_gib(lib):
+    # Hd above 2^29 would make the row size (2 * Hd bytes) overflow an int
+    vp = ctypes.c_void_p
+    _setup(lib)
+    lib.ep_unpermute.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
+                                 ctypes.c_int32, vp, vp, vp, vp]
+    lib.ep_combine.argtypes = [vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, ctypes.c_int32,
+                               vp, vp, vp, vp, vp]
+    f = vp(0x10000)                       # never dereferenced: every call below fails validation
+    for hd in ((1 << 29) + 8, (1 << 30), (1 << 31) - 8):
+        assert lib.ep_permute(f, 4, 2, hd, 1, f, f, None, None) == 1
+        assert lib.ep_unpermute(f, 4, 2, hd, 1, f, f, None, None) == 1
+        assert lib.ep_combine(f, 4, 2, hd, 1, f, f, f, None, None) == 1
+    # the largest accepted row with no rows to move: nothing is launched
+    assert lib.ep_permute(f, 0, 2, 1 << 29, 1, None, f, None, None) == 0
+
+
 def test_count_noalloc_host_rejections_need_no_gpu(lib):
     vp = ctypes.c_void_p
     lib.ep_count_noalloc.argtypes = [ctypes.POINTER(Dom), vp, ctypes.c_int64, ctypes.c_int32,
@@ -218,6 +235,11 @@ def test_count_noalloc_host_rejections_need_no_gpu(lib):
                                 None) == 1                                   # bad domain
     assert lib.ep_count_noalloc(ctypes.byref(d), f, 16, 1, None, f, None, None) == 1  # no counts
     # more instances than the library's fixed array holds tickets for: refused
-    # before any CUDA call
+    # before any CUDA call; 16384 tickets fill the 64 KiB exactly, 16385 do not fit
     assert lib.ep_count_noalloc(ctypes.byref(d), f, 1, 20000, f, f, None, None) == 4
+    assert lib.ep_count_noalloc(ctypes.byref(d), f, 1, 16385, f, f, None, None) == 4
+    lib.ep_count_workspace_bytes.restype = ctypes.c_size_t
+    lib.ep_count_workspace_bytes.argtypes = [ctypes.POINTER(Dom), ctypes.c_int64, ctypes.c_int32]
+    assert lib.ep_count_workspace_bytes(ctypes.byref(d), 1, 16384) == 64 << 10
+    assert lib.ep_count_workspace_bytes(ctypes.byref(d), 1, 16385) > 64 << 10
     assert lib.ep_count_noalloc(ctypes.byref(d), None, 16, 0, None, None, None, None) == 0

@@ -39,6 +39,7 @@ CASES = [
     ("R64_full_rank",  64, 2, 1, 8,  131072, 1,     False),   # 16384 slots per source rank
     ("R64_E256_S2",    64, 4, 2, 8,  20000, 1,      False),
     ("R64_3_inst",     64, 2, 1, 8,  4096,  3,      False),   # more wide blocks than SMs
+    ("R64_5_inst_quad", 64, 2, 1, 8, 4096,  5,      True),    # the quad reroute kernel
     ("many_chunks",    4,  4, 2, 8,  40000, 1,      False),   # 80000 slots per source rank
     ("max_E_and_k",    64, 16, 16, 32, 1024, 1,     False),
     ("no_spares",      8,  4, 0, 4,  3000,  2,      False),
@@ -91,7 +92,7 @@ def test_balance_reuses_its_workspace():
     R, H, S, k, T, n_inst = 16, 4, 1, 8, 6000, 2
     E = R * H
     dom = U.Domain(R, E, S, k)
-    b = U.Buffers(dom, T, n_inst, device="cuda")
+    b = G().guarded_buffers(dom, T, n_inst)
     for it in range(5):
         ids = _zipf_ids(R, E, k, T, n_inst, seed=500 + it)
         b.balance_fused(torch.from_numpy(ids).cuda())
@@ -101,6 +102,7 @@ def test_balance_reuses_its_workspace():
         assert np.array_equal(b.quota.cpu().numpy(), np.stack(ref["quota"]))
         assert not b.workspace.any().item()
     assert int(b.dev_status.item()) == 0
+    b.guard.check()
 
 
 def test_balance_layer_after_layer_reusing_buffers():
@@ -109,7 +111,7 @@ def test_balance_layer_after_layer_reusing_buffers():
     from moe_expert_load_id_b300 import ultraep as U
     w = W.WORKLOADS["qwen3-235b"]
     dom = U.Domain(w.R, w.E, w.S, w.k)
-    b = U.Buffers(dom, w.T, 1, Hd=w.Hd, device="cuda")
+    b = G().guarded_buffers(dom, w.T, 1, Hd=w.Hd)
     hid = W.hidden(w.T, w.Hd, w.seed(1000, 2), device="cuda")[None]
     layers = [W.topk_ids(w, l, 2, device="cuda")[None] for l in range(3)]
     got = []
@@ -119,7 +121,7 @@ def test_balance_layer_after_layer_reusing_buffers():
         got.append((b.counts.clone(), b.quota.clone(), b.dst_row.clone()))
     torch.cuda.synchronize()
     assert int(b.dev_status.item()) == 0
-    ref = U.Buffers(dom, w.T, 1, device="cuda")
+    ref = G().guarded_buffers(dom, w.T, 1, guard=b.guard)
     for ids, (c, q, d) in zip(layers, got):
         ref.count(ids)
         ref.plan()
@@ -134,3 +136,4 @@ def test_balance_layer_after_layer_reusing_buffers():
     pl = oracle.plan(cnt, w.R, w.E, w.S)
     dst, _, _ = oracle.reroute(ids_h, w.R, w.E, w.S, pl)
     assert np.array_equal(got[2][2][0].cpu().numpy(), dst)
+    b.guard.check()

@@ -28,6 +28,11 @@ def _rows(rng, n, Hd):
     return bits
 
 
+def G():
+    import gpu_common
+    return gpu_common
+
+
 def _case(T, k, Hd, n_inst, seed):
     rng = np.random.default_rng(seed)
     N = T * k
@@ -45,10 +50,11 @@ def _gpu_combine(grouped, dst, w, T, k):
     g = torch.from_numpy(grouped.view(np.int16)).cuda().view(torch.bfloat16)
     d = torch.from_numpy(dst).cuda()
     wt = torch.from_numpy(w).cuda()
-    y = torch.full((n_inst, T, Hd), 7.0, dtype=torch.bfloat16, device="cuda")
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    guard = G().Guard()
+    y = guard.alloc("y", (n_inst, T, Hd), torch.bfloat16, 7.0)
+    st = guard.alloc("dev_status", (1,), torch.int32, 0)
     U().ep_combine(g, T, k, d, wt, y, st)
-    torch.cuda.synchronize()
+    guard.check()
     return y.view(torch.int16).cpu().numpy().view(np.uint16), int(st.item())
 
 
@@ -92,13 +98,13 @@ def test_combine_full_size_layer_sample():
     w_ = W.WORKLOADS["qwen3-235b"]
     ids = W.topk_ids(w_, 5, 0, device="cuda")[None]
     hid = W.hidden(w_.T, w_.Hd, w_.seed(5, 0), device="cuda")[None]
-    b = Uu.Buffers(Uu.Domain(w_.R, w_.E, w_.S, w_.k), w_.T, 1, Hd=w_.Hd, device="cuda")
+    b = G().guarded_buffers(Uu.Domain(w_.R, w_.E, w_.S, w_.k), w_.T, 1, Hd=w_.Hd)
     b.balance(ids, hid)
     gen = torch.Generator(device="cuda").manual_seed(11)
     wts = torch.softmax(torch.randn((1, w_.T, w_.k), device="cuda", generator=gen), -1)
-    y = torch.empty((1, w_.T, w_.Hd), dtype=torch.bfloat16, device="cuda")
+    y = b.guard.alloc("y", (1, w_.T, w_.Hd), torch.bfloat16)
     Uu.ep_combine(b.grouped, w_.T, w_.k, b.dst_row, wts, y, b.dev_status)
-    torch.cuda.synchronize()
+    b.guard.check()
     assert int(b.dev_status.item()) == 0
     rng = np.random.default_rng(5)
     toks = np.sort(rng.choice(w_.T, size=2048, replace=False))

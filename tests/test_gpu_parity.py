@@ -1,7 +1,10 @@
 """GPU parity: every C-ABI call against the CPU oracle, bit-exact, on seeded inputs.
 
-Small and medium cases compare every output element; the full-size workloads
-compare the index outputs completely and the bf16 rows on a seeded sample.
+Every case compares every output element.  At full size the bf16 rows are
+compared on the device, in chunks: each permuted row against the hidden row
+of the token the oracle's src_slot names, and each unpermuted slot against its
+own token's row (what the oracle's unpermute of its permute gives).  Every
+output buffer carries a guard tail that must be unchanged after the calls.
 """
 import numpy as np
 import pytest
@@ -136,6 +139,17 @@ CASES = [
     ("R33_second_rank_per_lane", 33, 2, 1, 4, 3000, 1,  8,   "zipf"),   # ragged last rank
     ("R40_glm_like",       40, 4, 1, 8,  4000,  1,      8,   "zipf"),
     ("W32_max_instances",  8,  1, 31, 4, 3000,  1,      8,   "zipf"),   # H + S = 32
+    # the quad reroute kernel (k a multiple of 4, 296 or more (instance, rank)
+    # units): repeated ids in a lane's four slots, a ragged T, empty source
+    # ranks, the largest E and k, a ragged last block of ranks (R = 36), every
+    # slot on one expert (every step by slot, replica boundaries crossed all
+    # the time)
+    ("quad_dups_R64",      64, 2, 1, 8,  2000,  5,      8,   "bad"),
+    ("quad_ragged_T",      16, 4, 2, 4,  3333,  19,     8,   "zipf"),
+    ("quad_T_below_R",     64, 2, 1, 4,  50,    5,      8,   "zipf"),
+    ("quad_max_E_and_k",   64, 16, 16, 32, 257, 5,      8,   "zipf"),
+    ("quad_R36_uniform",   36, 4, 1, 4,  4000,  9,      8,   "uniform"),
+    ("quad_one_expert",    8,  4, 2, 4,  5000,  40,     8,   "one"),
 ]
 
 
@@ -155,6 +169,9 @@ def _make_ids(R, E, k, T, n_inst, kind, seed):
                 ids[rng.integers(0, T, 5), -1] = -3
                 if k > 1:
                     ids[rng.integers(0, T, 5), 1] = ids[rng.integers(0, T, 5), 0] % E  # duplicates
+                if k > 2:
+                    t2 = rng.integers(0, T, 5)
+                    ids[t2, 1] = ids[t2, 2]                # the same expert twice in one token
         out.append(ids)
     return np.stack(out) if n_inst else np.zeros((0, T, k), np.int32)
 
@@ -195,13 +212,14 @@ def test_iteration_cap_matches_oracle():
 
 def test_plan_rejects_bad_counts():
     dom = G().dom_of(4, 8, 1, 2)
-    b = U.Buffers(dom, 16, 2)
+    b = G().guarded_buffers(dom, 16, 2)
     b.counts.copy_(torch.tensor([[5, -1, 0, 0, 0, 0, 0, 0],
                                  [2 ** 30, 2 ** 30, 0, 0, 0, 0, 0, 0]], dtype=torch.int32))
     b.plan()
     st = b.inst_status.cpu().numpy()
     assert st.tolist() == [U.EP_ERR_INVAL, U.EP_ERR_INVAL]
     assert (b.n_iter.cpu().numpy() == 0).all()
+    b.guard.check()
 
 
 def test_device_status_flags():
@@ -212,7 +230,7 @@ def test_device_status_flags():
     out = G().gpu_run(dom, ids)
     assert int(out["dev_status"][0]) & U.EP_DEV_BAD_ID
     # a plan whose quotas do not cover the ids: overflowing slots get no row
-    b = U.Buffers(dom, T, 1)
+    b = G().guarded_buffers(dom, T, 1)
     dids = torch.from_numpy(ids).cuda()
     b.count(dids)
     b.plan()
@@ -226,22 +244,58 @@ def test_device_status_flags():
     hidden = torch.ones((T, Hd), dtype=torch.bfloat16, device="cuda")
     dst = torch.arange(T * k, dtype=torch.int32, device="cuda")
     dst[5] = T * k + 3
-    out_rows = torch.zeros((T * k, Hd), dtype=torch.bfloat16, device="cuda")
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out_rows = b.guard.alloc("out_rows", (T * k, Hd), torch.bfloat16, 0)
+    st = b.guard.alloc("st", (1,), torch.int32, 0)
     U.ep_permute(hidden, k, dst, out_rows, st)
     assert int(st.item()) & U.EP_DEV_ROW_RANGE
     assert float(out_rows[5].float().abs().sum()) == 0.0
-    y = torch.full((T, k, Hd), 7.0, dtype=torch.bfloat16, device="cuda")
+    y = b.guard.alloc("y", (T, k, Hd), torch.bfloat16, 7.0)
     st.zero_()
     U.ep_unpermute(out_rows, T, k, dst, y, st)
     assert int(st.item()) & U.EP_DEV_ROW_RANGE
     assert float(y.reshape(T * k, Hd)[5].float().abs().sum()) == 0.0
+    b.guard.check()
+
+
+@pytest.mark.parametrize("case", [(8, 4, 1, 4, 4096, 2), (64, 2, 1, 8, 131072, 1),
+                                  (64, 2, 1, 8, 4096, 5)])
+def test_reroute_flags_counts_of_other_ids(case):
+    # counts_src taken from other ids (another layer's buffer): every block
+    # compares what it ranked with its own counts_src row and flags the
+    # difference; the same call with the right counts_src raises nothing
+    R, H, S, k, T, n_inst = case
+    E = R * H
+    dom = G().dom_of(R, E, S, k)
+    ids_a = torch.from_numpy(_make_ids(R, E, k, T, n_inst, "zipf", 41)).cuda()
+    ids_b = torch.from_numpy(_make_ids(R, E, k, T, n_inst, "zipf", 42)).cuda()
+    b = G().guarded_buffers(dom, T, n_inst, src_slot=True)
+    b.count(ids_a)
+    b.plan()
+    b.reroute(ids_a)
+    torch.cuda.synchronize()
+    assert int(b.dev_status.item()) == 0
+    stale = b.counts_src.clone()
+    b.count(ids_b)
+    b.plan()
+    b.counts_src.copy_(stale)              # the other ids' per-source-rank counts
+    b.reroute(ids_b)
+    torch.cuda.synchronize()
+    assert int(b.dev_status.item()) & U.EP_DEV_COUNTS_MISMATCH
+    # only the block of source rank 0 of an instance starts at prefix zero; a
+    # counts_src differing in one entry still raises the flag
+    b.dev_status.zero_()
+    b.count(ids_b)
+    b.counts_src[0, R - 1, int(ids_b[0, -1, 0].item())] += 1
+    b.reroute(ids_b)
+    torch.cuda.synchronize()
+    assert int(b.dev_status.item()) & U.EP_DEV_COUNTS_MISMATCH
+    b.guard.check()
 
 
 def test_workspace_reused_across_calls():
     w, ids, _ = _tiny_inputs([0, 1])
     dom = G().dom_of(w.R, w.E, w.S, w.k)
-    b = U.Buffers(dom, w.T, 2)
+    b = G().guarded_buffers(dom, w.T, 2)
     d = torch.from_numpy(ids).cuda()
     outs = []
     for _ in range(3):
@@ -250,6 +304,7 @@ def test_workspace_reused_across_calls():
         assert (b.workspace.cpu().numpy()[:2] == 0).all()          # the two instance tickets
     for c, cs in outs[1:]:
         assert (c == outs[0][0]).all() and (cs == outs[0][1]).all()
+    b.guard.check()
 
 
 def test_permute_preserves_bit_patterns():
@@ -265,17 +320,43 @@ def test_permute_preserves_bit_patterns():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def _full_size_layer(name, layer, microbatch, n_samples=4096):
+ROW_CHUNK = 1 << 16
+
+
+def check_all_rows(hid_d, grouped_d, y_d, src_slot_oracle, n_rows, k):
+    """Every permuted row equals the hidden row of the token the oracle's
+    src_slot names; every unpermuted slot equals its own token's row (the
+    oracle's unpermute of its permute).  On the device, in chunks of rows."""
+    src = torch.from_numpy(np.ascontiguousarray(src_slot_oracle[:n_rows])).cuda()
+    for r0 in range(0, n_rows, ROW_CHUNK):
+        r1 = min(n_rows, r0 + ROW_CHUNK)
+        want = hid_d.index_select(0, (src[r0:r1] // k).long())
+        got = grouped_d[r0:r1]
+        if not torch.equal(got.view(torch.int16), want.view(torch.int16)):
+            bad = (got.view(torch.int16) != want.view(torch.int16)).any(1).nonzero()[0].item()
+            raise AssertionError(f"grouped row {r0 + bad} differs from the oracle's")
+    if y_d is None:
+        return
+    N = y_d.shape[0] * y_d.shape[1] if y_d.dim() == 3 else y_d.shape[0]
+    y2 = y_d.reshape(N, -1)
+    for s0 in range(0, N, ROW_CHUNK):
+        s1 = min(N, s0 + ROW_CHUNK)
+        tok = torch.arange(s0, s1, device="cuda") // k
+        if not torch.equal(y2[s0:s1].view(torch.int16), hid_d.index_select(0, tok).view(torch.int16)):
+            raise AssertionError(f"unpermuted slots {s0}..{s1} differ from the oracle's")
+
+
+def _full_size_layer(name, layer, microbatch):
     w = W.WORKLOADS[name]
     ids_d = W.topk_ids(w, layer, microbatch, device="cuda")
     hid_d = W.hidden(w.T, w.Hd, w.seed(layer, microbatch), device="cuda")
     ids = ids_d.cpu().numpy()[None]
     dom = U.Domain(w.R, w.E, w.S, w.k)
-    b = U.Buffers(dom, w.T, 1, Hd=w.Hd, device="cuda", src_slot=True)
+    b = G().guarded_buffers(dom, w.T, 1, Hd=w.Hd, src_slot=True)
     b.balance(ids_d[None], hid_d[None])                    # the per-layer launches the bench times
-    y = torch.empty((1, w.T, w.k, w.Hd), dtype=torch.bfloat16, device="cuda")
+    y = b.guard.alloc("y", (1, w.T, w.k, w.Hd), torch.bfloat16)
     U.ep_unpermute(b.grouped, w.T, w.k, b.dst_row, y, b.dev_status)
-    torch.cuda.synchronize()
+    b.guard.check()
     orc = G().oracle_run(w.R, w.E, w.S, ids)
     out = {key: getattr(b, key).cpu().numpy() for key in
            ("counts", "counts_src", "quota", "slot_expert", "rank_load", "inst_ptr", "inst_id",
@@ -283,19 +364,9 @@ def _full_size_layer(name, layer, microbatch, n_samples=4096):
             "src_slot", "dev_status")}
     G().compare(w.R, w.E, w.S, out, orc, check_rows=False)
     assert int(out["dev_status"][0]) == 0
-    # rows: a seeded sample of grouped rows against the oracle's source token
-    rng = np.random.default_rng(layer * 31 + microbatch)
     n_rows = int(orc["inst_offset"][0][-1])
-    rows = np.sort(rng.choice(n_rows, size=min(n_samples, n_rows), replace=False))
-    src_tok = orc["src_slot"][0][rows] // w.k
-    got = b.grouped[0][torch.from_numpy(rows).cuda()].view(torch.int16).cpu().numpy()
-    want = hid_d[torch.from_numpy(src_tok).cuda()].view(torch.int16).cpu().numpy()
-    assert np.array_equal(got, want)
-    # unpermute: a seeded sample of slots against the token's own row
-    slots = np.sort(rng.choice(w.N, size=n_samples, replace=False))
-    gy = y.reshape(w.N, w.Hd)[torch.from_numpy(slots).cuda()].view(torch.int16).cpu().numpy()
-    want = hid_d[torch.from_numpy(slots // w.k).cuda()].view(torch.int16).cpu().numpy()
-    assert np.array_equal(gy, want)
+    assert n_rows == w.N
+    check_all_rows(hid_d, b.grouped[0], y[0], orc["src_slot"][0], n_rows, w.k)
     return out
 
 
@@ -327,10 +398,36 @@ def test_full_size_layer_without_src_slot():
     G().compare(w.R, w.E, w.S, out, orc, check_rows=False)
 
 
-@pytest.mark.parametrize("R,S,tpr,s", [(8, 4, 8192, 1.6), (64, 4, 512, 0.6), (32, 2, 2048, 1.0)])
+# one point per (R, S) pair of the stress grid, its tokens per rank and Zipf
+# skew cycling through the grid's values (the largest, 8192 tokens per rank at
+# R = 64, included)
+STRESS_POINTS = [(8, 1, 512, 0.6), (8, 2, 1024, 1.0), (8, 4, 8192, 1.6),
+                 (16, 1, 2048, 1.0), (16, 2, 4096, 1.6), (16, 4, 512, 0.6),
+                 (32, 1, 1024, 1.6), (32, 2, 2048, 1.0), (32, 4, 4096, 0.6),
+                 (64, 1, 2048, 1.6), (64, 2, 1024, 0.6), (64, 4, 8192, 1.0)]
+
+
+@pytest.mark.parametrize("R,S,tpr,s", STRESS_POINTS,
+                         ids=[f"R{r}_S{s_}_T{t}_z{z}" for r, s_, t, z in STRESS_POINTS])
 def test_stress_points(R, S, tpr, s):
+    # two layers batched through the separate calls, every index output
+    # against the oracle; then the first layer through the ep_balance and
+    # ep_permute launches the benchmark makes, every row checked
     w = W.stress(R, S, tpr, s)
     ids_d = torch.stack([W.topk_ids(w, l, 0, device="cuda") for l in range(2)])
     ids = ids_d.cpu().numpy()
-    out = G().gpu_run(U.Domain(w.R, w.E, w.S, w.k), ids, src_slot=True)
-    G().compare(w.R, w.E, w.S, out, G().oracle_run(w.R, w.E, w.S, ids), check_rows=False)
+    dom = U.Domain(w.R, w.E, w.S, w.k)
+    out = G().gpu_run(dom, ids, src_slot=True)
+    orc = G().oracle_run(w.R, w.E, w.S, ids)
+    G().compare(w.R, w.E, w.S, out, orc, check_rows=False)
+    assert int(out["dev_status"][0]) == 0
+    hid_d = W.hidden(w.T, w.Hd, w.seed(0, 0), device="cuda")
+    b = G().guarded_buffers(dom, w.T, 1, Hd=w.Hd)
+    b.balance_fused(ids_d[:1])
+    b.permute(hid_d[None])
+    b.guard.check()
+    assert np.array_equal(b.dst_row[0].cpu().numpy(), orc["dst_row"][0])
+    check_all_rows(hid_d, b.grouped[0], None, orc["src_slot"][0], int(orc["inst_offset"][0][-1]),
+                   w.k)
+    del b, hid_d
+    torch.cuda.empty_cache()

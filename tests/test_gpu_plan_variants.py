@@ -31,10 +31,10 @@ def G():
 def _gpu_plan(R, E, S, counts, flags, max_iters=0):
     counts = np.ascontiguousarray(counts, dtype=np.int32).reshape(-1, E)
     n = counts.shape[0]
-    b = U().Buffers(U().Domain(R, E, S, 1), 1, n, device="cuda")
+    b = G().guarded_buffers(U().Domain(R, E, S, 1), 1, n)
     b.counts.copy_(torch.from_numpy(counts))
     b.plan(max_iters=max_iters, flags=flags)
-    torch.cuda.synchronize()
+    b.guard.check()
     return {key: getattr(b, key).cpu().numpy() for key in
             ("quota", "slot_expert", "rank_load", "inst_ptr", "inst_id", "inst_cum", "n_iter",
              "inst_status")}
@@ -113,10 +113,10 @@ def test_tiny_workload_through_reroute(variant):
 def test_full_size_layer_skip():
     w = W.WORKLOADS["qwen3-235b"]
     ids = W.topk_ids(w, 11, 0, device="cuda")[None]
-    b = U().Buffers(U().Domain(w.R, w.E, w.S, w.k), w.T, 1, device="cuda")
+    b = G().guarded_buffers(U().Domain(w.R, w.E, w.S, w.k), w.T, 1)
     b.count(ids)
     b.plan(flags=FLAGS["skip+release"])
-    torch.cuda.synchronize()
+    b.guard.check()
     c = b.counts.cpu().numpy()[0]
     want = oracle.plan(c, w.R, w.E, w.S, variant="skip+release")
     got = {key: getattr(b, key).cpu().numpy() for key in

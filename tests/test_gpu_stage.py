@@ -18,6 +18,11 @@ def U():
     return ultraep
 
 
+def G():
+    import gpu_common
+    return gpu_common
+
+
 @pytest.mark.parametrize("nbytes", [16, 4112, 200000])
 @pytest.mark.parametrize("with_prev", [False, True])
 def test_stage_matches_oracle(nbytes, with_prev):
@@ -31,11 +36,13 @@ def test_stage_matches_oracle(nbytes, with_prev):
     prev = prev.astype(np.int32)
     dom = U().Domain(R, E, S, k)
     ew_d = torch.from_numpy(ew).cuda()
-    sw_d = torch.from_numpy(sw0).cuda()
-    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    guard = G().Guard()
+    sw_d = guard.alloc("slot_w", tuple(sw0.shape), torch.uint8)
+    sw_d.copy_(torch.from_numpy(sw0))
+    st = guard.alloc("dev_status", (1,), torch.int32, 0)
     U().ep_stage(dom, ew_d, torch.from_numpy(se).cuda(), sw_d,
                  torch.from_numpy(prev).cuda() if with_prev else None, st)
-    torch.cuda.synchronize()
+    guard.check()
     got = sw_d.cpu().numpy()
     for g in range(n_inst):
         want, _, _ = oracle.stage(ew[g], se[g], R, S, sw0[g], prev=prev[g] if with_prev else None)
@@ -47,15 +54,15 @@ def test_stage_from_a_real_plan():
     w = W.WORKLOADS["tiny"]
     dom = U().Domain(w.R, w.E, w.S, w.k)
     ids = W.topk_ids(w, 1, 0, device="cuda")[None]
-    b = U().Buffers(dom, w.T, 1, device="cuda")
+    b = G().guarded_buffers(dom, w.T, 1)
     b.count(ids)
     b.plan()
     nbytes = 3 * 256 * 64 * 2                               # a small bf16 expert: 3 matrices
     gen = torch.Generator(device="cuda").manual_seed(3)
     ew = torch.randint(0, 256, (w.E, nbytes), dtype=torch.uint8, device="cuda", generator=gen)
-    sw = torch.zeros((w.R, w.S, nbytes), dtype=torch.uint8, device="cuda")
+    sw = b.guard.alloc("slot_w", (w.R, w.S, nbytes), torch.uint8, 0)
     U().ep_stage(dom, ew, b.slot_expert, sw, None, b.dev_status)
-    torch.cuda.synchronize()
+    b.guard.check()
     se = b.slot_expert.cpu().numpy().reshape(-1)
     want, n, bad = oracle.stage(ew.cpu().numpy(), se, w.R, w.S,
                                 np.zeros((w.R * w.S, nbytes), np.uint8))
