@@ -582,6 +582,324 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     if (tid == 0 && flags) raise_flag(dev_status, flags);
 }
 
+// ---------------------------------------------------------------- quad kernel
+// Batched launches with k a multiple of 4 and 16-byte aligned ids: one warp
+// per (instance, source rank), eight consecutive source ranks of one instance
+// per block.  A warp walks its rank's slots in steps of 128: lane l holds the
+// 16-byte group of slots 4l .. 4l+3 of the step, four of one token's top-k
+// ids, which a top-k gate makes distinct.  So a lane adds at most one bit to
+// any expert's lane mask, and one OR per slot, one warp barrier and one read
+// per slot give every slot its rank in the step (lanes below holding the same
+// expert); the group's lowest lane then advances the warp's running count.
+//
+// Every expert has one 16-byte entry in the warp's table: {lane mask of the
+// step, running count (the within-expert rank of the warp's next slot of e),
+// lim, del}, where ranks below lim lie in the instance whose rows start at
+// rank + del.  One 16-byte shared load per slot therefore yields the rank and
+// the row; a rank at or past lim (a warp crossing into the next replica of
+// its expert) searches the expert's instance list, and the group leader moves
+// lim and del on.  The running count starts at the prefix of counts_src over
+// earlier source ranks, so no scan over warps or chunks is needed, and it ends
+// at prefix + this rank's own count: the check against counts_src is one
+// compare per expert.
+//
+// A step in which some lane's four ids are not distinct (ids that no top-k
+// gate produces, e.g. a repeated expert) is ranked slot by slot instead: four
+// sub-steps of 32 consecutive slots with the same table.
+constexpr int kQuadWarps = 8;
+constexpr int kQuadThreads = kQuadWarps * 32;
+constexpr int kQuadAhead = 4;  // steps of ids loaded ahead of the one being ranked
+#ifndef EP_REROUTE_QUAD_MIN_RANKS
+#define EP_REROUTE_QUAD_MIN_RANKS 296  // (instance, source rank) units from which the
+                                        // quad kernel is used (build-time tunable)
+#endif
+#ifndef EP_REROUTE_QUAD_BLOCKS_PER_SM
+#define EP_REROUTE_QUAD_BLOCKS_PER_SM 4  // build-time tunable
+#endif
+
+struct QuadLayout {
+    int P, M;
+    size_t pre_off;  // [kQuadWarps + 1][E] int32: prefix of counts_src for each warp's rank
+    size_t tab_off;  // [kQuadWarps][E] int4 entry tables
+    size_t bytes;
+};
+
+__host__ __device__ inline QuadLayout quad_layout(int R, int E, int S) {
+    QuadLayout l;
+    l.P = R * (E / R + S);
+    l.M = E + R * S;
+    // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E]
+    l.pre_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E);
+    l.tab_off = (l.pre_off + sizeof(int32_t) * (size_t)(kQuadWarps + 1) * E + 15) & ~(size_t)15;
+    l.bytes = l.tab_off + sizeof(int4) * (size_t)kQuadWarps * E;
+    return l;
+}
+
+__global__ void __launch_bounds__(kQuadThreads, EP_REROUTE_QUAD_BLOCKS_PER_SM)
+reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
+                    const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
+                    const int32_t* __restrict__ inst_ptr, const int32_t* __restrict__ inst_id,
+                    const int32_t* __restrict__ inst_cum, int32_t* __restrict__ dst_row,
+                    int32_t* __restrict__ src_slot, int32_t* __restrict__ inst_offset,
+                    int32_t* dev_status, int early) {
+    extern __shared__ __align__(16) int32_t sm[];
+    __shared__ int32_t warp_tot[kQuadWarps];
+    __shared__ int32_t flags;
+    const QuadLayout lay = quad_layout(R, E, S);
+    const int P = lay.P, M = lay.M;
+    int32_t* off = sm;              // [P+1]
+    int32_t* ptr = off + (P + 1);   // [E+1]
+    int32_t* bcum = ptr + (E + 1);  // [M]
+    int32_t* bdel = bcum + M;       // [M]
+    int32_t* base = bdel + M;       // [E] slots of e on source ranks below the block's first
+    int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(sm) + lay.pre_off);
+    int4* tabs = reinterpret_cast<int4*>(reinterpret_cast<unsigned char*>(sm) + lay.tab_off);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int gpi = (R + kQuadWarps - 1) / kQuadWarps;  // blocks per instance
+    const int inst = blockIdx.x / gpi;
+    const int r0 = (blockIdx.x - inst * gpi) * kQuadWarps;
+    const int r = r0 + warp;
+    const bool has_rank = r < R;
+    const int nr = min(kQuadWarps, R - r0);  // ranks of this block
+
+    // this warp's slots: source rank r (T*k < 2^31, so 32-bit offsets)
+    const int Tr = ((int)T + R - 1) / R;
+    const int64_t N = T * k;
+    const int s0 = has_rank ? (int)min(T, (int64_t)r * Tr) * k : 0;
+    const int s1 = has_rank ? (int)min(T, (int64_t)(r + 1) * Tr) * k : 0;
+    const int L = s1 - s0;  // a multiple of 4
+    const int nsteps = (L + 127) >> 7;
+    const int32_t* idw = ids + (int64_t)inst * N + s0;
+    int32_t* dsw = dst_row + (int64_t)inst * N + s0;
+    int32_t* srci = src_slot ? src_slot + (int64_t)inst * N : nullptr;
+    auto load_step = [&](int st) -> int4 {
+        const int sl = (st << 7) + (lane << 2);
+        return (st < nsteps && sl < L) ? __ldcs(reinterpret_cast<const int4*>(idw + sl))
+                                       : make_int4(-1, -1, -1, -1);
+    };
+    // the first steps' ids depend only on the call's input: in ep_balance they
+    // are in flight while the planner finishes
+    if (!early) pdl_wait();
+    int4 buf[kQuadAhead];
+#pragma unroll
+    for (int j = 0; j < kQuadAhead; ++j) buf[j] = load_step(j);
+    if (tid == 0) flags = 0;
+    for (int e = tid; e < E; e += kQuadThreads) base[e] = 0;
+    __syncthreads();
+    if (early) pdl_wait();
+    pdl_trigger();
+
+    // ---- prologue: plan tables, then each warp's prefix over source ranks
+    plan_tables<kQuadThreads>(R, E, P, M, inst, r0, counts_src, quota, inst_ptr, inst_id,
+                              inst_cum, inst_offset, off, ptr, bcum, bdel, base, nullptr,
+                              warp_tot);
+    {
+        const int32_t* cs = counts_src + ((int64_t)inst * R + r0) * E;
+        for (int x = tid; x < kQuadWarps * E; x += kQuadThreads) {
+            const int w = x / E, e = x - w * E;
+            pre[(w + 1) * E + e] = (w < nr) ? __ldg(cs + (int64_t)w * E + e) : 0;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kQuadThreads) {
+        int run = base[e];
+        pre[e] = run;
+#pragma unroll
+        for (int w = 1; w <= kQuadWarps; ++w) {
+            run += pre[w * E + e];
+            pre[w * E + e] = run;
+        }
+    }
+    __syncthreads();
+    int my_flags = 0;
+    if (!has_rank) {
+        __syncwarp();
+    } else {
+        // ---- the warp's entry table: count = prefix, lim / del of its instance
+        int4* tab = tabs + (size_t)warp * E;
+        const int32_t* mypre = pre + warp * E;
+        for (int e = lane; e < E; e += 32) {
+            const int x = mypre[e];
+            const int end = ptr[e + 1];
+            const int m = upper_bound(bcum, ptr[e], end, x);
+            tab[e] = (m < end) ? make_int4(0, x, bcum[m], bdel[m]) : make_int4(0, x, x, 0);
+        }
+        __syncwarp();
+        const unsigned lt = lanemask_lt(), bit = 1u << lane;
+        uint32_t* tabw = reinterpret_cast<uint32_t*>(tab);
+        // the row of rank x of expert e when x is past the entry's lim
+        auto search = [&](int e, int x, int& fl) -> int {
+            const int end = ptr[e + 1];
+            const int m = upper_bound(bcum, ptr[e], end, x);
+            if (m < end) return x + bdel[m];
+            fl |= EP_DEV_QUOTA_OVERFLOW;
+            return -1;
+        };
+        // the leader of a group whose new count reached lim moves the entry on
+        auto advance = [&](int e, int c) {
+            const int end = ptr[e + 1];
+            const int m = upper_bound(bcum, ptr[e], end, c);
+            int2* z = reinterpret_cast<int2*>(tab + e) + 1;
+            *z = (m < end) ? make_int2(bcum[m], bdel[m]) : make_int2(c, 0);
+        };
+        auto store_rows = [&](int sl, int4 rows) {
+            if (sl < L) {
+                __stcs(reinterpret_cast<int4*>(dsw + sl), rows);
+                if (srci != nullptr) {
+                    const int g = s0 + sl;
+                    if (rows.x >= 0) srci[rows.x] = g;
+                    if (rows.y >= 0) srci[rows.y] = g + 1;
+                    if (rows.z >= 0) srci[rows.z] = g + 2;
+                    if (rows.w >= 0) srci[rows.w] = g + 3;
+                }
+            }
+        };
+        // one slot's row from its (valid) rank and entry, range-checked
+        auto finish = [&](bool v, int row) -> int {
+            if (!v) return -1;
+            if ((unsigned)row >= (unsigned)N) {
+                my_flags |= EP_DEV_QUOTA_OVERFLOW;
+                return -1;
+            }
+            return row;
+        };
+        // a step whose lanes hold a repeated id: four sub-steps of 32
+        // consecutive slots, one slot per lane, in slot order
+        auto step_by_slot = [&](int4 q, int st) {
+#pragma unroll 1
+            for (int a = 0; a < 4; ++a) {
+                const int srcl = (a << 3) + (lane >> 2), c = lane & 3;
+                const int qx = __shfl_sync(kFull, q.x, srcl), qy = __shfl_sync(kFull, q.y, srcl);
+                const int qz = __shfl_sync(kFull, q.z, srcl), qw = __shfl_sync(kFull, q.w, srcl);
+                const int e = c == 0 ? qx : c == 1 ? qy : c == 2 ? qz : qw;
+                const int sl = (st << 7) + (a << 5) + lane;
+                const bool v = (unsigned)e < (unsigned)E;
+                if (v) atomicOr(&tabw[4 * e], bit);
+                __syncwarp();
+                const int4 en = v ? tab[e] : make_int4(0, 0, 0, 0);
+                const unsigned below = (unsigned)en.x & lt;
+                const int rk = en.y + __popc(below);
+                const int nc = en.y + __popc((unsigned)en.x);
+                const bool lead = v && below == 0u;
+                int row = rk + en.w;
+                __syncwarp();
+                if (lead) *reinterpret_cast<int2*>(tab + e) = make_int2(0, nc);
+                if (lead && nc >= en.z) advance(e, nc);
+                if (v && rk >= en.z) row = search(e, rk, my_flags);
+                __syncwarp();
+                row = finish(v, row);
+                if (sl < L) {
+                    dsw[sl] = row;
+                    if (srci != nullptr && row >= 0) srci[row] = s0 + sl;
+                }
+            }
+        };
+
+#pragma unroll 1
+        for (int st = 0; st < nsteps; ++st) {
+            {
+                const int4 q = buf[0];
+#pragma unroll
+                for (int j = 0; j + 1 < kQuadAhead; ++j) buf[j] = buf[j + 1];
+                buf[kQuadAhead - 1] = load_step(st + kQuadAhead);
+                const int sl = (st << 7) + (lane << 2);
+                const bool v0 = (unsigned)q.x < (unsigned)E, v1 = (unsigned)q.y < (unsigned)E;
+                const bool v2 = (unsigned)q.z < (unsigned)E, v3 = (unsigned)q.w < (unsigned)E;
+                if (sl < L && !(v0 && v1 && v2 && v3)) my_flags |= EP_DEV_BAD_ID;
+                const bool dup = (v0 && v1 && q.x == q.y) || (v0 && v2 && q.x == q.z) ||
+                                 (v0 && v3 && q.x == q.w) || (v1 && v2 && q.y == q.z) ||
+                                 (v1 && v3 && q.y == q.w) || (v2 && v3 && q.z == q.w);
+                if (__any_sync(kFull, dup)) {
+                    step_by_slot(q, st);
+                    continue;
+                }
+                if (v0) atomicOr(&tabw[4 * q.x], bit);
+                if (v1) atomicOr(&tabw[4 * q.y], bit);
+                if (v2) atomicOr(&tabw[4 * q.z], bit);
+                if (v3) atomicOr(&tabw[4 * q.w], bit);
+                __syncwarp();
+                const int4 n0 = v0 ? tab[q.x] : make_int4(0, 0, 0, 0);
+                const int4 n1 = v1 ? tab[q.y] : make_int4(0, 0, 0, 0);
+                const int4 n2 = v2 ? tab[q.z] : make_int4(0, 0, 0, 0);
+                const int4 n3 = v3 ? tab[q.w] : make_int4(0, 0, 0, 0);
+                const unsigned b0 = (unsigned)n0.x & lt, b1 = (unsigned)n1.x & lt;
+                const unsigned b2 = (unsigned)n2.x & lt, b3 = (unsigned)n3.x & lt;
+                const int k0 = n0.y + __popc(b0), k1 = n1.y + __popc(b1);
+                const int k2 = n2.y + __popc(b2), k3 = n3.y + __popc(b3);
+                const int c0 = n0.y + __popc((unsigned)n0.x), c1 = n1.y + __popc((unsigned)n1.x);
+                const int c2 = n2.y + __popc((unsigned)n2.x), c3 = n3.y + __popc((unsigned)n3.x);
+                const bool l0 = v0 && b0 == 0u, l1 = v1 && b1 == 0u;
+                const bool l2 = v2 && b2 == 0u, l3 = v3 && b3 == 0u;
+                int4 rows = make_int4(k0 + n0.w, k1 + n1.w, k2 + n2.w, k3 + n3.w);
+                const bool x0 = v0 && k0 >= n0.z, x1 = v1 && k1 >= n1.z;
+                const bool x2 = v2 && k2 >= n2.z, x3 = v3 && k3 >= n3.z;
+                __syncwarp();
+                if (l0) *reinterpret_cast<int2*>(tab + q.x) = make_int2(0, c0);
+                if (l1) *reinterpret_cast<int2*>(tab + q.y) = make_int2(0, c1);
+                if (l2) *reinterpret_cast<int2*>(tab + q.z) = make_int2(0, c2);
+                if (l3) *reinterpret_cast<int2*>(tab + q.w) = make_int2(0, c3);
+                // rare: a group past its entry's lim (a replica boundary)
+                const bool a0 = l0 && c0 >= n0.z, a1 = l1 && c1 >= n1.z;
+                const bool a2 = l2 && c2 >= n2.z, a3 = l3 && c3 >= n3.z;
+                if (__any_sync(kFull, a0 || a1 || a2 || a3 || x0 || x1 || x2 || x3)) {
+                    if (a0) advance(q.x, c0);
+                    if (a1) advance(q.y, c1);
+                    if (a2) advance(q.z, c2);
+                    if (a3) advance(q.w, c3);
+                    if (x0) rows.x = search(q.x, k0, my_flags);
+                    if (x1) rows.y = search(q.y, k1, my_flags);
+                    if (x2) rows.z = search(q.z, k2, my_flags);
+                    if (x3) rows.w = search(q.w, k3, my_flags);
+                }
+                __syncwarp();
+                rows.x = finish(v0, rows.x);
+                rows.y = finish(v1, rows.y);
+                rows.z = finish(v2, rows.z);
+                rows.w = finish(v3, rows.w);
+                store_rows(sl, rows);
+            }
+        }
+        // every slot of the rank is ranked: the running counts must have
+        // reached the prefix over the ranks up to and including this one
+        const int32_t* want = pre + (warp + 1) * E;
+        for (int e = lane; e < E; e += 32)
+            if (tab[e].y != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
+    }
+    if (my_flags) atomicOr(&flags, my_flags);
+    __syncthreads();
+    if (tid == 0 && flags) raise_flag(dev_status, flags);
+}
+
+cudaError_t launch_reroute_quad(const ep_domain_t& d, const int32_t* ids, int64_t T,
+                                int32_t n_inst, const int32_t* counts_src, const int32_t* quota,
+                                const int32_t* inst_ptr, const int32_t* inst_id,
+                                const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
+                                int32_t* inst_offset, int32_t* dev_status, cudaStream_t s,
+                                bool pdl) {
+    const QuadLayout lay = quad_layout(d.R, d.E, d.S);
+    if (lay.bytes > 48 * 1024) {
+        cudaError_t err = cudaFuncSetAttribute(reroute_quad_kernel,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)lay.bytes);
+        if (err != cudaSuccess) return err;
+    }
+    const int gpi = (d.R + kQuadWarps - 1) / kQuadWarps;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)((int64_t)n_inst * gpi));
+    cfg.blockDim = dim3(kQuadThreads);
+    cfg.dynamicSmemBytes = lay.bytes;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, reroute_quad_kernel, ids, T, (int)d.k, (int)d.R, (int)d.E,
+                              (int)d.S, counts_src, quota, inst_ptr, inst_id, inst_cum, dst_row,
+                              src_slot, inst_offset, dev_status, pdl ? 1 : 0);
+}
+
 template <int kThreads>
 cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                              const int32_t* counts_src, const int32_t* quota,
@@ -625,6 +943,14 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
     const int64_t blocks = (int64_t)n_inst * d.R;
     const DeviceInfo di = device_info();
     const int sms = di.sms;
+    // k a multiple of 4 and 16-byte aligned ids: the quad kernel for batched
+    // launches, when its tables fit in shared memory
+    const bool quad_ok = d.k % 4 == 0 && (reinterpret_cast<uintptr_t>(ids) & 15u) == 0 &&
+                         (reinterpret_cast<uintptr_t>(dst_row) & 15u) == 0 &&
+                         quad_layout(d.R, d.E, d.S).bytes + 1024 <= di.smem_optin;
+    if (quad_ok && blocks >= (int64_t)EP_REROUTE_QUAD_MIN_RANKS)
+        return launch_reroute_quad(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
+                                   inst_cum, dst_row, src_slot, inst_offset, dev_status, s, pdl);
     // wide blocks only when their tables (and the chunk's ids) fit in shared memory
     const bool wide_fits =
         rr_layout(d.R, d.E, d.S, 1024 / 32, ev_in_smem<1024>()).bytes + 1024 <= di.smem_optin;
