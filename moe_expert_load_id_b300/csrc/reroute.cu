@@ -583,32 +583,35 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 }
 
 // ---------------------------------------------------------------- quad kernel
-// Batched launches with k a multiple of 4 and 16-byte aligned ids: one warp
-// per (instance, source rank), eight consecutive source ranks of one instance
-// per block.  A warp walks its rank's slots in steps of 128: lane l holds the
-// 16-byte group of slots 4l .. 4l+3 of the step, four of one token's top-k
-// ids, which a top-k gate makes distinct.  So a lane adds at most one bit to
-// any expert's lane mask, and one OR per slot, one warp barrier and one read
-// per slot give every slot its rank in the step (lanes below holding the same
-// expert); the group's lowest lane then advances the warp's running count.
+// Batched launches with k a multiple of 4 and 16-byte aligned ids and rows:
+// one warp per (instance, source rank), eight consecutive source ranks of one
+// instance per block.  A warp walks its rank's slots in steps of 128: lane l
+// holds the 16-byte group of slots 4l .. 4l+3 of the step, four of one
+// token's top-k ids, which a top-k gate makes distinct.  So a lane adds at
+// most one bit to any expert's lane mask, and one OR per slot, one warp
+// barrier and one 8-byte read per slot give every slot its place among the
+// step's slots of its expert (the lanes below holding the same expert); the
+// group's lowest lane then advances the expert's next row.
 //
-// Every expert has one 16-byte entry in the warp's table: {lane mask of the
-// step, running count (the within-expert rank of the warp's next slot of e),
-// lim, del}, where ranks below lim lie in the instance whose rows start at
-// rank + del.  One 16-byte shared load per slot therefore yields the rank and
-// the row; a rank at or past lim (a warp crossing into the next replica of
-// its expert) searches the expert's instance list, and the group leader moves
-// lim and del on.  The running count starts at the prefix of counts_src over
-// earlier source ranks, so no scan over warps or chunks is needed, and it ends
-// at prefix + this rank's own count: the check against counts_src is one
-// compare per expert.
+// Each expert has two entries in the warp's tables:
+//   hot[e]  = {lane mask of the step, the row of e's next slot}
+//   cold[e] = {the row just past the current instance of e, row - rank there}
+// A slot's row is hot[e].row + (lanes below in its group).  Only a group that
+// runs past its instance (a replica boundary, or the expert's quotas used up)
+// takes the slow path: its slots search the expert's instance list and the
+// leader moves both entries on.  The rows start at the prefix of counts_src
+// over earlier source ranks (mapped through the plan), so no scan over warps
+// or chunks is needed; at the end the rank a warp reached must be that
+// prefix plus its own counts_src row, one compare per expert.
 //
-// A step in which some lane's four ids are not distinct (ids that no top-k
-// gate produces, e.g. a repeated expert) is ranked slot by slot instead: four
-// sub-steps of 32 consecutive slots with the same table.
+// Ids outside [0, E), and the slots past the end of a rank, use four spare
+// entries E .. E+3 (one per position in the lane's group), whose rows are
+// discarded.  A step in which some lane's four valid ids are not distinct (no
+// top-k gate produces those) is ranked slot by slot instead: four sub-steps
+// of 32 consecutive slots on the same tables.
 constexpr int kQuadWarps = 8;
 constexpr int kQuadThreads = kQuadWarps * 32;
-constexpr int kQuadAhead = 4;  // steps of ids loaded ahead of the one being ranked
+constexpr int kQuadAhead = 3;  // steps of ids loaded ahead of the one being ranked
 #ifndef EP_REROUTE_QUAD_MIN_RANKS
 #define EP_REROUTE_QUAD_MIN_RANKS 296  // (instance, source rank) units from which the
                                         // quad kernel is used (build-time tunable)
@@ -620,7 +623,8 @@ constexpr int kQuadAhead = 4;  // steps of ids loaded ahead of the one being ran
 struct QuadLayout {
     int P, M;
     size_t pre_off;  // [kQuadWarps + 1][E] int32: prefix of counts_src for each warp's rank
-    size_t tab_off;  // [kQuadWarps][E] int4 entry tables
+    size_t hot_off;  // [kQuadWarps][E + 4] uint2 {mask, next row}
+    size_t cold_off; // [kQuadWarps][E + 4] int2 {end row, row - rank}
     size_t bytes;
 };
 
@@ -630,8 +634,9 @@ __host__ __device__ inline QuadLayout quad_layout(int R, int E, int S) {
     l.M = E + R * S;
     // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E]
     l.pre_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E);
-    l.tab_off = (l.pre_off + sizeof(int32_t) * (size_t)(kQuadWarps + 1) * E + 15) & ~(size_t)15;
-    l.bytes = l.tab_off + sizeof(int4) * (size_t)kQuadWarps * E;
+    l.hot_off = (l.pre_off + sizeof(int32_t) * (size_t)(kQuadWarps + 1) * E + 15) & ~(size_t)15;
+    l.cold_off = l.hot_off + sizeof(uint2) * (size_t)kQuadWarps * (E + 4);
+    l.bytes = l.cold_off + sizeof(int2) * (size_t)kQuadWarps * (E + 4);
     return l;
 }
 
@@ -653,7 +658,8 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
     int32_t* bdel = bcum + M;       // [M]
     int32_t* base = bdel + M;       // [E] slots of e on source ranks below the block's first
     int32_t* pre = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(sm) + lay.pre_off);
-    int4* tabs = reinterpret_cast<int4*>(reinterpret_cast<unsigned char*>(sm) + lay.tab_off);
+    uint2* hots = reinterpret_cast<uint2*>(reinterpret_cast<unsigned char*>(sm) + lay.hot_off);
+    int2* colds = reinterpret_cast<int2*>(reinterpret_cast<unsigned char*>(sm) + lay.cold_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int gpi = (R + kQuadWarps - 1) / kQuadWarps;  // blocks per instance
@@ -713,37 +719,146 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
     }
     __syncthreads();
     int my_flags = 0;
-    if (!has_rank) {
-        __syncwarp();
-    } else {
-        // ---- the warp's entry table: count = prefix, lim / del of its instance
-        int4* tab = tabs + (size_t)warp * E;
+    if (has_rank) {
+        // ---- the warp's tables: each expert's next row (its prefix mapped
+        // through the plan) and the end of that row's instance
+        uint2* hot = hots + (size_t)warp * (E + 4);
+        int2* cold = colds + (size_t)warp * (E + 4);
         const int32_t* mypre = pre + warp * E;
-        for (int e = lane; e < E; e += 32) {
-            const int x = mypre[e];
-            const int end = ptr[e + 1];
-            const int m = upper_bound(bcum, ptr[e], end, x);
-            tab[e] = (m < end) ? make_int4(0, x, bcum[m], bdel[m]) : make_int4(0, x, x, 0);
+        for (int e = lane; e < E + 4; e += 32) {
+            if (e < E) {
+                const int x = mypre[e];
+                const int end = ptr[e + 1];
+                const int m = upper_bound(bcum, ptr[e], end, x);
+                const int del = (m < end) ? bdel[m] : 0;  // quotas used up: every rank overflows
+                hot[e] = make_uint2(0u, (unsigned)(x + del));
+                cold[e] = make_int2((m < end) ? bcum[m] + del : x, del);
+            } else {
+                hot[e] = make_uint2(0u, 0u);
+                cold[e] = make_int2(INT_MAX, 0);  // spare entries never cross
+            }
         }
         __syncwarp();
         const unsigned lt = lanemask_lt(), bit = 1u << lane;
-        uint32_t* tabw = reinterpret_cast<uint32_t*>(tab);
-        // the row of rank x of expert e when x is past the entry's lim
-        auto search = [&](int e, int x, int& fl) -> int {
+        uint32_t* hotw = reinterpret_cast<uint32_t*>(hot);
+        // rank x of expert e past its entry: search e's instance list
+        auto search = [&](int e, int x) -> int {
             const int end = ptr[e + 1];
             const int m = upper_bound(bcum, ptr[e], end, x);
             if (m < end) return x + bdel[m];
-            fl |= EP_DEV_QUOTA_OVERFLOW;
+            my_flags |= EP_DEV_QUOTA_OVERFLOW;
             return -1;
         };
-        // the leader of a group whose new count reached lim moves the entry on
-        auto advance = [&](int e, int c) {
+        // the leader of a group that reached the end of its instance moves
+        // e's entries to the instance of its next row (rank = row - del)
+        auto advance = [&](int e, int next_row, int del) {
+            const int x = next_row - del;
             const int end = ptr[e + 1];
-            const int m = upper_bound(bcum, ptr[e], end, c);
-            int2* z = reinterpret_cast<int2*>(tab + e) + 1;
-            *z = (m < end) ? make_int2(bcum[m], bdel[m]) : make_int2(c, 0);
+            const int m = upper_bound(bcum, ptr[e], end, x);
+            const int nd = (m < end) ? bdel[m] : 0;
+            hot[e].y = (unsigned)(x + nd);
+            cold[e] = make_int2((m < end) ? bcum[m] + nd : x, nd);
         };
-        auto store_rows = [&](int sl, int4 rows) {
+        // a step whose lanes hold a repeated id: four sub-steps of 32
+        // consecutive slots, one slot per lane, in slot order
+        auto step_by_slot = [&](int4 q, int st) {
+#pragma unroll 1
+            for (int a = 0; a < 4; ++a) {
+                const int srcl = (a << 3) + (lane >> 2), c = lane & 3;
+                const int qx = __shfl_sync(kFull, q.x, srcl), qy = __shfl_sync(kFull, q.y, srcl);
+                const int qz = __shfl_sync(kFull, q.z, srcl), qw = __shfl_sync(kFull, q.w, srcl);
+                const int id = c == 0 ? qx : c == 1 ? qy : c == 2 ? qz : qw;
+                const int sl = (st << 7) + (a << 5) + lane;
+                const bool v = (unsigned)id < (unsigned)E;
+                const int e = v ? id : E;
+                atomicOr(&hotw[2 * e], bit);
+                __syncwarp();
+                const uint2 h = hot[e];
+                const int2 cd = cold[e];
+                const unsigned below = h.x & lt;
+                int row = (int)h.y + __popc(below);
+                const int nr = (int)h.y + __popc(h.x);
+                const bool lead = below == 0u;
+                __syncwarp();
+                if (lead) hot[e] = make_uint2(0u, (unsigned)nr);
+                if (v && row >= cd.x) row = search(e, row - cd.y);
+                __syncwarp();
+                if (lead && v && nr >= cd.x) advance(e, nr, cd.y);
+                __syncwarp();
+                row = v ? row : -1;
+                if ((unsigned)row >= (unsigned)N && v && row >= 0) my_flags |= EP_DEV_QUOTA_OVERFLOW;
+                row = ((unsigned)row < (unsigned)N) ? row : -1;
+                if (sl < L) {
+                    dsw[sl] = row;
+                    if (srci != nullptr && row >= 0) srci[row] = s0 + sl;
+                }
+            }
+        };
+
+        int ovf = 0, bad = 0;
+#pragma unroll 1
+        for (int st = 0; st < nsteps; ++st) {
+            const int4 q = buf[0];
+#pragma unroll
+            for (int j = 0; j + 1 < kQuadAhead; ++j) buf[j] = buf[j + 1];
+            buf[kQuadAhead - 1] = load_step(st + kQuadAhead);
+            const int sl = (st << 7) + (lane << 2);
+            // invalid ids and slots past the end: the spare entries E + a
+            const bool v0 = (unsigned)q.x < (unsigned)E, v1 = (unsigned)q.y < (unsigned)E;
+            const bool v2 = (unsigned)q.z < (unsigned)E, v3 = (unsigned)q.w < (unsigned)E;
+            const int e0 = v0 ? q.x : E, e1 = v1 ? q.y : E + 1;
+            const int e2 = v2 ? q.z : E + 2, e3 = v3 ? q.w : E + 3;
+            bad |= (sl < L) && !(v0 && v1 && v2 && v3);
+            const bool dup = (e0 == e1) || (e0 == e2) || (e0 == e3) || (e1 == e2) ||
+                             (e1 == e3) || (e2 == e3);
+            if (__any_sync(kFull, dup)) {
+                step_by_slot(q, st);
+                continue;
+            }
+            atomicOr(&hotw[2 * e0], bit);
+            atomicOr(&hotw[2 * e1], bit);
+            atomicOr(&hotw[2 * e2], bit);
+            atomicOr(&hotw[2 * e3], bit);
+            __syncwarp();
+            const uint2 h0 = hot[e0], h1 = hot[e1], h2 = hot[e2], h3 = hot[e3];
+            const unsigned b0 = h0.x & lt, b1 = h1.x & lt, b2 = h2.x & lt, b3 = h3.x & lt;
+            int4 rows = make_int4((int)h0.y + __popc(b0), (int)h1.y + __popc(b1),
+                                  (int)h2.y + __popc(b2), (int)h3.y + __popc(b3));
+            const int n0 = (int)h0.y + __popc(h0.x), n1 = (int)h1.y + __popc(h1.x);
+            const int n2 = (int)h2.y + __popc(h2.x), n3 = (int)h3.y + __popc(h3.x);
+            __syncwarp();
+            if (b0 == 0u) hot[e0] = make_uint2(0u, (unsigned)n0);
+            if (b1 == 0u) hot[e1] = make_uint2(0u, (unsigned)n1);
+            if (b2 == 0u) hot[e2] = make_uint2(0u, (unsigned)n2);
+            if (b3 == 0u) hot[e3] = make_uint2(0u, (unsigned)n3);
+            // a group reaching the end of its instance: the leader sees it
+            const bool x0 = b0 == 0u && n0 >= cold[e0].x, x1 = b1 == 0u && n1 >= cold[e1].x;
+            const bool x2 = b2 == 0u && n2 >= cold[e2].x, x3 = b3 == 0u && n3 >= cold[e3].x;
+            if (__any_sync(kFull, x0 || x1 || x2 || x3)) {
+                // every slot past its entry's end searches; then the leaders
+                // move their entries on
+                const int2 c0 = cold[e0], c1 = cold[e1], c2 = cold[e2], c3 = cold[e3];
+                if (v0 && rows.x >= c0.x) rows.x = search(e0, rows.x - c0.y);
+                if (v1 && rows.y >= c1.x) rows.y = search(e1, rows.y - c1.y);
+                if (v2 && rows.z >= c2.x) rows.z = search(e2, rows.z - c2.y);
+                if (v3 && rows.w >= c3.x) rows.w = search(e3, rows.w - c3.y);
+                __syncwarp();
+                if (x0 && v0) advance(e0, n0, c0.y);
+                if (x1 && v1) advance(e1, n1, c1.y);
+                if (x2 && v2) advance(e2, n2, c2.y);
+                if (x3 && v3) advance(e3, n3, c3.y);
+            }
+            __syncwarp();
+            rows.x = v0 ? rows.x : -1;
+            rows.y = v1 ? rows.y : -1;
+            rows.z = v2 ? rows.z : -1;
+            rows.w = v3 ? rows.w : -1;
+            ovf |= (rows.x >= (int)N) | (rows.y >= (int)N) | (rows.z >= (int)N) |
+                   (rows.w >= (int)N);
+            rows.x = ((unsigned)rows.x < (unsigned)N) ? rows.x : -1;
+            rows.y = ((unsigned)rows.y < (unsigned)N) ? rows.y : -1;
+            rows.z = ((unsigned)rows.z < (unsigned)N) ? rows.z : -1;
+            rows.w = ((unsigned)rows.w < (unsigned)N) ? rows.w : -1;
             if (sl < L) {
                 __stcs(reinterpret_cast<int4*>(dsw + sl), rows);
                 if (srci != nullptr) {
@@ -754,117 +869,15 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
                     if (rows.w >= 0) srci[rows.w] = g + 3;
                 }
             }
-        };
-        // one slot's row from its (valid) rank and entry, range-checked
-        auto finish = [&](bool v, int row) -> int {
-            if (!v) return -1;
-            if ((unsigned)row >= (unsigned)N) {
-                my_flags |= EP_DEV_QUOTA_OVERFLOW;
-                return -1;
-            }
-            return row;
-        };
-        // a step whose lanes hold a repeated id: four sub-steps of 32
-        // consecutive slots, one slot per lane, in slot order
-        auto step_by_slot = [&](int4 q, int st) {
-#pragma unroll 1
-            for (int a = 0; a < 4; ++a) {
-                const int srcl = (a << 3) + (lane >> 2), c = lane & 3;
-                const int qx = __shfl_sync(kFull, q.x, srcl), qy = __shfl_sync(kFull, q.y, srcl);
-                const int qz = __shfl_sync(kFull, q.z, srcl), qw = __shfl_sync(kFull, q.w, srcl);
-                const int e = c == 0 ? qx : c == 1 ? qy : c == 2 ? qz : qw;
-                const int sl = (st << 7) + (a << 5) + lane;
-                const bool v = (unsigned)e < (unsigned)E;
-                if (v) atomicOr(&tabw[4 * e], bit);
-                __syncwarp();
-                const int4 en = v ? tab[e] : make_int4(0, 0, 0, 0);
-                const unsigned below = (unsigned)en.x & lt;
-                const int rk = en.y + __popc(below);
-                const int nc = en.y + __popc((unsigned)en.x);
-                const bool lead = v && below == 0u;
-                int row = rk + en.w;
-                __syncwarp();
-                if (lead) *reinterpret_cast<int2*>(tab + e) = make_int2(0, nc);
-                if (lead && nc >= en.z) advance(e, nc);
-                if (v && rk >= en.z) row = search(e, rk, my_flags);
-                __syncwarp();
-                row = finish(v, row);
-                if (sl < L) {
-                    dsw[sl] = row;
-                    if (srci != nullptr && row >= 0) srci[row] = s0 + sl;
-                }
-            }
-        };
-
-#pragma unroll 1
-        for (int st = 0; st < nsteps; ++st) {
-            {
-                const int4 q = buf[0];
-#pragma unroll
-                for (int j = 0; j + 1 < kQuadAhead; ++j) buf[j] = buf[j + 1];
-                buf[kQuadAhead - 1] = load_step(st + kQuadAhead);
-                const int sl = (st << 7) + (lane << 2);
-                const bool v0 = (unsigned)q.x < (unsigned)E, v1 = (unsigned)q.y < (unsigned)E;
-                const bool v2 = (unsigned)q.z < (unsigned)E, v3 = (unsigned)q.w < (unsigned)E;
-                if (sl < L && !(v0 && v1 && v2 && v3)) my_flags |= EP_DEV_BAD_ID;
-                const bool dup = (v0 && v1 && q.x == q.y) || (v0 && v2 && q.x == q.z) ||
-                                 (v0 && v3 && q.x == q.w) || (v1 && v2 && q.y == q.z) ||
-                                 (v1 && v3 && q.y == q.w) || (v2 && v3 && q.z == q.w);
-                if (__any_sync(kFull, dup)) {
-                    step_by_slot(q, st);
-                    continue;
-                }
-                if (v0) atomicOr(&tabw[4 * q.x], bit);
-                if (v1) atomicOr(&tabw[4 * q.y], bit);
-                if (v2) atomicOr(&tabw[4 * q.z], bit);
-                if (v3) atomicOr(&tabw[4 * q.w], bit);
-                __syncwarp();
-                const int4 n0 = v0 ? tab[q.x] : make_int4(0, 0, 0, 0);
-                const int4 n1 = v1 ? tab[q.y] : make_int4(0, 0, 0, 0);
-                const int4 n2 = v2 ? tab[q.z] : make_int4(0, 0, 0, 0);
-                const int4 n3 = v3 ? tab[q.w] : make_int4(0, 0, 0, 0);
-                const unsigned b0 = (unsigned)n0.x & lt, b1 = (unsigned)n1.x & lt;
-                const unsigned b2 = (unsigned)n2.x & lt, b3 = (unsigned)n3.x & lt;
-                const int k0 = n0.y + __popc(b0), k1 = n1.y + __popc(b1);
-                const int k2 = n2.y + __popc(b2), k3 = n3.y + __popc(b3);
-                const int c0 = n0.y + __popc((unsigned)n0.x), c1 = n1.y + __popc((unsigned)n1.x);
-                const int c2 = n2.y + __popc((unsigned)n2.x), c3 = n3.y + __popc((unsigned)n3.x);
-                const bool l0 = v0 && b0 == 0u, l1 = v1 && b1 == 0u;
-                const bool l2 = v2 && b2 == 0u, l3 = v3 && b3 == 0u;
-                int4 rows = make_int4(k0 + n0.w, k1 + n1.w, k2 + n2.w, k3 + n3.w);
-                const bool x0 = v0 && k0 >= n0.z, x1 = v1 && k1 >= n1.z;
-                const bool x2 = v2 && k2 >= n2.z, x3 = v3 && k3 >= n3.z;
-                __syncwarp();
-                if (l0) *reinterpret_cast<int2*>(tab + q.x) = make_int2(0, c0);
-                if (l1) *reinterpret_cast<int2*>(tab + q.y) = make_int2(0, c1);
-                if (l2) *reinterpret_cast<int2*>(tab + q.z) = make_int2(0, c2);
-                if (l3) *reinterpret_cast<int2*>(tab + q.w) = make_int2(0, c3);
-                // rare: a group past its entry's lim (a replica boundary)
-                const bool a0 = l0 && c0 >= n0.z, a1 = l1 && c1 >= n1.z;
-                const bool a2 = l2 && c2 >= n2.z, a3 = l3 && c3 >= n3.z;
-                if (__any_sync(kFull, a0 || a1 || a2 || a3 || x0 || x1 || x2 || x3)) {
-                    if (a0) advance(q.x, c0);
-                    if (a1) advance(q.y, c1);
-                    if (a2) advance(q.z, c2);
-                    if (a3) advance(q.w, c3);
-                    if (x0) rows.x = search(q.x, k0, my_flags);
-                    if (x1) rows.y = search(q.y, k1, my_flags);
-                    if (x2) rows.z = search(q.z, k2, my_flags);
-                    if (x3) rows.w = search(q.w, k3, my_flags);
-                }
-                __syncwarp();
-                rows.x = finish(v0, rows.x);
-                rows.y = finish(v1, rows.y);
-                rows.z = finish(v2, rows.z);
-                rows.w = finish(v3, rows.w);
-                store_rows(sl, rows);
-            }
         }
-        // every slot of the rank is ranked: the running counts must have
-        // reached the prefix over the ranks up to and including this one
+        if (ovf) my_flags |= EP_DEV_QUOTA_OVERFLOW;
+        if (bad) my_flags |= EP_DEV_BAD_ID;
+        // every slot of the rank is ranked: the rank each expert reached
+        // (next row - del) must be the prefix over the ranks up to and
+        // including this one
         const int32_t* want = pre + (warp + 1) * E;
         for (int e = lane; e < E; e += 32)
-            if (tab[e].y != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
+            if ((int)hot[e].y - cold[e].y != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
     }
     if (my_flags) atomicOr(&flags, my_flags);
     __syncthreads();
