@@ -316,6 +316,9 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     int32_t* slot = reinterpret_cast<int32_t*>(base + align16((size_t)P * 4));
     uint64_t* holder = reinterpret_cast<uint64_t*>(base + align16((size_t)P * 4) +
                                                    align16((size_t)R * S * 4));
+    int32_t* csr_pos = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(holder) +
+                                                  align16((size_t)E * 8));
+    int32_t* csr_val = csr_pos + align16((size_t)(E + 1) * 4) / 4;
     int32_t* qo = quota_out + (int64_t)g * P;
     int32_t* so = slot_out + (int64_t)g * R * S;
     int32_t* lo = load_out + (int64_t)g * R;
@@ -350,7 +353,7 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     __syncwarp();
 
     // logical -> physical CSR: home first, then replicas by ascending rank (= ascending p)
-    plan_csr(q, slot, holder, R, E, S, lane, ptr_out + (int64_t)g * (E + 1),
+    plan_csr(q, slot, holder, R, E, S, lane, csr_pos, csr_val, ptr_out + (int64_t)g * (E + 1),
              id_out + (int64_t)g * (E + R * S), cum_out + (int64_t)g * (E + R * S));
     if (lane == 0) {
         iter_out[g] = iters;

@@ -17,12 +17,16 @@
 namespace ultraep {
 
 constexpr long long kPackLimit = 1ll << 25;  // total below this: loads fit a 6-bit-shifted key
+constexpr long long kQPackLimit = 1ll << 21; // ... and quotas fit a 10-bit-shifted key
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// One warp's shared memory: q[P], slot[R*S], holder[E] (the table), then the
+// CSR epilogue's scratch pos[E+1] and val[E+R*S].
 __host__ __device__ inline size_t plan_warp_bytes(int R, int E, int S) {
     const int P = R * (E / R + S);
-    return align16((size_t)P * 4) + align16((size_t)R * S * 4) + (size_t)E * 8;
+    return align16((size_t)P * 4) + align16((size_t)R * S * 4) + align16((size_t)E * 8) +
+           align16((size_t)(E + 1) * 4) + align16((size_t)(E + R * S) * 4);
 }
 
 // Hottest rank (lowest index on ties) and its load.
@@ -52,7 +56,17 @@ __device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB
 // free slot), and the bookkeeping is a few single-lane stores, so nothing in a
 // move grows with the instances per rank.  Same rule, same ties, same outputs
 // as plan_moves with no flags; the tables are exactly the epilogue's.
-template <bool kTwo, bool kPacked>
+//
+// Every quota and spare-slot entry of the table is read and written by one
+// lane only: lane j owns local instance j of every rank (q[r*W + j] and, for
+// j >= H, slot[r*S + j - H]); every lane writes the same value to a holder
+// mask.  So each lane sees its own earlier writes in program order and a move
+// needs no warp barrier before the next one reads the table: the bookkeeping
+// of one move overlaps the search of the next.
+//
+// kQPacked (total below 2^21): the hot rank's largest instance (lowest expert
+// on ties) is one max-reduction over the key 1 + (quota << 10 | 1023 - e).
+template <bool kTwo, bool kPacked, bool kQPacked>
 __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint64_t* holder,
                                                  int& loadA, int& loadB, int lane, int H, int S,
                                                  int W, int R, int max_iters, int& iters,
@@ -61,24 +75,34 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
     const int ra = lane, rb = lane + 32;
     const uint64_t exist = (R >= 64) ? ~0ull : ((1ull << R) - 1ull);
     uint64_t freem = S > 0 ? exist : 0ull;  // ranks with a free spare slot (warp-uniform)
+    const bool owner = lane < W;            // lane j owns local instance j
+    const bool spare = lane >= H && owner;  // ... a spare slot of every rank
     int hot, Lmax;
     argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, hot, Lmax);
     while (true) {
         // 2. hot's largest-quota instance, lowest expert on ties (lane j:
         // instance j; every rank has its H >= 1 home instances)
-        int qj = -1;
-        unsigned cxj = 0xffffffffu;
-        if (lane < W) {  // the two loads are independent
-            const int xj = lane < H ? hot * H + lane : slot[hot * S + (lane - H)];
-            const int qv = q[hot * W + lane];
-            if (xj >= 0) {
-                qj = qv;
-                cxj = ((unsigned)xj << 5) | (unsigned)lane;
-            }
+        int xj = -1, qv = 0;
+        if (owner) {  // the two loads are independent
+            xj = lane < H ? hot * H + lane : slot[hot * S + (lane - H)];
+            qv = q[hot * W + lane];
         }
-        const int qmax = __reduce_max_sync(kFull, qj);
-        const unsigned cx = __reduce_min_sync(kFull, qj == qmax ? cxj : 0xffffffffu);
-        const int e = (int)(cx >> 5), src_j = (int)(cx & 31u);
+        int qmax, e;
+        bool mine;  // this lane owns the instance that gives
+        if (kQPacked) {
+            const unsigned key = (xj >= 0) ? 1u + (((unsigned)qv << 10) | (unsigned)(1023 - xj)) : 0u;
+            const unsigned kmax = __reduce_max_sync(kFull, key);
+            qmax = (int)((kmax - 1u) >> 10);
+            e = 1023 - (int)((kmax - 1u) & 1023u);
+            mine = key == kmax;
+        } else {
+            const int qj = xj >= 0 ? qv : -1;
+            const unsigned cxj = xj >= 0 ? (((unsigned)xj << 5) | (unsigned)lane) : 0xffffffffu;
+            qmax = __reduce_max_sync(kFull, qj);
+            const unsigned cx = __reduce_min_sync(kFull, qj == qmax ? cxj : 0xffffffffu);
+            e = (int)(cx >> 5);
+            mine = lane == (int)(cx & 31u);
+        }
 
         // 3-5. eligible ranks: the others that hold e or have a free slot;
         // the coldest of them (lowest rank on ties) and the amount
@@ -116,11 +140,11 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, nhot, nLmax);
         // ... and the tables: cold's instance of e is its home, a spare slot
         // already holding e, or its lowest free spare slot (filled now).  The
-        // spare slots are read and voted on unconditionally (no branch), so
-        // this overlaps the argmax above.
-        const int sv = (lane < S) ? slot[cold * S + lane] : 0;
-        const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
-        const unsigned freeb = __ballot_sync(kFull, lane < S && sv < 0);  // cold's free slots
+        // spare slots are read by their owner lanes and voted on
+        // unconditionally (no branch), so this overlaps the argmax above.
+        const int sv = spare ? slot[cold * S + (lane - H)] : 0;
+        const unsigned hit = __ballot_sync(kFull, spare && sv == e);
+        const unsigned freeb = __ballot_sync(kFull, spare && sv < 0);  // cold's free slots
         const bool held = (hm >> cold) & 1ull;
         const int ej = e - cold * H;
         const bool home = (unsigned)ej < (unsigned)H;  // e is one of cold's home experts
@@ -129,20 +153,15 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
             status = EP_ERR_INVAL;
             break;
         }
-        const int dj = home ? ej : H + __ffs(pick) - 1;
-        // every read of this move was consumed by the warp's votes and
-        // reductions above; the updates are fire-and-forget shared-memory
-        // additions, no read-modify-write chain
-        if (lane == 0) {
-            atomicAdd(&q[hot * W + src_j], -mv);
-            atomicAdd(&q[cold * W + dj], mv);
-            if (!held) {
-                slot[cold * S + (dj - H)] = e;
-                holder[e] = hm | (1ull << cold);
-            }
+        const int dj = home ? ej : __ffs(pick) - 1;     // cold's instance (a lane index)
+        // owner-lane updates, no read-modify-write across lanes
+        if (mine) q[hot * W + lane] = qv - mv;
+        if (lane == dj) {
+            q[cold * W + lane] += mv;
+            if (!held) slot[cold * S + (lane - H)] = e;
         }
+        if (!held) holder[e] = hm | (1ull << cold);  // every lane, the same value
         if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
-        __syncwarp();  // the updates land before the next move reads the table
         hot = nhot;
         Lmax = nLmax;
         ++iters;
@@ -195,14 +214,17 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
     }
     __syncwarp();
     if (status == EP_OK) {
-        if (tot < kPackLimit)
-            plan_moves_table<kTwo, true>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
-                                         max_iters, iters, status);
+        if (tot < kQPackLimit)
+            plan_moves_table<kTwo, true, true>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
+                                               max_iters, iters, status);
+        else if (tot < kPackLimit)
+            plan_moves_table<kTwo, true, false>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
+                                                max_iters, iters, status);
         else
-            plan_moves_table<kTwo, false>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
-                                          max_iters, iters, status);
+            plan_moves_table<kTwo, false, false>(q, slot, holder, loadA, loadB, lane, H, S, W,
+                                                 R, max_iters, iters, status);
     }
-    __syncwarp();
+    __syncwarp();  // the table's entries, written by their owner lanes, for every lane
     for (int p = lane; p < P; p += 32) qo[p] = q[p];
     for (int x = lane; x < R * S; x += 32) so[x] = slot[x];
     if (lane < R) lo[lane] = loadA;
@@ -211,16 +233,21 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
 
 // Logical -> physical CSR from the tables: for each expert its home instance
 // first, then its replicas by ascending rank (= ascending p), with inclusive
-// cumulative quotas.  One warp; writes po[0..E], io and co.
+// cumulative quotas.  One warp; writes po[0..E], io and co.  The list offsets
+// are one warp scan over the holder counts; every spare slot then finds its
+// own place in its expert's list (1 + its expert's replicas on lower ranks),
+// and each expert's running sums are one short walk over its list.  pos[E+1]
+// and val[E+R*S] are shared-memory scratch (the offsets and each entry's
+// quota).
 __device__ __forceinline__ void plan_csr(const int32_t* q, const int32_t* slot,
                                          const uint64_t* holder, int R, int E, int S, int lane,
-                                         int32_t* po, int32_t* io, int32_t* co) {
+                                         int32_t* pos, int32_t* val, int32_t* po, int32_t* io,
+                                         int32_t* co) {
     const int H = E / R, W = H + S;
     int run = 0;
     for (int e0 = 0; e0 < E; e0 += 32) {
         const int e = e0 + lane;
-        const uint64_t hm = (e < E) ? holder[e] : 0ull;
-        const int n = __popcll(hm);
+        const int n = (e < E) ? __popcll(holder[e]) : 0;
         int x = n;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -228,30 +255,41 @@ __device__ __forceinline__ void plan_csr(const int32_t* q, const int32_t* slot,
             if (lane >= o) x += y;
         }
         if (e < E) {
-            int m = run + x - n;
+            const int m = run + x - n;
+            pos[e] = m;
             po[e] = m;
             const int home = e / H;
-            const int hp = home * W + (e - home * H);
-            int cum = q[hp];
+            const int hp = home * W + (e - home * H);  // the home instance heads the list
             io[m] = hp;
-            co[m] = cum;
-            ++m;
-            uint64_t rest = hm & ~(1ull << home);
-            while (rest) {
-                const int c = __ffsll((long long)rest) - 1;
-                rest &= rest - 1;
-                int j = 0;
-                while (j < S && slot[c * S + j] != e) ++j;
-                const int p = c * W + H + j;
-                cum += q[p];
-                io[m] = p;
-                co[m] = cum;
-                ++m;
-            }
+            val[m] = q[hp];
         }
         run += __shfl_sync(kFull, x, 31);
     }
-    if (lane == 0) po[E] = run;
+    if (lane == 0) {
+        po[E] = run;
+        pos[E] = run;
+    }
+    __syncwarp();
+    // replicas: slot (c, s) of expert e sits after e's home and e's replicas on ranks below c
+    for (int x = lane; x < R * S; x += 32) {
+        const int e = slot[x];
+        if (e < 0) continue;
+        const int c = x / S, s = x - c * S;
+        const uint64_t lower = holder[e] & ~(1ull << (e / H)) & ((1ull << c) - 1ull);
+        const int m = pos[e] + 1 + __popcll(lower);
+        const int p = c * W + H + s;
+        io[m] = p;
+        val[m] = q[p];
+    }
+    __syncwarp();
+    for (int e = lane; e < E; e += 32) {
+        const int m1 = pos[e + 1];
+        int cum = 0;
+        for (int m = pos[e]; m < m1; ++m) {
+            cum += val[m];
+            co[m] = cum;
+        }
+    }
 }
 
 }  // namespace ultraep

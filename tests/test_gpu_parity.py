@@ -150,6 +150,9 @@ CASES = [
     ("quad_max_E_and_k",   64, 16, 16, 32, 257, 5,      8,   "zipf"),
     ("quad_R36_uniform",   36, 4, 1, 4,  4000,  9,      8,   "uniform"),
     ("quad_one_expert",    8,  4, 2, 4,  5000,  40,     8,   "one"),
+    # the quad kernel with many slots per rank and with E in (256, 512]
+    ("quad_long_ranks",    8,  4, 1, 8,  20000, 37,     8,   "bad"),
+    ("quad_E320",          16, 20, 2, 8, 3000,  19,     8,   "bad"),
 ]
 
 
