@@ -44,19 +44,23 @@ DeviceInfo device_info();
 int count_chunks_per_rank(const ep_domain_t& d, int64_t T, int32_t n_inst);
 size_t count_workspace_bytes(const ep_domain_t& d, int64_t T, int32_t n_inst);
 size_t count_ticket_bytes(int32_t n_inst);
+// rows_only: write counts_src only (the planner of ep_balance sums the rows)
 cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                          int32_t* counts, int32_t* counts_src, int32_t* dev_status, void* ws,
-                         cudaStream_t s);
+                         cudaStream_t s, bool rows_only = false);
 size_t count_noalloc_scratch_capacity();
 cudaError_t launch_count_noalloc(const ep_domain_t& d, const int32_t* ids, int64_t T,
                                  int32_t n_inst, int32_t* counts, int32_t* counts_src,
                                  int32_t* dev_status, cudaStream_t s);
 
 // plan
+// counts_src non-null (ep_balance): every instance first sums counts_src over
+// the source ranks into counts, then plans
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
                         int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
                         int32_t* inst_ptr, int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter,
-                        int32_t* inst_status, cudaStream_t s, bool pdl = false);
+                        int32_t* inst_status, cudaStream_t s, bool pdl = false,
+                        const int32_t* counts_src = nullptr);
 
 // reroute
 cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,

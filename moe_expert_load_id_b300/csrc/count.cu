@@ -93,7 +93,7 @@ __device__ __forceinline__ void count_one(int v, int E, int32_t* hist, int C, in
 __global__ void __launch_bounds__(kCountThreads, 2048 / kCountThreads)
 count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int cps,
              int32_t* __restrict__ counts, int32_t* __restrict__ counts_src,
-             int32_t* dev_status, uint32_t* inst_ticket) {
+             int32_t* dev_status, uint32_t* inst_ticket, int rows_only) {
     extern __shared__ __align__(16) int32_t sh[];
     __shared__ int bad;
     __shared__ int is_last;
@@ -186,6 +186,9 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
         for (int e = tid; e < E; e += kCountThreads) counts_src[rank_row + e] = blk[e];
     }
 
+    // rows_only (ep_balance): the planner, which waits for this grid, sums the
+    // rows itself, so the blocks stop here
+    if (rows_only) return;
     // the last source rank of the instance folds counts_src into counts.  The
     // barrier orders the block's counts_src writes before thread 0's fence and
     // ticket (fences are cumulative), so one thread fences for the block; the
@@ -272,7 +275,7 @@ size_t count_ticket_bytes(int32_t n_inst) { return (size_t)n_inst * sizeof(uint3
 
 cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                          int32_t* counts, int32_t* counts_src, int32_t* dev_status, void* ws,
-                         cudaStream_t s) {
+                         cudaStream_t s, bool rows_only) {
     if (n_inst == 0) return cudaSuccess;
     const int cps = count_chunks_per_rank(d, T, n_inst);
     uint32_t* inst_ticket = static_cast<uint32_t*>(ws);
@@ -290,7 +293,7 @@ cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, in
     cfg.attrs = attr;
     cfg.numAttrs = cps > 1 ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, count_kernel, ids, T, (int)d.k, (int)d.R, (int)d.E, cps,
-                              counts, counts_src, dev_status, inst_ticket);
+                              counts, counts_src, dev_status, inst_ticket, rows_only ? 1 : 0);
 }
 
 }  // namespace ultraep

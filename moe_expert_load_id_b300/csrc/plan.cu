@@ -292,7 +292,8 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
             int32_t* __restrict__ quota_out, int32_t* __restrict__ slot_out,
             int32_t* __restrict__ load_out, int32_t* __restrict__ ptr_out,
             int32_t* __restrict__ id_out, int32_t* __restrict__ cum_out,
-            int32_t* __restrict__ iter_out, int32_t* __restrict__ status_out) {
+            int32_t* __restrict__ iter_out, int32_t* __restrict__ status_out,
+            const int32_t* __restrict__ counts_src, int32_t* __restrict__ counts_out) {
     extern __shared__ __align__(16) unsigned char smem[];
     // in ep_balance this grid is a programmatic dependent of ep_count: wait for
     // its counts, then let the dependent reroute start its plan-independent
@@ -301,17 +302,56 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = blockIdx.x * kPlanWarps + warp;
-    if (g >= n_inst) return;  // whole warp; no block-wide barrier follows
-
     const int H = E / R, W = H + S, P = R * W;
+    const size_t wbytes = plan_warp_bytes(R, E, S);
+    // the instance's counts: counts_src summed over the source ranks by the
+    // whole block (ep_balance, whose count stops at the per-rank rows), or
+    // the counts input
     const int32_t* cnt = counts + (int64_t)g * E;
+    if (counts_src != nullptr) {
+        int32_t* csum0 = reinterpret_cast<int32_t*>(smem + wbytes - align16((size_t)E * 4));
+        const int g0 = blockIdx.x * kPlanWarps;
+        const int nb = min(kPlanWarps, n_inst - g0);
+        for (int x = threadIdx.x; x < kPlanWarps * E; x += kPlanWarps * 32) {
+            const int w = x / E;
+            csum0[w * (wbytes / 4) + (x - w * E)] = 0;
+        }
+        __syncthreads();
+        // thread (column, row group): column c of E, rows rg, rg + G, ...
+        constexpr int kThr = kPlanWarps * 32;
+        const int G = max(1, kThr / E);
+        for (int x = threadIdx.x; x < nb * E * G; x += kThr) {
+            const int wi = x / (E * G), rem = x - wi * E * G;
+            const int rg = rem / E, e = rem - rg * E;
+            const int32_t* cs = counts_src + (int64_t)(g0 + wi) * R * E + e;
+            int t = 0;
+            for (int r0 = rg; r0 < R; r0 += 8 * G) {
+                int v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int rr = r0 + u * G;
+                    v[u] = (rr < R) ? __ldg(cs + (int64_t)rr * E) : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) t += v[u];
+            }
+            atomicAdd(&csum0[wi * (wbytes / 4) + e], t);
+        }
+        __syncthreads();
+        if (g < n_inst) {
+            const int32_t* mine = csum0 + warp * (wbytes / 4);
+            for (int e = lane; e < E; e += 32) counts_out[(int64_t)g * E + e] = mine[e];
+            cnt = mine;
+        }
+    }
+    if (g >= n_inst) return;  // whole warp; no block-wide barrier follows
 
     // counts must be >= 0 with a total below 2^31; otherwise the instance is
     // rejected (EP_ERR_INVAL) and its outputs describe the home-only placement
     long long tot = 0;
     int status = plan_check_counts(cnt, E, lane, tot);
 
-    unsigned char* base = smem + (size_t)warp * plan_warp_bytes(R, E, S);
+    unsigned char* base = smem + (size_t)warp * wbytes;
     int32_t* q = reinterpret_cast<int32_t*>(base);
     int32_t* slot = reinterpret_cast<int32_t*>(base + align16((size_t)P * 4));
     uint64_t* holder = reinterpret_cast<uint64_t*>(base + align16((size_t)P * 4) +
@@ -366,7 +406,7 @@ cudaError_t launch_plan_k(const ep_domain_t& d, const int32_t* counts, int32_t n
                            int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
                            int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                            int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
-                           cudaStream_t s, bool pdl) {
+                           cudaStream_t s, bool pdl, const int32_t* counts_src) {
     const size_t smem = kPlanWarps * plan_warp_bytes(d.R, d.E, d.S);
     if (smem > 48 * 1024) {
         cudaError_t err = cudaFuncSetAttribute(plan_kernel<WB, kTwo, kFlags>,
@@ -386,7 +426,8 @@ cudaError_t launch_plan_k(const ep_domain_t& d, const int32_t* counts, int32_t n
     cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, plan_kernel<WB, kTwo, kFlags>, counts, (int)n_inst, (int)d.R,
                               (int)d.E, (int)d.S, (int)max_iters, (int)flags, quota, slot_expert, rank_load,
-                              inst_ptr, inst_id, inst_cum, n_iter, inst_status);
+                              inst_ptr, inst_id, inst_cum, n_iter, inst_status, counts_src,
+                              const_cast<int32_t*>(counts));
 }
 
 // the flag-free base rule gets its own kernel
@@ -395,14 +436,14 @@ cudaError_t launch_plan_wb(const ep_domain_t& d, const int32_t* counts, int32_t 
                            int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
                            int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                            int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
-                           cudaStream_t s, bool pdl) {
+                           cudaStream_t s, bool pdl, const int32_t* counts_src) {
     if (flags != 0)
         return launch_plan_k<WB, kTwo, true>(d, counts, n_inst, max_iters, flags, quota,
                                              slot_expert, rank_load, inst_ptr, inst_id, inst_cum,
-                                             n_iter, inst_status, s, pdl);
+                                             n_iter, inst_status, s, pdl, counts_src);
     return launch_plan_k<WB, kTwo, false>(d, counts, n_inst, max_iters, flags, quota, slot_expert,
                                           rank_load, inst_ptr, inst_id, inst_cum, n_iter,
-                                          inst_status, s, pdl);
+                                          inst_status, s, pdl, counts_src);
 }
 
 template <int WB>
@@ -410,14 +451,14 @@ cudaError_t launch_plan_r(const ep_domain_t& d, const int32_t* counts, int32_t n
                           int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,
                           int32_t* rank_load, int32_t* inst_ptr, int32_t* inst_id,
                           int32_t* inst_cum, int32_t* n_iter, int32_t* inst_status,
-                          cudaStream_t s, bool pdl) {
+                          cudaStream_t s, bool pdl, const int32_t* counts_src) {
     if (d.R > 32)
         return launch_plan_wb<WB, true>(d, counts, n_inst, max_iters, flags, quota, slot_expert,
                                         rank_load, inst_ptr, inst_id, inst_cum, n_iter,
-                                        inst_status, s, pdl);
+                                        inst_status, s, pdl, counts_src);
     return launch_plan_wb<WB, false>(d, counts, n_inst, max_iters, flags, quota, slot_expert,
                                      rank_load, inst_ptr, inst_id, inst_cum, n_iter,
-                                     inst_status, s, pdl);
+                                     inst_status, s, pdl, counts_src);
 }
 
 }  // namespace
@@ -425,14 +466,14 @@ cudaError_t launch_plan_r(const ep_domain_t& d, const int32_t* counts, int32_t n
 cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
                         int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert, int32_t* rank_load,
                         int32_t* inst_ptr, int32_t* inst_id, int32_t* inst_cum, int32_t* n_iter,
-                        int32_t* inst_status, cudaStream_t s, bool pdl) {
+                        int32_t* inst_status, cudaStream_t s, bool pdl, const int32_t* counts_src) {
     if (n_inst == 0) return cudaSuccess;
     // register arrays sized to the instances per rank W = H + S (<= 32)
     const int W = d.E / d.R + d.S;
 #define EP_PLAN_WB(wb)                                                                       \
     if (W <= wb)                                                                             \
         return launch_plan_r<wb>(d, counts, n_inst, max_iters, flags, quota, slot_expert, rank_load, \
-                                 inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl);
+                                 inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl, counts_src);
     EP_PLAN_WB(2)
     EP_PLAN_WB(3)
     EP_PLAN_WB(4)
@@ -441,7 +482,7 @@ cudaError_t launch_plan(const ep_domain_t& d, const int32_t* counts, int32_t n_i
     EP_PLAN_WB(16)
 #undef EP_PLAN_WB
     return launch_plan_r<32>(d, counts, n_inst, max_iters, flags, quota, slot_expert, rank_load,
-                             inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl);
+                             inst_ptr, inst_id, inst_cum, n_iter, inst_status, s, pdl, counts_src);
 }
 
 }  // namespace ultraep

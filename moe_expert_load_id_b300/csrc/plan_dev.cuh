@@ -21,12 +21,14 @@ constexpr long long kQPackLimit = 1ll << 21; // ... and quotas fit a 10-bit-shif
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
-// One warp's shared memory: q[P], slot[R*S], holder[E] (the table), then the
-// CSR epilogue's scratch pos[E+1] and val[E+R*S].
+// One warp's shared memory: q[P], slot[R*S], holder[E] (the table), the CSR
+// epilogue's scratch pos[E+1] and val[E+R*S], and the instance's counts[E]
+// when the planner sums them itself.
 __host__ __device__ inline size_t plan_warp_bytes(int R, int E, int S) {
     const int P = R * (E / R + S);
     return align16((size_t)P * 4) + align16((size_t)R * S * 4) + align16((size_t)E * 8) +
-           align16((size_t)(E + 1) * 4) + align16((size_t)(E + R * S) * 4);
+           align16((size_t)(E + 1) * 4) + align16((size_t)(E + R * S) * 4) +
+           align16((size_t)E * 4);
 }
 
 // Hottest rank (lowest index on ties) and its load.

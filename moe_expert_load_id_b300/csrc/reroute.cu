@@ -40,15 +40,22 @@
 #include <climits>
 #include <type_traits>
 
+#include <cooperative_groups.h>
+
 #include "common.cuh"
 
 namespace ultraep {
 namespace {
 
+namespace cg = cooperative_groups;
+
 // 32-slot steps per warp per chunk (ids held in registers), blocks per SM of
 // the many-block launches (build-time tunables)
 #ifndef EP_REROUTE_ITEMS
 #define EP_REROUTE_ITEMS 16
+#endif
+#ifndef EP_REROUTE_CLUSTER_PARTS
+#define EP_REROUTE_CLUSTER_PARTS 1  // one-layer launches split a rank over a cluster (build-time tunable)
 #endif
 #ifndef EP_REROUTE_BLOCKS_PER_SM
 #define EP_REROUTE_BLOCKS_PER_SM 4
@@ -73,7 +80,8 @@ struct RrLayout {
     size_t bytes;
 };
 
-__host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps, bool ev_smem) {
+__host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps, bool ev_smem,
+                                              int items = kItems) {
     RrLayout l;
     l.P = R * (E / R + S);
     l.M = E + R * S;
@@ -89,13 +97,13 @@ __host__ __device__ inline RrLayout rr_layout(int R, int E, int S, int warps, bo
         l.Es = l.El = E;
     }
     // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E] wx0[warps][Es] wdb[warps][Es]
-    //        want[E]
+    //        want[E] ctot[E]
     // uint16: wlim[warps][El]
     l.lim_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E +
-                                   2 * (size_t)warps * l.Es + E);
+                                   2 * (size_t)warps * l.Es + 2 * (size_t)E);
     l.bytes = l.lim_off + sizeof(uint16_t) * (size_t)warps * l.El;
     l.ev_off = (l.bytes + 15) & ~(size_t)15;
-    if (ev_smem) l.bytes = l.ev_off + sizeof(int32_t) * (size_t)kItems * warps * 32;
+    if (ev_smem) l.bytes = l.ev_off + sizeof(int32_t) * (size_t)items * warps * 32;
     return l;
 }
 
@@ -135,7 +143,8 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
                                             const int32_t* __restrict__ inst_cum,
                                             int32_t* __restrict__ inst_offset, int32_t* off,
                                             int32_t* ptr, int32_t* bcum, int32_t* bdel,
-                                            int32_t* base, int32_t* want, int32_t* warp_tot) {
+                                            int32_t* base, int32_t* want, int32_t* warp_tot,
+                                            bool write_offsets = true) {
     constexpr int kWarps = kThreads / 32;
     constexpr int kIpt = (2048 + kThreads - 1) / kThreads;  // P <= 2048 quota per thread
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -266,7 +275,7 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
         const int p = bdel[m];
         bdel[m] = (p >= 0) ? off[p] - (bcum[m] - (off[p + 1] - off[p])) : 0;
     }
-    if (r == 0) {
+    if (r == 0 && write_offsets) {
         int32_t* og = inst_offset + (int64_t)inst * (P + 1);
         for (int p = tid; p <= P; p += kThreads) og[p] = off[p];
     }
@@ -276,7 +285,14 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
 // chunks of kThreads * kItems.  kThreads = 1024 when few blocks run (one
 // instance: the whole rank is one chunk) and E <= 512; else 256, four blocks
 // per SM (measured faster for batched calls than 512 x 2).
-template <int kThreads>
+//
+// kCl > 1 (one-layer launches): a thread-block cluster of kCl blocks shares
+// one source rank, block c taking the c-th part of its slots as one chunk of
+// kThreads * kIt.  After ranking its part (before the wait for the plan in
+// ep_balance) every block publishes its per-expert totals; block c adds the
+// totals of the blocks below it, read through distributed shared memory, to
+// its starting ranks.  The rank's rows then take kCl SMs instead of one.
+template <int kThreads, int kIt = kItems, int kCl = 1>
 __global__ void __launch_bounds__(kThreads, kThreads == 256 ? EP_REROUTE_BLOCKS_PER_SM : 1024 / kThreads)
 reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int S,
                const int32_t* __restrict__ counts_src, const int32_t* __restrict__ quota,
@@ -285,14 +301,14 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
                int32_t* __restrict__ src_slot, int32_t* __restrict__ inst_offset,
                int32_t* dev_status, int early) {
     constexpr int kWarps = kThreads / 32;
-    constexpr int kChunk = kThreads * kItems;
+    constexpr int kChunk = kThreads * kIt;
     extern __shared__ __align__(16) int32_t sm[];
     __shared__ int32_t warp_tot[kWarps];
     __shared__ int32_t flags;
 
-    static_assert(kItems % 4 == 0, "phase C takes four steps at a time");
+    static_assert(kIt % 4 == 0, "phase C takes four steps at a time");
     constexpr bool kEvSmem = ev_in_smem<kThreads>();
-    const RrLayout lay = rr_layout(R, E, S, kWarps, kEvSmem);
+    const RrLayout lay = rr_layout(R, E, S, kWarps, kEvSmem, kIt);
     const int P = lay.P, M = lay.M;
     int32_t* off = sm;              // [P+1] first row of each instance
     int32_t* ptr = off + (P + 1);   // [E+1] CSR row pointers (clamped)
@@ -303,23 +319,29 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     int32_t* wx0 = base + E;        // [kWarps][Es] per-warp counts, then each warp's first rank
     int32_t* wdb = wx0 + kWarps * Es;  // [kWarps][Es] row of that first rank
     int32_t* want = wdb + kWarps * Es;  // [E] expected base after the last chunk
+    int32_t* ctot = want + E;           // [E] this block's per-expert totals (clusters)
     uint16_t* wlim = reinterpret_cast<uint16_t*>(reinterpret_cast<unsigned char*>(sm) + lay.lim_off);
                                     // [kWarps][El] ranks left in its instance (capped)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int inst = blockIdx.x / R, r = blockIdx.x % R;
+    const int cl = (kCl > 1) ? (int)(blockIdx.x % kCl) : 0;  // rank in the cluster
+    const int unit = (kCl > 1) ? (int)(blockIdx.x / kCl) : (int)blockIdx.x;
+    const int inst = unit / R, r = unit % R;
 
-    // ---- this block's slots (source rank r).  Out-of-range ids are flagged
-    // at load time; slots past the end load as -1.
+    // ---- this block's slots (source rank r, part cl).  Out-of-range ids are
+    // flagged at load time; slots past the end load as -1.
     // (32-bit division: T < 2^31 since T*k < 2^31)
     const int Tr = ((int)T + R - 1) / R;
     const int64_t N = T * k;
-    const int64_t s0 = min(T, (int64_t)r * Tr) * k, s1 = min(T, (int64_t)(r + 1) * Tr) * k;
+    const int64_t rs0 = min(T, (int64_t)r * Tr) * k, rs1 = min(T, (int64_t)(r + 1) * Tr) * k;
+    const int64_t part = (rs1 - rs0 + kCl - 1) / kCl;
+    const int64_t s0 = (kCl > 1) ? min(rs1, rs0 + cl * part) : rs0;
+    const int64_t s1 = (kCl > 1) ? min(rs1, rs0 + (cl + 1) * part) : rs1;
     const int32_t* idi = ids + (int64_t)inst * N;
     int my_flags = 0;
     // item it of this thread: a register, or word it * kThreads + tid of the
     // chunk's shared array (consecutive threads, consecutive banks)
-    int evr[kEvSmem ? 1 : kItems] = {};
+    int evr[kEvSmem ? 1 : kIt] = {};
     int* evs = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(sm) + lay.ev_off) + threadIdx.x;
     auto ev_get = [&](int it) -> int {
         if constexpr (kEvSmem) return evs[it * kThreads];
@@ -329,12 +351,12 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         if constexpr (kEvSmem) evs[it * kThreads] = v;
         else evr[it] = v;
     };
-    const int lbase = warp * 32 * kItems + lane;  // chunk-local index of item 0
+    const int lbase = warp * 32 * kIt + lane;  // chunk-local index of item 0
     auto load_chunk = [&](int64_t cs) {
         const int nc = (int)min((int64_t)kChunk, s1 - cs);
         const int32_t* src = idi + cs;
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
+        for (int it = 0; it < kIt; ++it) {
             const int li = lbase + it * 32;
             const int v = (li < nc) ? __ldcs(src + li) : -1;
             if (li < nc && (unsigned)v >= (unsigned)E) my_flags |= EP_DEV_BAD_ID;
@@ -358,7 +380,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     auto phase_a = [&]() {
         uint32_t* mrow = reinterpret_cast<uint32_t*>(wdb) + warp * Es;
 #pragma unroll
-        for (int it = 0; it < kItems; ++it) {
+        for (int it = 0; it < kIt; ++it) {
             const int e = ev_get(it);
             const bool valid = (unsigned)e < (unsigned)E;
             if (valid) atomicOr(&mrow[e], 1u << lane);
@@ -386,12 +408,33 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         load_chunk(s0);
         phase_a();
     }
+    int lower = 0;  // thread e: slots of e in the cluster's blocks below this one
+    if constexpr (kCl > 1) {
+        // the block's per-expert totals (its one chunk's per-warp counts),
+        // read by the blocks above it through distributed shared memory
+        // (E <= 512 < kThreads: thread e holds expert e)
+        __syncthreads();
+        for (int e = tid; e < E; e += kThreads) {
+            int t = 0;
+            for (int w = 0; w < kWarps; ++w) t += wx0[w * Es + e];
+            ctot[e] = t;
+        }
+        cg::cluster_group cluster = cg::this_cluster();
+        cluster.sync();
+        if (tid < E)
+            for (int c2 = 0; c2 < cl; ++c2) lower += cluster.map_shared_rank(ctot, c2)[tid];
+        cluster.sync();  // every read of a block's totals is done before any block moves on
+    }
     if (early) pdl_wait();
     pdl_trigger();
 
-    // ---- prologue: plan tables
+    // ---- prologue: plan tables (want[] gets the rank's whole count); a block
+    // of a cluster starts at the slots of the blocks below it
     plan_tables<kThreads>(R, E, P, M, inst, r, counts_src, quota, inst_ptr, inst_id, inst_cum,
-                          inst_offset, off, ptr, bcum, bdel, base, want, warp_tot);
+                          inst_offset, off, ptr, bcum, bdel, base, want, warp_tot, cl == 0);
+    if constexpr (kCl > 1) {
+        if (tid < E) base[tid] += lower;  // (thread e alone touches base[e] here)
+    }
     // (the barrier before phase B orders the writes above before any read of
     // bcum / bdel)
 
@@ -517,7 +560,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             // four steps at a time: their rows first (no branch), then the rare
             // search for ranks past the instance of the warp's first rank
 #pragma unroll
-            for (int it0 = 0; it0 < kItems; it0 += 4) {
+            for (int it0 = 0; it0 < kIt; it0 += 4) {
                 int d[4];
                 unsigned slow = 0u;
 #pragma unroll
@@ -573,10 +616,12 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
     }
     // every slot of the rank has been ranked: base[e] - (slots of e on earlier
     // ranks) is this rank's own count of e, which must equal counts_src[r][e]
-    // (the within-expert ranks above started from the counts_src prefix)
+    // (the within-expert ranks above started from the counts_src prefix); in
+    // a cluster the block holding the rank's last part sees the whole count
     __syncthreads();
-    for (int e = tid; e < E; e += kThreads)
-        if (base[e] != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
+    if (cl == kCl - 1)
+        for (int e = tid; e < E; e += kThreads)
+            if (base[e] != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
     if (my_flags) atomicOr(&flags, my_flags);
     __syncthreads();
     if (tid == 0 && flags) raise_flag(dev_status, flags);
@@ -913,36 +958,45 @@ cudaError_t launch_reroute_quad(const ep_domain_t& d, const int32_t* ids, int64_
                               src_slot, inst_offset, dev_status, pdl ? 1 : 0);
 }
 
-template <int kThreads>
+template <int kThreads, int kIt = kItems, int kCl = 1>
 cudaError_t launch_reroute_t(const ep_domain_t& d, const int32_t* ids, int64_t T, int32_t n_inst,
                              const int32_t* counts_src, const int32_t* quota,
                              const int32_t* inst_ptr, const int32_t* inst_id,
                              const int32_t* inst_cum, int32_t* dst_row, int32_t* src_slot,
                              int32_t* inst_offset, int32_t* dev_status, cudaStream_t s,
                              bool pdl) {
-    const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32, ev_in_smem<kThreads>());
+    const RrLayout lay = rr_layout(d.R, d.E, d.S, kThreads / 32, ev_in_smem<kThreads>(), kIt);
     if (lay.bytes > 48 * 1024) {
-        cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads>,
+        cudaError_t err = cudaFuncSetAttribute(reroute_kernel<kThreads, kIt, kCl>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)lay.bytes);
         if (err != cudaSuccess) return err;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)n_inst * d.R));
+    cfg.gridDim = dim3((unsigned)((int64_t)n_inst * d.R * kCl));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = lay.bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int na = 0;
+    if (pdl) {
+        attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    if (kCl > 1) {
+        attr[na].id = cudaLaunchAttributeClusterDimension;
+        attr[na].val.clusterDim.x = kCl;
+        attr[na].val.clusterDim.y = 1;
+        attr[na].val.clusterDim.z = 1;
+        ++na;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, reroute_kernel<kThreads>, ids, T, (int)d.k, (int)d.R,
-                              (int)d.E, (int)d.S, counts_src, quota, inst_ptr, inst_id, inst_cum,
-                              dst_row, src_slot, inst_offset, dev_status, pdl ? 1 : 0);
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, reroute_kernel<kThreads, kIt, kCl>, ids, T, (int)d.k,
+                              (int)d.R, (int)d.E, (int)d.S, counts_src, quota, inst_ptr, inst_id,
+                              inst_cum, dst_row, src_slot, inst_offset, dev_status, pdl ? 1 : 0);
 }
-
-
 
 }  // namespace
 
@@ -970,6 +1024,22 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
     if (blocks >= 2 * (int64_t)sms || d.E > 512 || !wide_fits)
         return launch_reroute_t<256>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
                                       inst_cum, dst_row, src_slot, inst_offset, dev_status, s, pdl);
+    // one-layer launches: a cluster of 2 or 4 blocks per source rank, each
+    // block one chunk of 8192 slots, when the rank has at most 32768 slots
+    const int64_t rank_slots = tokens_per_rank(T, d.R) * d.k;
+    constexpr int kPart = 1024 * 8;
+    const bool parts_fit =
+        rr_layout(d.R, d.E, d.S, 1024 / 32, ev_in_smem<1024>(), 8).bytes + 1024 <= di.smem_optin;
+    if (parts_fit && EP_REROUTE_CLUSTER_PARTS) {
+        if (rank_slots > 2 * kPart && rank_slots <= 4 * kPart)
+            return launch_reroute_t<1024, 8, 4>(d, ids, T, n_inst, counts_src, quota, inst_ptr,
+                                                inst_id, inst_cum, dst_row, src_slot,
+                                                inst_offset, dev_status, s, pdl);
+        if (rank_slots > kPart && rank_slots <= 2 * kPart)
+            return launch_reroute_t<1024, 8, 2>(d, ids, T, n_inst, counts_src, quota, inst_ptr,
+                                                inst_id, inst_cum, dst_row, src_slot,
+                                                inst_offset, dev_status, s, pdl);
+    }
     return launch_reroute_t<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
                                    inst_cum, dst_row, src_slot, inst_offset, dev_status, s,
                                    pdl);

@@ -172,12 +172,14 @@ ep_status_t ep_balance(const ep_domain_t* dom, const int32_t* topk_ids, int64_t 
         return EP_ERR_WORKSPACE;
     if (max_iters <= 0) max_iters = EP_PLAN_MAX_ITERS;
     const cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // count writes the per-source-rank rows only; the planner sums them into
+    // counts (one launch fewer synchronisation points on the critical path)
     cudaError_t err = launch_count(*dom, topk_ids, T, n_inst, out->counts, out->counts_src,
-                                   dev_status, workspace, s);
+                                   dev_status, workspace, s, /*rows_only=*/true);
     if (err != cudaSuccess) return EP_ERR_CUDA;
     err = launch_plan(*dom, out->counts, n_inst, max_iters, 0, out->quota, out->slot_expert,
                       out->rank_load, out->inst_ptr, out->inst_id, out->inst_cum, out->n_iter,
-                      out->inst_status, s, /*pdl=*/true);
+                      out->inst_status, s, /*pdl=*/true, out->counts_src);
     if (err != cudaSuccess) return EP_ERR_CUDA;
     return from_cuda(launch_reroute(*dom, topk_ids, T, n_inst, out->counts_src, out->quota,
                                     out->inst_ptr, out->inst_id, out->inst_cum, out->dst_row,

@@ -57,6 +57,7 @@ def test_balance_matches_oracle_and_separate_calls(case):
     dom = G().dom_of(R, E, S, k)
     fused = G().gpu_run(dom, ids, src_slot=True, fused=True)
     assert not fused["workspace"].any()  # left zero for the next call
+    assert int(fused["dev_status"][0]) == (1 if bad else 0)  # EP_DEV_BAD_ID only
     G().compare(R, E, S, fused, G().oracle_run(R, E, S, ids), check_rows=False)
     sep = G().gpu_run(dom, ids, src_slot=True, fused=False)
     for key in ("counts", "counts_src", "quota", "slot_expert", "rank_load", "inst_ptr",

@@ -152,6 +152,9 @@ CASES = [
     ("quad_one_expert",    8,  4, 2, 4,  5000,  40,     8,   "one"),
     # the quad kernel with many slots per rank and with E in (256, 512]
     ("quad_long_ranks",    8,  4, 1, 8,  20000, 37,     8,   "bad"),
+    # one-layer launches with a rank split over a cluster of 4 or 2 blocks
+    ("cluster4_ragged",    8,  4, 1, 8,  30001, 1,      8,   "bad"),
+    ("cluster2_ragged",    16, 4, 2, 4,  50001, 1,      8,   "zipf"),
     ("quad_E320",          16, 20, 2, 8, 3000,  19,     8,   "bad"),
 ]
 
