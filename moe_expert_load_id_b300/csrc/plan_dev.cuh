@@ -1,6 +1,6 @@
-// Device code of the planner's flag-free rule: the count checks, the
-// shared-memory table move loop and the logical->physical CSR epilogue (the
-// last also serves the register loop of the rule variants in plan.cu).
+// Device code of the planner: the count checks, the shared-memory table move
+// loops of the flag-free rule and of the rule variants, and the
+// logical->physical CSR epilogue.
 //
 // UltraEP article (m.youleyou.com), "key design" section, control-plane
 // paragraph: the solver fixes the load (quota) every expert instance receives;
@@ -22,12 +22,13 @@ constexpr long long kQPackLimit = 1ll << 21; // ... and quotas fit a 10-bit-shif
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
 // One warp's shared memory: q[P], slot[R*S], holder[E] (the table), the CSR
-// epilogue's scratch pos[E+1] and val[E+R*S], and the instance's counts[E]
-// when the planner sums them itself.
+// epilogue's scratch pos[E+1] and val[E+R*S], a copy of the loads Ls[64] (the
+// rule variants), and the instance's counts[E] when the planner sums them
+// itself (last).
 __host__ __device__ inline size_t plan_warp_bytes(int R, int E, int S) {
     const int P = R * (E / R + S);
     return align16((size_t)P * 4) + align16((size_t)R * S * 4) + align16((size_t)E * 8) +
-           align16((size_t)(E + 1) * 4) + align16((size_t)(E + R * S) * 4) +
+           align16((size_t)(E + 1) * 4) + align16((size_t)(E + R * S) * 4) + 64 * 4 +
            align16((size_t)E * 4);
 }
 
@@ -56,8 +57,8 @@ __device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB
 // rank's largest instance is one warp reduction over its W instances (lane j:
 // instance j), eligibility is one 64-bit mask (holders of e | ranks with a
 // free slot), and the bookkeeping is a few single-lane stores, so nothing in a
-// move grows with the instances per rank.  Same rule, same ties, same outputs
-// as plan_moves with no flags; the tables are exactly the epilogue's.
+// move grows with the instances per rank.  The tables are exactly the
+// epilogue's.
 //
 // Every quota and spare-slot entry of the table is read and written by one
 // lane only: lane j owns local instance j of every rank (q[r*W + j] and, for
@@ -170,6 +171,183 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
     }
 }
 
+// The rule variants of ep_plan_ex on the same shared-memory table.
+//   EP_PLAN_SKIP: the move is the first (rank, instance) candidate that can
+//   move, in the order ranks by load (highest first, lowest index on ties),
+//   then a rank's instances with quota >= 1 by quota (largest first, lowest
+//   expert on ties).  A candidate (c, e) can move exactly when some eligible
+//   rank d != c (holding e, or with a free slot) has L[d] <= L[c] - 2: the
+//   coldest eligible rank then gives q >= 1.  So every lane evaluates its own
+//   ranks at once: the mask of ranks at least 2 below its rank's load (from a
+//   shared-memory copy of the loads), then each of the rank's instances
+//   against (holders of e | ranks with a free slot); one reduction over the
+//   ranks that have a movable instance picks the candidate.  A move costs the
+//   same however many candidates cannot move.
+//   EP_PLAN_RELEASE: a spare-slot instance a move leaves at quota 0 frees its
+//   slot (its rank no longer holds the expert; the slot is free again).
+// Without EP_PLAN_SKIP the candidate is the base rule's (the hottest rank's
+// largest instance with quota >= 1) and the plan stops when it cannot move.
+// Ls[64] is scratch for the loads; ranks >= R hold INT_MAX.
+template <bool kTwo, bool kPacked>
+__device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot,
+                                                       uint64_t* holder, int32_t* Ls,
+                                                       int& loadA, int& loadB, int lane, int H,
+                                                       int S, int W, int R, int max_iters,
+                                                       int flags, int& iters, int& status) {
+    const bool skip = (flags & EP_PLAN_SKIP) != 0;
+    const bool release = (flags & EP_PLAN_RELEASE) != 0;
+    const bool hasA = loadA >= 0, hasB = kTwo && loadB >= 0;
+    const int ra = lane, rb = lane + 32;
+    const uint64_t exist = (R >= 64) ? ~0ull : ((1ull << R) - 1ull);
+    uint64_t freem = S > 0 ? exist : 0ull;  // ranks with a free spare slot (warp-uniform)
+    Ls[ra] = hasA ? loadA : INT_MAX;
+    Ls[rb] = hasB ? loadB : INT_MAX;
+    __syncwarp();
+    // the best instance (largest quota >= 1, lowest expert) of rank r whose
+    // expert has an eligible rank in `low`; bq = -1 when there is none
+    auto best_movable = [&](int r, bool has, uint64_t low, int& bq, int& be, int& bj) {
+        bq = -1;
+        be = INT_MAX;
+        bj = 0;
+        if (!has) return;
+        for (int j = 0; j < W; ++j) {
+            const int ex = j < H ? r * H + j : slot[r * S + (j - H)];
+            if (ex < 0) continue;
+            const int qq = q[r * W + j];
+            if (qq < 1 || (qq < bq) || (qq == bq && ex > be)) continue;
+            if (((holder[ex] | freem) & exist & low) == 0ull) continue;
+            bq = qq;
+            be = ex;
+            bj = j;
+        }
+    };
+    while (true) {
+        int c, Lc, e, qsrc, src_j;  // the candidate (warp-uniform)
+        if (skip) {
+            // ranks at least 2 below my ranks' loads (a rank is never below itself)
+            unsigned loA = 0u, hiA = 0u, loB = 0u, hiB = 0u;
+            const int tA = loadA - 2, tB = loadB - 2;
+#pragma unroll 4
+            for (int d = 0; d < 32; d += 4) {
+                const int4 v = *reinterpret_cast<const int4*>(Ls + d);
+                const int4 w = *reinterpret_cast<const int4*>(Ls + 32 + d);
+                loA |= ((unsigned)(v.x <= tA) | (unsigned)(v.y <= tA) << 1 |
+                        (unsigned)(v.z <= tA) << 2 | (unsigned)(v.w <= tA) << 3) << d;
+                hiA |= ((unsigned)(w.x <= tA) | (unsigned)(w.y <= tA) << 1 |
+                        (unsigned)(w.z <= tA) << 2 | (unsigned)(w.w <= tA) << 3) << d;
+                if (kTwo) {
+                    loB |= ((unsigned)(v.x <= tB) | (unsigned)(v.y <= tB) << 1 |
+                            (unsigned)(v.z <= tB) << 2 | (unsigned)(v.w <= tB) << 3) << d;
+                    hiB |= ((unsigned)(w.x <= tB) | (unsigned)(w.y <= tB) << 1 |
+                            (unsigned)(w.z <= tB) << 2 | (unsigned)(w.w <= tB) << 3) << d;
+                }
+            }
+            int bqA, beA, bjA, bqB = -1, beB = INT_MAX, bjB = 0;
+            best_movable(ra, hasA, ((uint64_t)hiA << 32) | loA, bqA, beA, bjA);
+            if (kTwo) best_movable(rb, hasB, ((uint64_t)hiB << 32) | loB, bqB, beB, bjB);
+            // the first rank in (load desc, index asc) order with a movable instance
+            const bool mA = bqA >= 1, mB = kTwo && bqB >= 1;
+            if (kPacked) {
+                const unsigned ka = mA ? ((unsigned)loadA << 6) | (unsigned)(63 - ra) : 0u;
+                const unsigned kb = mB ? ((unsigned)loadB << 6) | (unsigned)(31 - lane) : 0u;
+                const unsigned k = __reduce_max_sync(kFull, kTwo ? max(ka, kb) : ka);
+                if (k == 0u) break;  // no candidate can move
+                c = 63 - (int)(k & 63u);
+                Lc = (int)(k >> 6);
+            } else {
+                const int la = mA ? loadA : -1, lb = mB ? loadB : -1;
+                Lc = __reduce_max_sync(kFull, kTwo ? max(la, lb) : la);
+                if (Lc < 0) break;
+                const unsigned b0 = __ballot_sync(kFull, mA && la == Lc);
+                const unsigned b1 = kTwo ? __ballot_sync(kFull, mB && lb == Lc) : 0u;
+                c = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+            }
+            const bool cB = c >= 32;
+            const int cl = c & 31;
+            qsrc = __shfl_sync(kFull, cB ? bqB : bqA, cl);
+            e = __shfl_sync(kFull, cB ? beB : beA, cl);
+            src_j = __shfl_sync(kFull, cB ? bjB : bjA, cl);
+        } else {
+            // the base candidate: the hottest rank's largest instance with quota >= 1
+            argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, c, Lc);
+            int qj = -1;
+            unsigned cxj = 0xffffffffu;
+            if (lane < W) {
+                const int xj = lane < H ? c * H + lane : slot[c * S + (lane - H)];
+                const int qv = q[c * W + lane];
+                if (xj >= 0 && qv >= 1) {
+                    qj = qv;
+                    cxj = ((unsigned)xj << 5) | (unsigned)lane;
+                }
+            }
+            qsrc = __reduce_max_sync(kFull, qj);
+            if (qsrc < 1) break;
+            const unsigned cx = __reduce_min_sync(kFull, qj == qsrc ? cxj : 0xffffffffu);
+            e = (int)(cx >> 5);
+            src_j = (int)(cx & 31u);
+        }
+        // the coldest eligible rank (lowest index on ties) and the amount
+        const uint64_t hm = holder[e];
+        const uint64_t el = (hm | freem) & exist & ~(1ull << c);
+        if (el == 0ull) break;  // (base candidate only)
+        const bool elA = hasA && ((el >> ra) & 1ull);
+        const bool elB = hasB && ((el >> rb) & 1ull);
+        int cold, Lmin;
+        if (kPacked) {
+            const unsigned ca = elA ? ((unsigned)loadA << 6) | (unsigned)ra : 0xffffffffu;
+            const unsigned cb = elB ? ((unsigned)loadB << 6) | (unsigned)rb : 0xffffffffu;
+            const unsigned kk = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            cold = (int)(kk & 63u);
+            Lmin = (int)(kk >> 6);
+        } else {
+            const int ca = elA ? loadA : INT_MAX;
+            const int cb = elB ? loadB : INT_MAX;
+            Lmin = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            const unsigned b0 = __ballot_sync(kFull, elA && ca == Lmin);
+            const unsigned b1 = kTwo ? __ballot_sync(kFull, elB && cb == Lmin) : 0u;
+            cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+        }
+        const int mv = min(qsrc, (Lc - Lmin) >> 1);
+        if (mv <= 0) break;  // (base candidate only: a skip candidate always moves)
+        if (iters == max_iters) {
+            status = EP_ERR_ITER_LIMIT;
+            break;
+        }
+        // the move: loads, then cold's instance of e (its home, a spare slot
+        // holding e, or its lowest free slot, filled now)
+        loadA += (ra == cold ? mv : 0) - (ra == c ? mv : 0);
+        if (kTwo) loadB += (rb == cold ? mv : 0) - (rb == c ? mv : 0);
+        const int sv = (lane < S) ? slot[cold * S + lane] : 0;
+        const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
+        const unsigned freeb = __ballot_sync(kFull, lane < S && sv < 0);  // cold's free slots
+        const bool held = (hm >> cold) & 1ull;
+        const int ej = e - cold * H;
+        const bool home = (unsigned)ej < (unsigned)H;
+        const unsigned pick = held ? hit : freeb;
+        if (!home && pick == 0u) {  // (never; keeps every index in range)
+            status = EP_ERR_INVAL;
+            break;
+        }
+        const int dj = home ? ej : H + __ffs(pick) - 1;
+        const bool freed = release && src_j >= H && qsrc == mv;  // the source replica emptied
+        if (lane == 0) {
+            q[c * W + src_j] -= mv;
+            q[cold * W + dj] += mv;
+            if (!held) slot[cold * S + (dj - H)] = e;
+            if (freed) slot[c * S + (src_j - H)] = -1;
+            uint64_t h2 = held ? hm : (hm | (1ull << cold));
+            if (freed) h2 &= ~(1ull << c);
+            holder[e] = h2;
+            Ls[c] = Lc - mv;
+            Ls[cold] = Lmin + mv;
+        }
+        if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
+        if (freed) freem |= 1ull << c;
+        __syncwarp();  // the table and the load copy, for every lane's next reads
+        ++iters;
+    }
+}
+
 // Counts must be >= 0 with a total below 2^31; otherwise the instance is
 // rejected (EP_ERR_INVAL).  tot: the warp-uniform total.
 __device__ __forceinline__ int plan_check_counts(const int32_t* cnt, int E, int lane,
@@ -186,16 +364,16 @@ __device__ __forceinline__ int plan_check_counts(const int32_t* cnt, int E, int 
     return (bad || tot > (long long)INT_MAX) ? EP_ERR_INVAL : EP_OK;
 }
 
-// The flag-free rule for one instance on the shared-memory tables q[P],
-// slot[R*S], holder[E] (plan_warp_bytes): the home placement from cnt, the
-// move loop (only while status is EP_OK), then quota, spare slots and loads to
-// qo / so / lo.  One warp; kTwo: R > 32.
-template <bool kTwo>
+// One instance on the shared-memory tables q[P], slot[R*S], holder[E]
+// (plan_warp_bytes): the home placement from cnt, the move loop of the rule
+// (kFlags: the variants of `flags`; only while status is EP_OK), then quota,
+// spare slots and loads to qo / so / lo.  One warp; kTwo: R > 32.
+template <bool kTwo, bool kFlags>
 __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int E, int S,
-                                                 int max_iters, long long tot, int32_t* q,
-                                                 int32_t* slot, uint64_t* holder, int lane,
-                                                 int32_t* qo, int32_t* so, int32_t* lo,
-                                                 int& iters, int& status) {
+                                                 int max_iters, int flags, long long tot,
+                                                 int32_t* q, int32_t* slot, uint64_t* holder,
+                                                 int32_t* Ls, int lane, int32_t* qo, int32_t* so,
+                                                 int32_t* lo, int& iters, int& status) {
     const int H = E / R, W = H + S, P = R * W;
     for (int p = lane; p < P; p += 32) {
         const int r = p / W, j = p - r * W;
@@ -215,7 +393,16 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
         loadB = (int)sum;
     }
     __syncwarp();
-    if (status == EP_OK) {
+    if (kFlags) {
+        if (status == EP_OK) {
+            if (tot < kPackLimit)
+                plan_moves_table_flags<kTwo, true>(q, slot, holder, Ls, loadA, loadB, lane, H, S,
+                                                   W, R, max_iters, flags, iters, status);
+            else
+                plan_moves_table_flags<kTwo, false>(q, slot, holder, Ls, loadA, loadB, lane, H, S,
+                                                    W, R, max_iters, flags, iters, status);
+        }
+    } else if (status == EP_OK) {
         if (tot < kQPackLimit)
             plan_moves_table<kTwo, true, true>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
                                                max_iters, iters, status);

@@ -644,7 +644,9 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 // A slot's row is hot[e].row + (lanes below in its group).  Only a group that
 // runs past its instance (a replica boundary, or the expert's quotas used up)
 // takes the slow path: its slots search the expert's instance list and the
-// leader moves both entries on.  The rows start at the prefix of counts_src
+// leader moves both entries on.  The top bit of hot[e].row marks the experts
+// whose ranks in this warp (by counts_src) reach a boundary at all; only their
+// leaders read cold[e] (rows are below 2^31, so the bit is free).  The rows start at the prefix of counts_src
 // over earlier source ranks (mapped through the plan), so no scan over warps
 // or chunks is needed; at the end the rank a warp reached must be that
 // prefix plus its own counts_src row, one compare per expert.
@@ -657,6 +659,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 constexpr int kQuadWarps = 8;
 constexpr int kQuadThreads = kQuadWarps * 32;
 constexpr int kQuadAhead = 3;  // steps of ids loaded ahead of the one being ranked
+constexpr unsigned kCross = 0x80000000u;  // hot[e].y: e's ranks here may cross a boundary
 #ifndef EP_REROUTE_QUAD_MIN_RANKS
 #define EP_REROUTE_QUAD_MIN_RANKS 296  // (instance, source rank) units from which the
                                         // quad kernel is used (build-time tunable)
@@ -776,7 +779,11 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
                 const int end = ptr[e + 1];
                 const int m = upper_bound(bcum, ptr[e], end, x);
                 const int del = (m < end) ? bdel[m] : 0;  // quotas used up: every rank overflows
-                hot[e] = make_uint2(0u, (unsigned)(x + del));
+                // the warp's ranks of e, by counts_src, all inside this
+                // instance: the leaders of e never look at cold[e]
+                const int own = mypre[E + e] - x;
+                const bool may_cross = m >= end || x + own > bcum[m];
+                hot[e] = make_uint2(0u, (unsigned)(x + del) | (may_cross ? kCross : 0u));
                 cold[e] = make_int2((m < end) ? bcum[m] + del : x, del);
             } else {
                 hot[e] = make_uint2(0u, 0u);
@@ -801,7 +808,7 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
             const int end = ptr[e + 1];
             const int m = upper_bound(bcum, ptr[e], end, x);
             const int nd = (m < end) ? bdel[m] : 0;
-            hot[e].y = (unsigned)(x + nd);
+            hot[e].y = (unsigned)(x + nd) | kCross;
             cold[e] = make_int2((m < end) ? bcum[m] + nd : x, nd);
         };
         // a step whose lanes hold a repeated id: four sub-steps of 32
@@ -821,11 +828,11 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
                 const uint2 h = hot[e];
                 const int2 cd = cold[e];
                 const unsigned below = h.x & lt;
-                int row = (int)h.y + __popc(below);
-                const int nr = (int)h.y + __popc(h.x);
+                int row = (int)(h.y & ~kCross) + __popc(below);
+                const int nr = (int)(h.y & ~kCross) + __popc(h.x);
                 const bool lead = below == 0u;
                 __syncwarp();
-                if (lead) hot[e] = make_uint2(0u, (unsigned)nr);
+                if (lead) hot[e] = make_uint2(0u, (unsigned)nr | (h.y & kCross));
                 if (v && row >= cd.x) row = search(e, row - cd.y);
                 __syncwarp();
                 if (lead && v && nr >= cd.x) advance(e, nr, cd.y);
@@ -867,18 +874,22 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
             __syncwarp();
             const uint2 h0 = hot[e0], h1 = hot[e1], h2 = hot[e2], h3 = hot[e3];
             const unsigned b0 = h0.x & lt, b1 = h1.x & lt, b2 = h2.x & lt, b3 = h3.x & lt;
-            int4 rows = make_int4((int)h0.y + __popc(b0), (int)h1.y + __popc(b1),
-                                  (int)h2.y + __popc(b2), (int)h3.y + __popc(b3));
-            const int n0 = (int)h0.y + __popc(h0.x), n1 = (int)h1.y + __popc(h1.x);
-            const int n2 = (int)h2.y + __popc(h2.x), n3 = (int)h3.y + __popc(h3.x);
+            const int y0 = (int)(h0.y & ~kCross), y1 = (int)(h1.y & ~kCross);
+            const int y2 = (int)(h2.y & ~kCross), y3 = (int)(h3.y & ~kCross);
+            int4 rows = make_int4(y0 + __popc(b0), y1 + __popc(b1), y2 + __popc(b2), y3 + __popc(b3));
+            const int n0 = y0 + __popc(h0.x), n1 = y1 + __popc(h1.x);
+            const int n2 = y2 + __popc(h2.x), n3 = y3 + __popc(h3.x);
             __syncwarp();
-            if (b0 == 0u) hot[e0] = make_uint2(0u, (unsigned)n0);
-            if (b1 == 0u) hot[e1] = make_uint2(0u, (unsigned)n1);
-            if (b2 == 0u) hot[e2] = make_uint2(0u, (unsigned)n2);
-            if (b3 == 0u) hot[e3] = make_uint2(0u, (unsigned)n3);
-            // a group reaching the end of its instance: the leader sees it
-            const bool x0 = b0 == 0u && n0 >= cold[e0].x, x1 = b1 == 0u && n1 >= cold[e1].x;
-            const bool x2 = b2 == 0u && n2 >= cold[e2].x, x3 = b3 == 0u && n3 >= cold[e3].x;
+            if (b0 == 0u) hot[e0] = make_uint2(0u, (unsigned)n0 | (h0.y & kCross));
+            if (b1 == 0u) hot[e1] = make_uint2(0u, (unsigned)n1 | (h1.y & kCross));
+            if (b2 == 0u) hot[e2] = make_uint2(0u, (unsigned)n2 | (h2.y & kCross));
+            if (b3 == 0u) hot[e3] = make_uint2(0u, (unsigned)n3 | (h3.y & kCross));
+            // a group reaching the end of its instance: its leader sees it
+            // (only experts whose ranks here may cross a boundary are checked)
+            const bool x0 = b0 == 0u && (h0.y & kCross) && n0 >= cold[e0].x;
+            const bool x1 = b1 == 0u && (h1.y & kCross) && n1 >= cold[e1].x;
+            const bool x2 = b2 == 0u && (h2.y & kCross) && n2 >= cold[e2].x;
+            const bool x3 = b3 == 0u && (h3.y & kCross) && n3 >= cold[e3].x;
             if (__any_sync(kFull, x0 || x1 || x2 || x3)) {
                 // every slot past its entry's end searches; then the leaders
                 // move their entries on
@@ -922,7 +933,7 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
         // including this one
         const int32_t* want = pre + (warp + 1) * E;
         for (int e = lane; e < E; e += 32)
-            if ((int)hot[e].y - cold[e].y != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
+            if ((int)(hot[e].y & ~kCross) - cold[e].y != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
     }
     if (my_flags) atomicOr(&flags, my_flags);
     __syncthreads();
@@ -1030,15 +1041,22 @@ cudaError_t launch_reroute(const ep_domain_t& d, const int32_t* ids, int64_t T, 
     constexpr int kPart = 1024 * 8;
     const bool parts_fit =
         rr_layout(d.R, d.E, d.S, 1024 / 32, ev_in_smem<1024>(), 8).bytes + 1024 <= di.smem_optin;
+    // (1024-thread blocks hold an SM each: a cluster launch is used only when
+    // all its blocks fit on the GPU at once)
     if (parts_fit && EP_REROUTE_CLUSTER_PARTS) {
-        if (rank_slots > 2 * kPart && rank_slots <= 4 * kPart)
+        if (rank_slots > 2 * kPart && rank_slots <= 4 * kPart && blocks * 4 <= sms)
             return launch_reroute_t<1024, 8, 4>(d, ids, T, n_inst, counts_src, quota, inst_ptr,
                                                 inst_id, inst_cum, dst_row, src_slot,
                                                 inst_offset, dev_status, s, pdl);
-        if (rank_slots > kPart && rank_slots <= 2 * kPart)
+        if (rank_slots > kPart && rank_slots <= 2 * kPart && blocks * 2 <= sms)
             return launch_reroute_t<1024, 8, 2>(d, ids, T, n_inst, counts_src, quota, inst_ptr,
                                                 inst_id, inst_cum, dst_row, src_slot,
                                                 inst_offset, dev_status, s, pdl);
+        if (rank_slots > 2 * kPart && rank_slots <= 4 * kPart && blocks * 2 <= sms &&
+            rr_layout(d.R, d.E, d.S, 1024 / 32, ev_in_smem<1024>(), 16).bytes + 1024 <= di.smem_optin)
+            return launch_reroute_t<1024, 16, 2>(d, ids, T, n_inst, counts_src, quota, inst_ptr,
+                                                 inst_id, inst_cum, dst_row, src_slot,
+                                                 inst_offset, dev_status, s, pdl);
     }
     return launch_reroute_t<1024>(d, ids, T, n_inst, counts_src, quota, inst_ptr, inst_id,
                                    inst_cum, dst_row, src_slot, inst_offset, dev_status, s,
