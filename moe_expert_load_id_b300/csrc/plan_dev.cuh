@@ -209,7 +209,7 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
         bq = -1;
         be = INT_MAX;
         bj = 0;
-        if (!has) return;
+        if (!has || low == 0ull) return;
         for (int j = 0; j < W; ++j) {
             const int ex = j < H ? r * H + j : slot[r * S + (j - H)];
             if (ex < 0) continue;
