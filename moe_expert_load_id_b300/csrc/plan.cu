@@ -42,6 +42,7 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
             int32_t* __restrict__ iter_out, int32_t* __restrict__ status_out,
             const int32_t* __restrict__ counts_src, int32_t* __restrict__ counts_out) {
     extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ int csr_warp_tot[kPlanWarps];
     // in ep_balance this grid is a programmatic dependent of ep_count: wait for
     // its counts, then let the dependent reroute start its plan-independent
     // work (for a plain launch both are no-ops)
@@ -91,39 +92,53 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
             cnt = mine;
         }
     }
-    if (g >= n_inst) return;  // whole warp; no block-wide barrier follows
-
-    // counts must be >= 0 with a total below 2^31; otherwise the instance is
-    // rejected (EP_ERR_INVAL) and its outputs describe the home-only placement
-    long long tot = 0;
-    int status = plan_check_counts(cnt, E, lane, tot);
-
-    unsigned char* base = smem + (size_t)warp * wbytes;
-    int32_t* q = reinterpret_cast<int32_t*>(base);
-    int32_t* slot = reinterpret_cast<int32_t*>(base + align16((size_t)P * 4));
-    uint64_t* holder = reinterpret_cast<uint64_t*>(base + align16((size_t)P * 4) +
-                                                   align16((size_t)R * S * 4));
-    int32_t* csr_pos = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(holder) +
-                                                  align16((size_t)E * 8));
-    int32_t* csr_val = csr_pos + align16((size_t)(E + 1) * 4) / 4;
-    int32_t* qo = quota_out + (int64_t)g * P;
-    int32_t* so = slot_out + (int64_t)g * R * S;
-    int32_t* lo = load_out + (int64_t)g * R;
-    int iters = 0;
-    int32_t* Ls = csr_val + align16((size_t)(E + R * S) * 4) / 4;  // [64] loads (variants)
-    plan_table_solve<kTwo, kFlags>(cnt, R, E, S, max_iters, flags, tot, q, slot, holder, Ls,
-                                   lane, qo, so, lo, iters, status);
-    __syncwarp();
-
-    // logical -> physical CSR: home first, then replicas by ascending rank (= ascending p)
-    plan_csr(q, slot, holder, R, E, S, lane, csr_pos, csr_val, ptr_out + (int64_t)g * (E + 1),
-             id_out + (int64_t)g * (E + R * S), cum_out + (int64_t)g * (E + R * S));
-    if (lane == 0) {
-        iter_out[g] = iters;
-        status_out[g] = status;
+    // each warp solves its instance (idle warps of the block skip to the barrier)
+    const int g0 = blockIdx.x * kPlanWarps;
+    const int nb = min(kPlanWarps, n_inst - g0);  // instances of this block
+    auto tables = [&](int w, int32_t*& q, int32_t*& slot, uint64_t*& holder, int32_t*& pos,
+                      int32_t*& val, int32_t*& Ls) {
+        unsigned char* base = smem + (size_t)w * wbytes;
+        q = reinterpret_cast<int32_t*>(base);
+        slot = reinterpret_cast<int32_t*>(base + align16((size_t)P * 4));
+        holder = reinterpret_cast<uint64_t*>(base + align16((size_t)P * 4) +
+                                             align16((size_t)R * S * 4));
+        pos = reinterpret_cast<int32_t*>(reinterpret_cast<unsigned char*>(holder) +
+                                         align16((size_t)E * 8));
+        val = pos + align16((size_t)(E + 1) * 4) / 4;
+        Ls = val + align16((size_t)(E + R * S) * 4) / 4;  // [64] loads (variants)
+    };
+    if (g < n_inst) {
+        // counts must be >= 0 with a total below 2^31; otherwise the instance is
+        // rejected (EP_ERR_INVAL) and its outputs describe the home-only placement
+        long long tot = 0;
+        int status = plan_check_counts(cnt, E, lane, tot);
+        int32_t *q, *slot, *pos, *val, *Ls;
+        uint64_t* holder;
+        tables(warp, q, slot, holder, pos, val, Ls);
+        int iters = 0;
+        plan_table_solve<kTwo, kFlags>(cnt, R, E, S, max_iters, flags, tot, q, slot, holder, Ls,
+                                       lane, quota_out + (int64_t)g * P,
+                                       slot_out + (int64_t)g * R * S, load_out + (int64_t)g * R,
+                                       iters, status);
+        if (lane == 0) {
+            iter_out[g] = iters;
+            status_out[g] = status;
+        }
+    }
+    __syncthreads();
+    // logical -> physical CSR of every instance of the block, by the whole block
+    // (home first, then replicas by ascending rank = ascending p)
+    for (int wi = 0; wi < nb; ++wi) {
+        int32_t *q, *slot, *pos, *val, *Ls;
+        uint64_t* holder;
+        tables(wi, q, slot, holder, pos, val, Ls);
+        const int gi = g0 + wi;
+        plan_csr_block<kPlanWarps * 32>(q, slot, holder, R, E, S, pos, val, csr_warp_tot,
+                                        ptr_out + (int64_t)gi * (E + 1),
+                                        id_out + (int64_t)gi * (E + R * S),
+                                        cum_out + (int64_t)gi * (E + R * S));
     }
 }
-
 template <bool kTwo, bool kFlags>
 cudaError_t launch_plan_k(const ep_domain_t& d, const int32_t* counts, int32_t n_inst,
                           int32_t max_iters, int32_t flags, int32_t* quota, int32_t* slot_expert,

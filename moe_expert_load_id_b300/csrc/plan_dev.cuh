@@ -422,56 +422,70 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
 
 // Logical -> physical CSR from the tables: for each expert its home instance
 // first, then its replicas by ascending rank (= ascending p), with inclusive
-// cumulative quotas.  One warp; writes po[0..E], io and co.  The list offsets
-// are one warp scan over the holder counts; every spare slot then finds its
-// own place in its expert's list (1 + its expert's replicas on lower ranks),
-// and each expert's running sums are one short walk over its list.  pos[E+1]
-// and val[E+R*S] are shared-memory scratch (the offsets and each entry's
-// quota).
-__device__ __forceinline__ void plan_csr(const int32_t* q, const int32_t* slot,
-                                         const uint64_t* holder, int R, int E, int S, int lane,
-                                         int32_t* pos, int32_t* val, int32_t* po, int32_t* io,
-                                         int32_t* co) {
+// cumulative quotas.  The whole block (kThreads threads) builds one instance's
+// lists: a block scan over the holder counts gives the list offsets (writes
+// po[0..E] and the home entries); every spare slot then finds its own place
+// in its expert's list (1 + its expert's replicas on lower ranks); each
+// expert's running sums are a short walk over its list.  pos[E+1] and
+// val[E+R*S] are shared-memory scratch (the offsets and each entry's quota),
+// wtot[kThreads/32] the scan's warp totals.  Called by every thread of the
+// block; starts and ends with a block barrier's worth of ordering.
+template <int kThreads>
+__device__ __forceinline__ void plan_csr_block(const int32_t* q, const int32_t* slot,
+                                               const uint64_t* holder, int R, int E, int S,
+                                               int32_t* pos, int32_t* val, int* wtot,
+                                               int32_t* po, int32_t* io, int32_t* co) {
+    constexpr int kWarps = kThreads / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = E / R, W = H + S;
-    int run = 0;
-    for (int e0 = 0; e0 < E; e0 += 32) {
-        const int e = e0 + lane;
-        const int n = (e < E) ? __popcll(holder[e]) : 0;
-        int x = n;
+    // thread t: experts [t*per, (t+1)*per)
+    const int per = (E + kThreads - 1) / kThreads;
+    const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
+    int n = 0;
+    for (int e = e0; e < e1; ++e) n += __popcll(holder[e]);
+    int x = n;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int y = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += y;
-        }
-        if (e < E) {
-            const int m = run + x - n;
-            pos[e] = m;
-            po[e] = m;
-            const int home = e / H;
-            const int hp = home * W + (e - home * H);  // the home instance heads the list
-            io[m] = hp;
-            val[m] = q[hp];
-        }
-        run += __shfl_sync(kFull, x, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
     }
-    if (lane == 0) {
-        po[E] = run;
-        pos[E] = run;
+    if (lane == 31) wtot[warp] = x;
+    __syncthreads();
+    int below = 0, total = 0;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+        const int t = wtot[w];
+        below += (w < warp) ? t : 0;
+        total += t;
     }
-    __syncwarp();
+    int run = below + x - n;
+    for (int e = e0; e < e1; ++e) {
+        pos[e] = run;
+        po[e] = run;
+        const int home = e / H;
+        const int hp = home * W + (e - home * H);  // the home instance heads the list
+        io[run] = hp;
+        val[run] = q[hp];
+        run += __popcll(holder[e]);
+    }
+    if (tid == 0) {
+        pos[E] = total;
+        po[E] = total;
+    }
+    __syncthreads();
     // replicas: slot (c, s) of expert e sits after e's home and e's replicas on ranks below c
-    for (int x = lane; x < R * S; x += 32) {
-        const int e = slot[x];
+    for (int xs = tid; xs < R * S; xs += kThreads) {
+        const int e = slot[xs];
         if (e < 0) continue;
-        const int c = x / S, s = x - c * S;
+        const int c = xs / S, sl = xs - c * S;
         const uint64_t lower = holder[e] & ~(1ull << (e / H)) & ((1ull << c) - 1ull);
         const int m = pos[e] + 1 + __popcll(lower);
-        const int p = c * W + H + s;
+        const int p = c * W + H + sl;
         io[m] = p;
         val[m] = q[p];
     }
-    __syncwarp();
-    for (int e = lane; e < E; e += 32) {
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
         const int m1 = pos[e + 1];
         int cum = 0;
         for (int m = pos[e]; m < m1; ++m) {
@@ -479,6 +493,7 @@ __device__ __forceinline__ void plan_csr(const int32_t* q, const int32_t* slot,
             co[m] = cum;
         }
     }
+    __syncthreads();  // the scratch may be reused by the next call
 }
 
 }  // namespace ultraep
