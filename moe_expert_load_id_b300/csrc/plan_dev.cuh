@@ -108,10 +108,11 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         }
 
         // 3-5. eligible ranks: the others that hold e or have a free slot;
-        // the coldest of them (lowest rank on ties) and the amount
+        // the coldest of them (lowest rank on ties) and the amount.  No
+        // eligible rank leaves the reduction at its identity (an amount <= 0);
+        // the stop conditions and the cap are tested with one branch.
         const uint64_t hm = holder[e];
         const uint64_t el = (hm | freem) & exist & ~(1ull << hot);
-        if (el == 0ull) break;  // no rank is eligible
         const bool elA = hasA && ((el >> ra) & 1ull);
         const bool elB = hasB && ((el >> rb) & 1ull);
         int cold, Lmin;
@@ -130,10 +131,10 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
             cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
         }
         const int mv = min(qmax, (Lmax - Lmin) >> 1);
-        if (mv <= 0) break;  // the global stop
-        // 6. safety cap
-        if (iters == max_iters) {
-            status = EP_ERR_ITER_LIMIT;
+        // 6. stop: no rank eligible, or nothing to move (the global stop);
+        // else the safety cap
+        if (el == 0ull || mv <= 0 || iters == max_iters) {
+            if (el != 0ull && mv > 0) status = EP_ERR_ITER_LIMIT;
             break;
         }
         // 7. move.  Loads first, then the next move's argmax ...
