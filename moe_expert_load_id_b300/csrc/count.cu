@@ -11,9 +11,10 @@
 // is not used.  ids are read with 16-byte streaming loads (scalar head and
 // tail).
 //
-// The chunks of one source rank form a thread-block cluster: after a cluster
-// barrier the cluster's first block sums the others' block totals through
-// distributed shared memory and writes counts_src[r].  Source ranks of one
+// The chunks of one source rank form a thread-block cluster: every block adds
+// its totals into the first block's accumulator through distributed shared
+// memory (atomics that need no reply), and after one cluster barrier the
+// first block writes counts_src[r].  Source ranks of one
 // instance meet in a last-block reduction (atomic ticket) that writes counts;
 // its ticket lives in the caller's workspace and is reset by that block, so
 // it is zero again after every call.
@@ -36,8 +37,13 @@ namespace cg = cooperative_groups;
 #define EP_COUNT_VEC 2
 #endif
 constexpr int kCountThreads = EP_COUNT_THREADS;
-constexpr int kCountWarps = kCountThreads / 32;
 constexpr int kVec = EP_COUNT_VEC;
+// A launch whose blocks all fit on the GPU at once (one layer) is bound by
+// load latency, not bandwidth: its blocks take four 16-byte loads per thread
+// in flight (one round trip for a 16384-slot source rank in five chunks), at
+// four blocks per SM.
+constexpr int kVecWave = 4;
+constexpr int kWaveBlocksPerSm = 4;
 #ifndef EP_COUNT_TARGET_BLOCKS
 #define EP_COUNT_TARGET_BLOCKS (2 * 148)        // blocks a launch aims at (build-time tunable)
 #endif
@@ -90,7 +96,8 @@ __device__ __forceinline__ void count_one(int v, int E, int32_t* hist, int C, in
     else bad = 1;
 }
 
-__global__ void __launch_bounds__(kCountThreads, 2048 / kCountThreads)
+template <int kV, int kMinBlocks>
+__global__ void __launch_bounds__(kCountThreads, kMinBlocks)
 count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, int cps,
              int32_t* __restrict__ counts, int32_t* __restrict__ counts_src,
              int32_t* dev_status, uint32_t* inst_ticket, int rows_only) {
@@ -99,7 +106,7 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     __shared__ int is_last;
     const int C = count_cols(E);
     int32_t* hist = sh;                                            // [E][C], later scratch
-    int32_t* blk = sh + (E * C > kCountThreads ? E * C : kCountThreads);  // [E] block total
+    int32_t* blk = sh + (E * C > kCountThreads ? E * C : kCountThreads);  // [E] rank total
 
     // A dependent planner (ep_balance) may launch now; it waits for this grid.
     pdl_trigger();
@@ -113,8 +120,13 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     const int r = rc / cps, c = rc - r * cps;  // c is also the block's rank in its cluster
 
     for (int x = tid; x < E * C; x += kCountThreads) hist[x] = 0;
+    for (int x = tid; x < E; x += kCountThreads) blk[x] = 0;
     if (tid == 0) bad = 0;
     __syncthreads();
+    // the first block's accumulator is zero before any block of the cluster
+    // adds to it: arrive now, wait just before the adds
+    cg::cluster_group cluster = cg::this_cluster();
+    if (cps > 1) cluster.barrier_arrive();
 
     // this block's slots: chunk c of source rank r (T < 2^31 since T*k < 2^31)
     const int Ti = (int)T;
@@ -137,15 +149,15 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     if (tid < head) count_one(__ldcs(p0 + tid), E, hist, C, col, local_bad);
     if (tid < n - tail0) count_one(__ldcs(p0 + tail0 + tid), E, hist, C, col, local_bad);
     // trip count is warp-uniform (v0 has no lane term)
-    for (int64_t v0 = (int64_t)warp * 32 * kVec; v0 < n4; v0 += (int64_t)kCountThreads * kVec) {
-        int4 w[kVec];
+    for (int64_t v0 = (int64_t)warp * 32 * kV; v0 < n4; v0 += (int64_t)kCountThreads * kV) {
+        int4 w[kV];
 #pragma unroll
-        for (int u = 0; u < kVec; ++u) {
+        for (int u = 0; u < kV; ++u) {
             const int64_t vi = v0 + u * 32 + lane;
             w[u] = (vi < n4) ? load_ids(body + vi) : make_int4(0, 0, 0, 0);
         }
 #pragma unroll
-        for (int u = 0; u < kVec; ++u) {
+        for (int u = 0; u < kV; ++u) {
             if (v0 + u * 32 + lane < n4) {
                 count_one(w[u].x, E, hist, C, col, local_bad);
                 count_one(w[u].y, E, hist, C, col, local_bad);
@@ -157,34 +169,35 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     if (local_bad) bad = 1;
     __syncthreads();
 
-    // block total: one warp per expert row, one redux over its C columns
-    for (int e = warp; e < E; e += kCountWarps) {
-        const int v = (lane < C) ? hist[e * C + lane] : 0;
-        const int t = __reduce_add_sync(kFull, v);
-        if (lane == 0) blk[e] = t;
+    // block total of expert e: thread e sums its C columns, starting at
+    // column e % C (the rotation keeps one warp's reads 2-way per bank at
+    // most), and adds it to the rank's total: the first block's accumulator,
+    // through distributed shared memory in a cluster
+    if (cps > 1) cluster.barrier_wait();
+    int32_t* acc = (cps > 1 && c != 0) ? cluster.map_shared_rank(blk, 0) : blk;
+    for (int e = tid; e < E; e += kCountThreads) {
+        const int32_t* row = hist + e * C;
+        int t = 0;
+        for (int j = 0; j < C; ++j) t += row[(j + e) & (C - 1)];
+        if (cps > 1) {
+            if (t != 0) atomicAdd(acc + e, t);
+        } else {
+            blk[e] = t;
+        }
     }
     if (tid == 0 && bad) raise_flag(dev_status, EP_DEV_BAD_ID);
 
+    // one barrier: every block's adds are done (the cluster barrier orders
+    // them before the first block's reads), then the first block writes the
+    // rank's row
     const int64_t rank_row = ((int64_t)inst * R + r) * E;
     if (cps > 1) {
-        // the cluster (the cps chunks of rank r) sums its block totals in
-        // distributed shared memory; the second barrier keeps every block's
-        // shared memory alive until the first block has read it
-        cg::cluster_group cluster = cg::this_cluster();
-        cluster.sync();
-        if (c == 0) {
-            for (int e = tid; e < E; e += kCountThreads) {
-                int t = 0;
-                for (int cc = 0; cc < cps; ++cc) t += cluster.map_shared_rank(blk, cc)[e];
-                counts_src[rank_row + e] = t;
-            }
-        }
         cluster.sync();
         if (c != 0) return;
     } else {
         __syncthreads();
-        for (int e = tid; e < E; e += kCountThreads) counts_src[rank_row + e] = blk[e];
     }
+    for (int e = tid; e < E; e += kCountThreads) counts_src[rank_row + e] = blk[e];
 
     // rows_only (ep_balance): the planner, which waits for this grid, sums the
     // rows itself, so the blocks stop here
@@ -280,8 +293,14 @@ cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, in
     const int cps = count_chunks_per_rank(d, T, n_inst);
     uint32_t* inst_ticket = static_cast<uint32_t*>(ws);
     const size_t smem = count_smem_bytes(d.E);
+    const int64_t blocks = (int64_t)n_inst * d.R * cps;
+    // one wave (every block resident at once) with more than one pass of
+    // kVec loads per thread: the latency-bound variant
+    const int64_t n4 = tokens_per_rank(T, d.R) * d.k / cps / 4;
+    const bool wave = blocks <= (int64_t)device_info().sms * kWaveBlocksPerSm &&
+                      n4 > (int64_t)kCountThreads * kVec;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)((int64_t)n_inst * d.R * cps));
+    cfg.gridDim = dim3((unsigned)blocks);
     cfg.blockDim = dim3(kCountThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
@@ -292,8 +311,13 @@ cudaError_t launch_count(const ep_domain_t& d, const int32_t* ids, int64_t T, in
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = cps > 1 ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, count_kernel, ids, T, (int)d.k, (int)d.R, (int)d.E, cps,
-                              counts, counts_src, dev_status, inst_ticket, rows_only ? 1 : 0);
+    if (wave)
+        return cudaLaunchKernelEx(&cfg, count_kernel<kVecWave, kWaveBlocksPerSm>, ids, T, (int)d.k,
+                                  (int)d.R, (int)d.E, cps, counts, counts_src, dev_status,
+                                  inst_ticket, rows_only ? 1 : 0);
+    return cudaLaunchKernelEx(&cfg, count_kernel<kVec, 2048 / kCountThreads>, ids, T, (int)d.k,
+                              (int)d.R, (int)d.E, cps, counts, counts_src, dev_status, inst_ticket,
+                              rows_only ? 1 : 0);
 }
 
 }  // namespace ultraep

@@ -65,25 +65,61 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
             csum0[w * (wbytes / 4) + (x - w * E)] = 0;
         }
         __syncthreads();
-        // thread (column, row group): column c of E, rows rg, rg + G, ...
+        // thread (column, row group): column c, rows rg, rg + G, ...; sixteen
+        // loads in flight per thread, so a 64 x 128 instance is one round trip
+        // to L2 (where ep_count just left the rows).  With E a multiple of 4
+        // and the rows 16-byte aligned a column is four experts (int4 loads).
         constexpr int kThr = kPlanWarps * 32;
-        const int G = max(1, kThr / E);
-        for (int x = threadIdx.x; x < nb * E * G; x += kThr) {
-            const int wi = x / (E * G), rem = x - wi * E * G;
-            const int rg = rem / E, e = rem - rg * E;
-            const int32_t* cs = counts_src + (int64_t)(g0 + wi) * R * E + e;
-            int t = 0;
-            for (int r0 = rg; r0 < R; r0 += 8 * G) {
-                int v[8];
+        constexpr int kU = 16;
+        if ((E & 3) == 0 && (reinterpret_cast<uintptr_t>(counts_src) & 15u) == 0) {
+            const int Q = E >> 2;
+            const int G = max(1, kThr / Q);
+            for (int x = threadIdx.x; x < nb * Q * G; x += kThr) {
+                const int wi = x / (Q * G), rem = x - wi * Q * G;
+                const int rg = rem / Q, c = rem - rg * Q;
+                const int4* cs =
+                    reinterpret_cast<const int4*>(counts_src + (int64_t)(g0 + wi) * R * E) + c;
+                int4 t = make_int4(0, 0, 0, 0);
+                for (int r0 = rg; r0 < R; r0 += kU * G) {
+                    int4 v[kU];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
-                    const int rr = r0 + u * G;
-                    v[u] = (rr < R) ? __ldg(cs + (int64_t)rr * E) : 0;
+                    for (int u = 0; u < kU; ++u) {
+                        const int rr = r0 + u * G;
+                        v[u] = (rr < R) ? __ldg(cs + (int64_t)rr * Q) : make_int4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        t.x += v[u].x;
+                        t.y += v[u].y;
+                        t.z += v[u].z;
+                        t.w += v[u].w;
+                    }
                 }
-#pragma unroll
-                for (int u = 0; u < 8; ++u) t += v[u];
+                int32_t* to = csum0 + wi * (wbytes / 4) + 4 * c;
+                atomicAdd(to, t.x);
+                atomicAdd(to + 1, t.y);
+                atomicAdd(to + 2, t.z);
+                atomicAdd(to + 3, t.w);
             }
-            atomicAdd(&csum0[wi * (wbytes / 4) + e], t);
+        } else {
+            const int G = max(1, kThr / E);
+            for (int x = threadIdx.x; x < nb * E * G; x += kThr) {
+                const int wi = x / (E * G), rem = x - wi * E * G;
+                const int rg = rem / E, e = rem - rg * E;
+                const int32_t* cs = counts_src + (int64_t)(g0 + wi) * R * E + e;
+                int t = 0;
+                for (int r0 = rg; r0 < R; r0 += kU * G) {
+                    int v[kU];
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) {
+                        const int rr = r0 + u * G;
+                        v[u] = (rr < R) ? __ldg(cs + (int64_t)rr * E) : 0;
+                    }
+#pragma unroll
+                    for (int u = 0; u < kU; ++u) t += v[u];
+                }
+                atomicAdd(&csum0[wi * (wbytes / 4) + e], t);
+            }
         }
         __syncthreads();
         if (g < n_inst) {

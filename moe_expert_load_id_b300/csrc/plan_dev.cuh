@@ -40,7 +40,7 @@ __device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB
         const unsigned ka = hasA ? ((unsigned)la << 6) | (unsigned)(63 - lane) : 0u;
         const unsigned kb = hasB ? ((unsigned)lb << 6) | (unsigned)(31 - lane) : 0u;
         const unsigned k = __reduce_max_sync(kFull, kTwo ? max(ka, kb) : ka);
-        hot = 63 - (int)(k & 63u);
+        hot = (int)((k & 63u) ^ 63u);  // 63 - (k & 63)
         Lmax = (int)(k >> 6);
     } else {
         Lmax = __reduce_max_sync(kFull, kTwo ? max(la, lb) : la);
@@ -55,10 +55,10 @@ __device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB
 // slots slot[R*S] (-1: empty) and, per expert, the mask of ranks holding it;
 // the loads stay in registers (lane l: ranks l and l+32).  Per move the hot
 // rank's largest instance is one warp reduction over its W instances (lane j:
-// instance j), eligibility is one 64-bit mask (holders of e | ranks with a
-// free slot), and the bookkeeping is a few single-lane stores, so nothing in a
-// move grows with the instances per rank.  The tables are exactly the
-// epilogue's.
+// instance j), eligibility is one rank mask (holders of e | ranks with a free
+// slot, each lane testing its own two bits), and the bookkeeping is a few
+// single-lane stores, so nothing in a move grows with the instances per rank.
+// The tables are exactly the epilogue's.
 //
 // Every quota and spare-slot entry of the table is read and written by one
 // lane only: lane j owns local instance j of every rank (q[r*W + j] and, for
@@ -67,19 +67,29 @@ __device__ __forceinline__ void argmax_rank(int la, int lb, bool hasA, bool hasB
 // needs no warp barrier before the next one reads the table: the bookkeeping
 // of one move overlaps the search of the next.
 //
+// The moves form one dependent chain of warp reductions and shared-memory
+// loads, issued in order by one warp, so every operation on it counts: rank
+// masks are handled as two 32-bit halves (lane l tests bit l of each), and a
+// rank holds e exactly when e is one of its home experts or one of its spare
+// slots votes for e.
+//
 // kQPacked (total below 2^21): the hot rank's largest instance (lowest expert
-// on ties) is one max-reduction over the key 1 + (quota << 10 | 1023 - e).
+// on ties) is one max-reduction over the key quota << 10 | 1023 - e; lanes
+// without an instance offer 1024 - E, the key of expert E - 1 at quota 0,
+// which can only win when every quota of the rank is 0 (then nothing moves).
 template <bool kTwo, bool kPacked, bool kQPacked>
 __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint64_t* holder,
                                                  int& loadA, int& loadB, int lane, int H, int S,
-                                                 int W, int R, int max_iters, int& iters,
+                                                 int W, int R, int E, int max_iters, int& iters,
                                                  int& status) {
     const bool hasA = loadA >= 0, hasB = kTwo && loadB >= 0;
     const int ra = lane, rb = lane + 32;
-    const uint64_t exist = (R >= 64) ? ~0ull : ((1ull << R) - 1ull);
-    uint64_t freem = S > 0 ? exist : 0ull;  // ranks with a free spare slot (warp-uniform)
+    // ranks with a free spare slot, as two halves (ranks 0-31, 32-63); a lane
+    // only tests the bits of its own ranks, which exist
+    unsigned freeLo = S > 0 ? ~0u : 0u, freeHi = freeLo;
     const bool owner = lane < W;            // lane j owns local instance j
     const bool spare = lane >= H && owner;  // ... a spare slot of every rank
+    const unsigned noInst = (unsigned)(1024 - E);
     int hot, Lmax;
     argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, hot, Lmax);
     while (true) {
@@ -93,10 +103,10 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         int qmax, e;
         bool mine;  // this lane owns the instance that gives
         if (kQPacked) {
-            const unsigned key = (xj >= 0) ? 1u + (((unsigned)qv << 10) | (unsigned)(1023 - xj)) : 0u;
+            const unsigned key = (xj >= 0) ? (((unsigned)qv << 10) | (unsigned)(1023 - xj)) : noInst;
             const unsigned kmax = __reduce_max_sync(kFull, key);
-            qmax = (int)((kmax - 1u) >> 10);
-            e = 1023 - (int)((kmax - 1u) & 1023u);
+            qmax = (int)(kmax >> 10);
+            e = 1023 - (int)(kmax & 1023u);
             mine = key == kmax;
         } else {
             const int qj = xj >= 0 ? qv : -1;
@@ -108,13 +118,13 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         }
 
         // 3-5. eligible ranks: the others that hold e or have a free slot;
-        // the coldest of them (lowest rank on ties) and the amount.  No
-        // eligible rank leaves the reduction at its identity (an amount <= 0);
-        // the stop conditions and the cap are tested with one branch.
+        // the coldest of them (lowest rank on ties) and the amount.  With no
+        // eligible rank the reduction keeps its identity, which gives an
+        // amount <= 0; the stop conditions and the cap are one branch.
         const uint64_t hm = holder[e];
-        const uint64_t el = (hm | freem) & exist & ~(1ull << hot);
-        const bool elA = hasA && ((el >> ra) & 1ull);
-        const bool elB = hasB && ((el >> rb) & 1ull);
+        const unsigned mLo = (unsigned)hm | freeLo, mHi = (unsigned)(hm >> 32) | freeHi;
+        const bool elA = hasA && ra != hot && ((mLo >> lane) & 1u);
+        const bool elB = hasB && rb != hot && ((mHi >> lane) & 1u);
         int cold, Lmin;
         if (kPacked) {
             const unsigned ca = elA ? ((unsigned)loadA << 6) | (unsigned)ra : 0xffffffffu;
@@ -133,8 +143,8 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         const int mv = min(qmax, (Lmax - Lmin) >> 1);
         // 6. stop: no rank eligible, or nothing to move (the global stop);
         // else the safety cap
-        if (el == 0ull || mv <= 0 || iters == max_iters) {
-            if (el != 0ull && mv > 0) status = EP_ERR_ITER_LIMIT;
+        if (mv <= 0 || iters == max_iters) {
+            if (mv > 0) status = EP_ERR_ITER_LIMIT;
             break;
         }
         // 7. move.  Loads first, then the next move's argmax ...
@@ -149,9 +159,9 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         const int sv = spare ? slot[cold * S + (lane - H)] : 0;
         const unsigned hit = __ballot_sync(kFull, spare && sv == e);
         const unsigned freeb = __ballot_sync(kFull, spare && sv < 0);  // cold's free slots
-        const bool held = (hm >> cold) & 1ull;
         const int ej = e - cold * H;
         const bool home = (unsigned)ej < (unsigned)H;  // e is one of cold's home experts
+        const bool held = home || hit != 0u;
         const unsigned pick = held ? hit : freeb;       // nonzero unless home: cold is eligible
         if (!home && pick == 0u) {                      // (never; keeps every index in range)
             status = EP_ERR_INVAL;
@@ -164,8 +174,15 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
             q[cold * W + lane] += mv;
             if (!held) slot[cold * S + (lane - H)] = e;
         }
-        if (!held) holder[e] = hm | (1ull << cold);  // every lane, the same value
-        if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
+        if (!held) {
+            const unsigned bit = 1u << (cold & 31);
+            const bool lo = cold < 32;
+            holder[e] = hm | ((uint64_t)(lo ? 0u : bit) << 32) | (lo ? bit : 0u);  // every lane
+            if ((freeb & (freeb - 1u)) == 0u) {  // its last free slot
+                if (lo) freeLo &= ~bit;
+                else freeHi &= ~bit;
+            }
+        }
         hot = nhot;
         Lmax = nLmax;
         ++iters;
@@ -406,13 +423,13 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
     } else if (status == EP_OK) {
         if (tot < kQPackLimit)
             plan_moves_table<kTwo, true, true>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
-                                               max_iters, iters, status);
+                                               E, max_iters, iters, status);
         else if (tot < kPackLimit)
             plan_moves_table<kTwo, true, false>(q, slot, holder, loadA, loadB, lane, H, S, W, R,
-                                                max_iters, iters, status);
+                                                E, max_iters, iters, status);
         else
             plan_moves_table<kTwo, false, false>(q, slot, holder, loadA, loadB, lane, H, S, W,
-                                                 R, max_iters, iters, status);
+                                                 R, E, max_iters, iters, status);
     }
     __syncwarp();  // the table's entries, written by their owner lanes, for every lane
     for (int p = lane; p < P; p += 32) qo[p] = q[p];
