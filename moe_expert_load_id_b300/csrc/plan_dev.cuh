@@ -89,6 +89,7 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
     unsigned freeLo = S > 0 ? ~0u : 0u, freeHi = freeLo;
     const bool owner = lane < W;            // lane j owns local instance j
     const bool spare = lane >= H && owner;  // ... a spare slot of every rank
+    const unsigned lt = lanemask_lt();
     const unsigned noInst = (unsigned)(1024 - E);
     int hot, Lmax;
     argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, hot, Lmax);
@@ -154,9 +155,11 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
         argmax_rank<kTwo, kPacked>(loadA, loadB, hasA, hasB, lane, nhot, nLmax);
         // ... and the tables: cold's instance of e is its home, a spare slot
         // already holding e, or its lowest free spare slot (filled now).  The
-        // spare slots are read by their owner lanes and voted on
-        // unconditionally (no branch), so this overlaps the argmax above.
+        // owner lanes read cold's spare slot and quota unconditionally and vote
+        // on the slots; each lane then tests whether it is the instance (no
+        // bit scan), so this overlaps the argmax above.
         const int sv = spare ? slot[cold * S + (lane - H)] : 0;
+        const int qc = owner ? q[cold * W + lane] : 0;
         const unsigned hit = __ballot_sync(kFull, spare && sv == e);
         const unsigned freeb = __ballot_sync(kFull, spare && sv < 0);  // cold's free slots
         const int ej = e - cold * H;
@@ -167,22 +170,22 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
             status = EP_ERR_INVAL;
             break;
         }
-        const int dj = home ? ej : __ffs(pick) - 1;     // cold's instance (a lane index)
+        // this lane is cold's instance: e's home, else the lowest lane of pick
+        const bool dst = home ? lane == ej : ((pick >> lane) & 1u) && (pick & lt) == 0u;
         // owner-lane updates, no read-modify-write across lanes
         if (mine) q[hot * W + lane] = qv - mv;
-        if (lane == dj) {
-            q[cold * W + lane] += mv;
+        if (dst) {
+            q[cold * W + lane] = qc + mv;
             if (!held) slot[cold * S + (lane - H)] = e;
         }
-        if (!held) {
-            const unsigned bit = 1u << (cold & 31);
-            const bool lo = cold < 32;
-            holder[e] = hm | ((uint64_t)(lo ? 0u : bit) << 32) | (lo ? bit : 0u);  // every lane
-            if ((freeb & (freeb - 1u)) == 0u) {  // its last free slot
-                if (lo) freeLo &= ~bit;
-                else freeHi &= ~bit;
-            }
-        }
+        // cold now holds e (a no-op when it held it already); its last free
+        // slot taken: it has none left
+        const unsigned bit = 1u << (cold & 31);
+        const bool lo = cold < 32;
+        holder[e] = hm | ((uint64_t)(lo ? 0u : bit) << 32) | (lo ? bit : 0u);  // every lane
+        const unsigned full = (!held && (freeb & (freeb - 1u)) == 0u) ? bit : 0u;
+        freeLo &= lo ? ~full : ~0u;
+        freeHi &= lo ? ~0u : ~full;
         hot = nhot;
         Lmax = nLmax;
         ++iters;

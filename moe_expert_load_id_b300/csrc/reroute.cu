@@ -122,21 +122,85 @@ __device__ __forceinline__ int upper_bound(const int32_t* a, int lo, int hi, int
     return lo;
 }
 
+// The rank's counts in shared memory (nothing here depends on the plan):
+//   base[E]   += slots of e on source ranks below r
+//   want[E]   = counts_src[r][e] (not loaded when want is null); plan_tables
+//             adds base[e] to it
+// base must be zero, and a block barrier passed, before the call.  With E a
+// multiple of 4 and the rows 16-byte aligned, thread (g, q) sums the int4
+// column q (experts 4q .. 4q+3) over rows g, g+G, ... < r (G = threads /
+// (E/4)), 2048 / threads loads in flight (every row of 64 ranks at E = 128 in
+// one round); otherwise thread (g, e) sums column e the same way (G =
+// threads / E).  The partial sums meet in base[] by atomics.
+template <int kThreads>
+__device__ __forceinline__ void rank_prefix(int R, int E, int inst, int r,
+                                            const int32_t* __restrict__ counts_src,
+                                            int32_t* base, int32_t* want) {
+    constexpr int kU = 2048 / kThreads > 1 ? 2048 / kThreads : 1;
+    const int tid = threadIdx.x;
+    const int32_t* own = counts_src + ((int64_t)inst * R + r) * E;
+    if (want != nullptr)
+        for (int e = tid; e < E; e += kThreads) want[e] = __ldg(own + e);
+    const int32_t* cs = counts_src + (int64_t)inst * R * E;
+    const int Q = E >> 2;
+    if ((E & 3) == 0 && Q <= kThreads && (reinterpret_cast<uintptr_t>(cs) & 15u) == 0) {
+        const int G = kThreads / Q;
+        const int q = tid % Q, g = tid / Q;
+        if (g < G) {
+            int4 t = make_int4(0, 0, 0, 0);
+            for (int r0 = g; r0 < r; r0 += kU * G) {
+                int4 v[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int rr = r0 + u * G;
+                    v[u] = (rr < r) ? __ldg(reinterpret_cast<const int4*>(cs + (int64_t)rr * E) + q)
+                                    : make_int4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    t.x += v[u].x;
+                    t.y += v[u].y;
+                    t.z += v[u].z;
+                    t.w += v[u].w;
+                }
+            }
+            if (t.x != 0) atomicAdd(&base[4 * q], t.x);
+            if (t.y != 0) atomicAdd(&base[4 * q + 1], t.y);
+            if (t.z != 0) atomicAdd(&base[4 * q + 2], t.z);
+            if (t.w != 0) atomicAdd(&base[4 * q + 3], t.w);
+        }
+    } else {
+        const int G = (E <= kThreads) ? kThreads / E : 1;
+        for (int x = tid; x < G * E; x += kThreads) {
+            const int e = x % E, g = x / E;
+            int t = 0;
+            for (int r0 = g; r0 < r; r0 += kU * G) {
+                int v[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int rr = r0 + u * G;
+                    v[u] = (rr < r) ? cs[(int64_t)rr * E + e] : 0;
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) t += v[u];
+            }
+            if (t != 0) atomicAdd(&base[e], t);
+        }
+    }
+}
+
 // Plan tables in shared memory:
 //   off[P+1]  first row of each instance (exclusive prefix of quota over p)
 //   ptr[E+1]  CSR row pointers of the instance lists, clamped to [0, M]
 //   bcum[M]   inclusive cumulative quota of each list entry (INT_MIN if unused)
 //   bdel[M]   row minus within-expert rank, for the ranks of that entry
-//   base[E]   += slots of e on source ranks below r
-//   want[E]   base[e] + counts_src[r][e]: the running base after the block's
-//             last chunk when counts_src describes these ids (not built when
-//             want is null)
-// base must be zero, and a block barrier passed, before the call; the block
-// of source rank 0 also writes inst_offset.  The caller puts a barrier
+//   want[E]   += base[e]: the running base after the block's last chunk when
+//             counts_src describes these ids (when want is not null)
+// rank_prefix must have run, and no block barrier is needed after it; the
+// block of source rank 0 also writes inst_offset.  The caller puts a barrier
 // between this and any read of the tables.
 template <int kThreads>
-__device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst, int r,
-                                            const int32_t* __restrict__ counts_src,
+__device__ __forceinline__ void plan_tables(int E, int P, int M, int inst, int r,
                                             const int32_t* __restrict__ quota,
                                             const int32_t* __restrict__ inst_ptr,
                                             const int32_t* __restrict__ inst_id,
@@ -149,93 +213,36 @@ __device__ __forceinline__ void plan_tables(int R, int E, int P, int M, int inst
     constexpr int kIpt = (2048 + kThreads - 1) / kThreads;  // P <= 2048 quota per thread
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int32_t* qg = quota + (int64_t)inst * P;
+    const int32_t* pg = inst_ptr + (int64_t)inst * (E + 1);
+    const int32_t* ig = inst_id + (int64_t)inst * M;
+    const int32_t* cg = inst_cum + (int64_t)inst * M;
+    // every load of the plan's outputs is independent of the others, so the
+    // prologue waits for memory once: the list entries are loaded whole and
+    // the used length applied afterwards
     int qv[kIpt];
-    int qlocal = 0;
 #pragma unroll
     for (int u = 0; u < kIpt; ++u) {
         const int p = tid * kIpt + u;
         qv[u] = (p < P) ? qg[p] : 0;
-        qlocal += qv[u];
     }
-    const int32_t* pg = inst_ptr + (int64_t)inst * (E + 1);
-    for (int e = tid; e <= E; e += kThreads) ptr[e] = min(max(pg[e], 0), M);
-    // the list entries: cumulative quota, and for now the instance (-1 when
-    // unused or out of range); every load here and below is independent, so
-    // the prologue waits for memory once
-    {
-        const int nM = min(max(__ldg(pg + E), 0), M);
-        const int32_t* ig = inst_id + (int64_t)inst * M;
-        const int32_t* cg = inst_cum + (int64_t)inst * M;
-        for (int m = tid; m < M; m += kThreads) {
-            int cum = INT_MIN, p = -1;
-            if (m < nM) {
-                const int pm = ig[m], cm = cg[m];
-                if (pm >= 0 && pm < P) {
-                    p = pm;
-                    cum = cm;
-                }
-            }
-            bcum[m] = cum;
-            bdel[m] = p;
+    const int nM = min(max(pg[E], 0), M);
+    const int xn = max(E + 1, M);
+    for (int x = tid; x < xn; x += kThreads) {
+        const int pe = (x <= E) ? pg[x] : 0;
+        const int pm = (x < M) ? ig[x] : -1;
+        const int cm = (x < M) ? cg[x] : 0;
+        if (x <= E) ptr[x] = min(max(pe, 0), M);
+        if (x < M) {
+            // cumulative quota, and for now the instance (-1 when unused or
+            // out of range)
+            const bool used = x < nM && pm >= 0 && pm < P;
+            bcum[x] = used ? cm : INT_MIN;
+            bdel[x] = used ? pm : -1;
         }
     }
-    // this rank's own row of counts_src, for the check after the last chunk
-    const int32_t* own = counts_src + ((int64_t)inst * R + r) * E;
-    if (want != nullptr)
-        for (int e = tid; e < E; e += kThreads) want[e] = __ldg(own + e);
-    // per-expert slots on earlier source ranks.  With E a multiple of 4 and
-    // the rows 16-byte aligned, thread (g, q) sums the int4 column q
-    // (experts 4q .. 4q+3) over rows g, g+G, ... < r (G = threads / (E/4)),
-    // eight loads in flight; otherwise thread (g, e) sums column e the same
-    // way (G = threads / E).  The partial sums meet in base[] by atomics.
-    {
-        const int32_t* cs = counts_src + (int64_t)inst * R * E;
-        const int Q = E >> 2;
-        if ((E & 3) == 0 && Q <= kThreads && (reinterpret_cast<uintptr_t>(cs) & 15u) == 0) {
-            const int G = kThreads / Q;
-            const int q = tid % Q, g = tid / Q;
-            if (g < G) {
-                int4 t = make_int4(0, 0, 0, 0);
-                for (int r0 = g; r0 < r; r0 += 8 * G) {
-                    int4 v[8];
+    int qlocal = 0;
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int rr = r0 + u * G;
-                        v[u] = (rr < r) ? __ldg(reinterpret_cast<const int4*>(cs + (int64_t)rr * E) + q)
-                                        : make_int4(0, 0, 0, 0);
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        t.x += v[u].x;
-                        t.y += v[u].y;
-                        t.z += v[u].z;
-                        t.w += v[u].w;
-                    }
-                }
-                if (t.x != 0) atomicAdd(&base[4 * q], t.x);
-                if (t.y != 0) atomicAdd(&base[4 * q + 1], t.y);
-                if (t.z != 0) atomicAdd(&base[4 * q + 2], t.z);
-                if (t.w != 0) atomicAdd(&base[4 * q + 3], t.w);
-            }
-        } else {
-            const int G = (E <= kThreads) ? kThreads / E : 1;
-            for (int x = tid; x < G * E; x += kThreads) {
-                const int e = x % E, g = x / E;
-                int t = 0;
-                for (int r0 = g; r0 < r; r0 += 8 * G) {
-                    int v[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int rr = r0 + u * G;
-                        v[u] = (rr < r) ? cs[(int64_t)rr * E + e] : 0;
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) t += v[u];
-                }
-                if (t != 0) atomicAdd(&base[e], t);
-            }
-        }
-    }
+    for (int u = 0; u < kIpt; ++u) qlocal += qv[u];
     // inst_offset: exclusive prefix of quota over p
     int qx = qlocal;
 #pragma unroll
@@ -408,6 +415,8 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         load_chunk(s0);
         phase_a();
     }
+    // the rank's counts (ep_count's output, complete before the plan started)
+    rank_prefix<kThreads>(R, E, inst, r, counts_src, base, want);
     int lower = 0;  // thread e: slots of e in the cluster's blocks below this one
     if constexpr (kCl > 1) {
         // the block's per-expert totals (its one chunk's per-warp counts),
@@ -430,8 +439,8 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 
     // ---- prologue: plan tables (want[] gets the rank's whole count); a block
     // of a cluster starts at the slots of the blocks below it
-    plan_tables<kThreads>(R, E, P, M, inst, r, counts_src, quota, inst_ptr, inst_id, inst_cum,
-                          inst_offset, off, ptr, bcum, bdel, base, want, warp_tot, cl == 0);
+    plan_tables<kThreads>(E, P, M, inst, r, quota, inst_ptr, inst_id, inst_cum, inst_offset, off,
+                          ptr, bcum, bdel, base, want, warp_tot, cl == 0);
     if constexpr (kCl > 1) {
         if (tid < E) base[tid] += lower;  // (thread e alone touches base[e] here)
     }
@@ -741,13 +750,10 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
     if (tid == 0) flags = 0;
     for (int e = tid; e < E; e += kQuadThreads) base[e] = 0;
     __syncthreads();
-    if (early) pdl_wait();
-    pdl_trigger();
-
-    // ---- prologue: plan tables, then each warp's prefix over source ranks
-    plan_tables<kQuadThreads>(R, E, P, M, inst, r0, counts_src, quota, inst_ptr, inst_id,
-                              inst_cum, inst_offset, off, ptr, bcum, bdel, base, nullptr,
-                              warp_tot);
+    // the counts (ep_count's output, complete before the plan started): the
+    // slots of every expert on the ranks below the block's, and the block's
+    // ranks' own rows
+    rank_prefix<kQuadThreads>(R, E, inst, r0, counts_src, base, nullptr);
     {
         const int32_t* cs = counts_src + ((int64_t)inst * R + r0) * E;
         for (int x = tid; x < kQuadWarps * E; x += kQuadThreads) {
@@ -755,6 +761,12 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
             pre[(w + 1) * E + e] = (w < nr) ? __ldg(cs + (int64_t)w * E + e) : 0;
         }
     }
+    if (early) pdl_wait();
+    pdl_trigger();
+
+    // ---- prologue: plan tables, then each warp's prefix over source ranks
+    plan_tables<kQuadThreads>(E, P, M, inst, r0, quota, inst_ptr, inst_id, inst_cum, inst_offset,
+                              off, ptr, bcum, bdel, base, nullptr, warp_tot);
     __syncthreads();
     for (int e = tid; e < E; e += kQuadThreads) {
         int run = base[e];
