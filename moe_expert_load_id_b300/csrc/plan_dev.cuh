@@ -446,10 +446,12 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
 // cumulative quotas.  The whole block (kThreads threads) builds one instance's
 // lists: a block scan over the holder counts gives the list offsets (writes
 // po[0..E] and the home entries); every spare slot then finds its own place
-// in its expert's list (1 + its expert's replicas on lower ranks); each
-// expert's running sums are a short walk over its list.  pos[E+1] and
-// val[E+R*S] are shared-memory scratch (the offsets and each entry's quota),
-// wtot[kThreads/32] the scan's warp totals.  Called by every thread of the
+// in its expert's list (1 + its expert's replicas on lower ranks); the
+// running sums are one segmented block scan over all entries (a list starts
+// at its home entry), so a hot expert's long list costs no more than a short
+// one.  pos[E+1] and val[E+R*S] are shared-memory scratch (the offsets, and
+// each entry's quota with bit 31 set on a list's first entry),
+// wtot[kThreads/32] the scans' warp totals.  Called by every thread of the
 // block; starts and ends with a block barrier's worth of ordering.
 template <int kThreads>
 __device__ __forceinline__ void plan_csr_block(const int32_t* q, const int32_t* slot,
@@ -486,7 +488,7 @@ __device__ __forceinline__ void plan_csr_block(const int32_t* q, const int32_t* 
         const int home = e / H;
         const int hp = home * W + (e - home * H);  // the home instance heads the list
         io[run] = hp;
-        val[run] = q[hp];
+        val[run] = q[hp] | INT_MIN;  // a list's first entry
         run += __popcll(holder[e]);
     }
     if (tid == 0) {
@@ -506,13 +508,35 @@ __device__ __forceinline__ void plan_csr_block(const int32_t* q, const int32_t* 
         val[m] = q[p];
     }
     __syncthreads();
-    for (int e = tid; e < E; e += kThreads) {
-        const int m1 = pos[e + 1];
-        int cum = 0;
-        for (int m = pos[e]; m < m1; ++m) {
-            cum += val[m];
-            co[m] = cum;
-        }
+    // segmented inclusive scan of the entries: a value is (bit 31: a list
+    // starts in it) | running sum, and seg(a, b) = b when b starts a list,
+    // else a + b (the sums stay below 2^31).  Thread t takes a run of
+    // consecutive entries: its own segmented sum, a warp scan and a scan of
+    // the warp totals give the value entering its run.
+    auto seg = [](unsigned a, unsigned b) -> unsigned { return (b >> 31) ? b : a + b; };
+    const int Mu = pos[E];
+    const int per2 = (Mu + kThreads - 1) / kThreads;
+    const int m0 = min(Mu, tid * per2), m1 = min(Mu, m0 + per2);
+    unsigned own = 0u;
+    for (int m = m0; m < m1; ++m) own = seg(own, (unsigned)val[m]);
+    unsigned sx = own;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned y = __shfl_up_sync(kFull, sx, o);
+        if (lane >= o) sx = seg(y, sx);
+    }
+    unsigned ex = __shfl_up_sync(kFull, sx, 1);
+    if (lane == 0) ex = 0u;
+    if (lane == 31) wtot[warp] = (int)sx;
+    __syncthreads();
+    unsigned run2 = 0u;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w)
+        if (w < warp) run2 = seg(run2, (unsigned)wtot[w]);
+    run2 = seg(run2, ex);
+    for (int m = m0; m < m1; ++m) {
+        run2 = seg(run2, (unsigned)val[m]);
+        co[m] = (int)(run2 & 0x7fffffffu);
     }
     __syncthreads();  // the scratch may be reused by the next call
 }
