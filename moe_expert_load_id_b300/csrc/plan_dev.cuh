@@ -199,11 +199,14 @@ __device__ __forceinline__ void plan_moves_table(int32_t* q, int32_t* slot, uint
 //   expert on ties).  A candidate (c, e) can move exactly when some eligible
 //   rank d != c (holding e, or with a free slot) has L[d] <= L[c] - 2: the
 //   coldest eligible rank then gives q >= 1.  So every lane evaluates its own
-//   ranks at once: the mask of ranks at least 2 below its rank's load (from a
-//   shared-memory copy of the loads), then each of the rank's instances
-//   against (holders of e | ranks with a free slot); one reduction over the
-//   ranks that have a movable instance picks the candidate.  A move costs the
-//   same however many candidates cannot move.
+//   ranks at once: each rank's mask of the ranks at least 2 below its load,
+//   then each of the rank's instances against (holders of e | ranks with a
+//   free slot); one reduction over the ranks that have a movable instance
+//   picks the candidate.  A move costs the same however many candidates
+//   cannot move.  The masks are built once (from a shared-memory copy of the
+//   loads) and then kept: a move changes two loads, so every other rank
+//   re-tests two bits, and the two ranks that moved take their masks from
+//   two ballots each over the new loads.
 //   EP_PLAN_RELEASE: a spare-slot instance a move leaves at quota 0 frees its
 //   slot (its rank no longer holds the expert; the slot is free again).
 // Without EP_PLAN_SKIP the candidate is the base rule's (the hottest rank's
@@ -224,48 +227,64 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
     Ls[ra] = hasA ? loadA : INT_MAX;
     Ls[rb] = hasB ? loadB : INT_MAX;
     __syncwarp();
-    // the best instance (largest quota >= 1, lowest expert) of rank r whose
-    // expert has an eligible rank in `low`; bq = -1 when there is none
-    auto best_movable = [&](int r, bool has, uint64_t low, int& bq, int& be, int& bj) {
-        bq = -1;
-        be = INT_MAX;
-        bj = 0;
-        if (!has || low == 0ull) return;
+    // my ranks' masks of the ranks at least 2 below them (a rank is never
+    // below itself), as halves: ranks 0-31 and 32-63
+    unsigned loA = 0u, hiA = 0u, loB = 0u, hiB = 0u;
+    if (skip) {
+        const int tA = loadA - 2, tB = loadB - 2;
+#pragma unroll 4
+        for (int d = 0; d < 32; d += 4) {
+            const int4 v = *reinterpret_cast<const int4*>(Ls + d);
+            const int4 w = *reinterpret_cast<const int4*>(Ls + 32 + d);
+            loA |= ((unsigned)(v.x <= tA) | (unsigned)(v.y <= tA) << 1 |
+                    (unsigned)(v.z <= tA) << 2 | (unsigned)(v.w <= tA) << 3) << d;
+            hiA |= ((unsigned)(w.x <= tA) | (unsigned)(w.y <= tA) << 1 |
+                    (unsigned)(w.z <= tA) << 2 | (unsigned)(w.w <= tA) << 3) << d;
+            if (kTwo) {
+                loB |= ((unsigned)(v.x <= tB) | (unsigned)(v.y <= tB) << 1 |
+                        (unsigned)(v.z <= tB) << 2 | (unsigned)(v.w <= tB) << 3) << d;
+                hiB |= ((unsigned)(w.x <= tB) | (unsigned)(w.y <= tB) << 1 |
+                        (unsigned)(w.z <= tB) << 2 | (unsigned)(w.w <= tB) << 3) << d;
+            }
+        }
+    }
+    // the best instance (largest quota >= 1, lowest expert) of each of my two
+    // ranks whose expert has an eligible rank in that rank's low mask; bq = -1
+    // when there is none.  The two ranks' loads are issued together and the
+    // tests are selects.
+    auto best_movable2 = [&](uint64_t lowA, uint64_t lowB, int& bqA, int& beA, int& bjA,
+                             int& bqB, int& beB, int& bjB) {
+        bqA = bqB = -1;
+        beA = beB = INT_MAX;
+        bjA = bjB = 0;
+        const bool tA = hasA && lowA != 0ull, tB = hasB && lowB != 0ull;
+        if (!tA && !tB) return;
         for (int j = 0; j < W; ++j) {
-            const int ex = j < H ? r * H + j : slot[r * S + (j - H)];
-            if (ex < 0) continue;
-            const int qq = q[r * W + j];
-            if (qq < 1 || (qq < bq) || (qq == bq && ex > be)) continue;
-            if (((holder[ex] | freem) & exist & low) == 0ull) continue;
-            bq = qq;
-            be = ex;
-            bj = j;
+            const bool home = j < H;
+            const int exA = home ? ra * H + j : (tA ? slot[ra * S + (j - H)] : -1);
+            const int exB = home ? rb * H + j : (tB ? slot[rb * S + (j - H)] : -1);
+            const int qA = tA ? q[ra * W + j] : 0;
+            const int qB = tB ? q[rb * W + j] : 0;
+            const uint64_t hA = (tA && exA >= 0) ? holder[exA] : 0ull;
+            const uint64_t hB = (tB && exB >= 0) ? holder[exB] : 0ull;
+            const bool okA = tA && exA >= 0 && qA >= 1 && (qA > bqA || (qA == bqA && exA < beA)) &&
+                             ((hA | freem) & lowA) != 0ull;
+            const bool okB = tB && exB >= 0 && qB >= 1 && (qB > bqB || (qB == bqB && exB < beB)) &&
+                             ((hB | freem) & lowB) != 0ull;
+            bqA = okA ? qA : bqA;
+            beA = okA ? exA : beA;
+            bjA = okA ? j : bjA;
+            bqB = okB ? qB : bqB;
+            beB = okB ? exB : beB;
+            bjB = okB ? j : bjB;
         }
     };
     while (true) {
         int c, Lc, e, qsrc, src_j;  // the candidate (warp-uniform)
         if (skip) {
-            // ranks at least 2 below my ranks' loads (a rank is never below itself)
-            unsigned loA = 0u, hiA = 0u, loB = 0u, hiB = 0u;
-            const int tA = loadA - 2, tB = loadB - 2;
-#pragma unroll 4
-            for (int d = 0; d < 32; d += 4) {
-                const int4 v = *reinterpret_cast<const int4*>(Ls + d);
-                const int4 w = *reinterpret_cast<const int4*>(Ls + 32 + d);
-                loA |= ((unsigned)(v.x <= tA) | (unsigned)(v.y <= tA) << 1 |
-                        (unsigned)(v.z <= tA) << 2 | (unsigned)(v.w <= tA) << 3) << d;
-                hiA |= ((unsigned)(w.x <= tA) | (unsigned)(w.y <= tA) << 1 |
-                        (unsigned)(w.z <= tA) << 2 | (unsigned)(w.w <= tA) << 3) << d;
-                if (kTwo) {
-                    loB |= ((unsigned)(v.x <= tB) | (unsigned)(v.y <= tB) << 1 |
-                            (unsigned)(v.z <= tB) << 2 | (unsigned)(v.w <= tB) << 3) << d;
-                    hiB |= ((unsigned)(w.x <= tB) | (unsigned)(w.y <= tB) << 1 |
-                            (unsigned)(w.z <= tB) << 2 | (unsigned)(w.w <= tB) << 3) << d;
-                }
-            }
-            int bqA, beA, bjA, bqB = -1, beB = INT_MAX, bjB = 0;
-            best_movable(ra, hasA, ((uint64_t)hiA << 32) | loA, bqA, beA, bjA);
-            if (kTwo) best_movable(rb, hasB, ((uint64_t)hiB << 32) | loB, bqB, beB, bjB);
+            int bqA, beA, bjA, bqB, beB, bjB;
+            best_movable2(((uint64_t)hiA << 32) | loA, kTwo ? ((uint64_t)hiB << 32) | loB : 0ull,
+                          bqA, beA, bjA, bqB, beB, bjB);
             // the first rank in (load desc, index asc) order with a movable instance
             const bool mA = bqA >= 1, mB = kTwo && bqB >= 1;
             if (kPacked) {
@@ -338,6 +357,34 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
         // holding e, or its lowest free slot, filled now)
         loadA += (ra == cold ? mv : 0) - (ra == c ? mv : 0);
         if (kTwo) loadB += (rb == cold ? mv : 0) - (rb == c ? mv : 0);
+        if (skip) {
+            // the masks: c and cold from ballots over the new loads; every
+            // other rank re-tests bits c and cold
+            const int nLc = Lc - mv, nLd = Lmin + mv;
+            const unsigned cLo = __ballot_sync(kFull, hasA && loadA <= nLc - 2);
+            const unsigned cHi = kTwo ? __ballot_sync(kFull, hasB && loadB <= nLc - 2) : 0u;
+            const unsigned dLo = __ballot_sync(kFull, hasA && loadA <= nLd - 2);
+            const unsigned dHi = kTwo ? __ballot_sync(kFull, hasB && loadB <= nLd - 2) : 0u;
+            const unsigned bc = 1u << (c & 31), bd = 1u << (cold & 31);
+            const bool cLoHalf = c < 32, dLoHalf = cold < 32;
+            auto retest = [&](int r, int L, unsigned& lo, unsigned& hi) {
+                if (r == c) {
+                    lo = cLo;
+                    hi = cHi;
+                } else if (r == cold) {
+                    lo = dLo;
+                    hi = dHi;
+                } else {
+                    const unsigned sc = nLc <= L - 2 ? bc : 0u, sd = nLd <= L - 2 ? bd : 0u;
+                    if (cLoHalf) lo = (lo & ~bc) | sc;
+                    else hi = (hi & ~bc) | sc;
+                    if (dLoHalf) lo = (lo & ~bd) | sd;
+                    else hi = (hi & ~bd) | sd;
+                }
+            };
+            if (hasA) retest(ra, loadA, loA, hiA);
+            if (hasB) retest(rb, loadB, loB, hiB);
+        }
         const int sv = (lane < S) ? slot[cold * S + lane] : 0;
         const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
         const unsigned freeb = __ballot_sync(kFull, lane < S && sv < 0);  // cold's free slots
@@ -359,12 +406,10 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
             uint64_t h2 = held ? hm : (hm | (1ull << cold));
             if (freed) h2 &= ~(1ull << c);
             holder[e] = h2;
-            Ls[c] = Lc - mv;
-            Ls[cold] = Lmin + mv;
         }
         if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
         if (freed) freem |= 1ull << c;
-        __syncwarp();  // the table and the load copy, for every lane's next reads
+        __syncwarp();  // the table, for every lane's next reads
         ++iters;
     }
 }
