@@ -220,6 +220,7 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
                                                        int flags, int& iters, int& status) {
     const bool skip = (flags & EP_PLAN_SKIP) != 0;
     const bool release = (flags & EP_PLAN_RELEASE) != 0;
+    const unsigned lt = lanemask_lt();
     const bool hasA = loadA >= 0, hasB = kTwo && loadB >= 0;
     const int ra = lane, rb = lane + 32;
     const uint64_t exist = (R >= 64) ? ~0ull : ((1ull << R) - 1ull);
@@ -330,8 +331,8 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
         const uint64_t hm = holder[e];
         const uint64_t el = (hm | freem) & exist & ~(1ull << c);
         if (el == 0ull) break;  // (base candidate only)
-        const bool elA = hasA && ((el >> ra) & 1ull);
-        const bool elB = hasB && ((el >> rb) & 1ull);
+        const bool elA = hasA && (((unsigned)el >> lane) & 1u);
+        const bool elB = hasB && (((unsigned)(el >> 32) >> lane) & 1u);
         int cold, Lmin;
         if (kPacked) {
             const unsigned ca = elA ? ((unsigned)loadA << 6) | (unsigned)ra : 0xffffffffu;
@@ -347,6 +348,12 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
             const unsigned b1 = kTwo ? __ballot_sync(kFull, elB && cb == Lmin) : 0u;
             cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
         }
+        // the table entries the move touches, read by their owner lanes (lane
+        // j: instance j of a rank) while the move is decided
+        const bool owner = lane < W, spare = owner && lane >= H;
+        const int qs = owner ? q[c * W + lane] : 0;      // c's instances
+        const int qc = owner ? q[cold * W + lane] : 0;   // cold's instances
+        const int sv = spare ? slot[cold * S + (lane - H)] : 0;  // cold's spare slots
         const int mv = min(qsrc, (Lc - Lmin) >> 1);
         if (mv <= 0) break;  // (base candidate only: a skip candidate always moves)
         if (iters == max_iters) {
@@ -385,28 +392,33 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
             if (hasA) retest(ra, loadA, loA, hiA);
             if (hasB) retest(rb, loadB, loB, hiB);
         }
-        const int sv = (lane < S) ? slot[cold * S + lane] : 0;
-        const unsigned hit = __ballot_sync(kFull, lane < S && sv == e);
-        const unsigned freeb = __ballot_sync(kFull, lane < S && sv < 0);  // cold's free slots
-        const bool held = (hm >> cold) & 1ull;
+        // cold holds e as a home expert or in a spare slot (lane j votes for
+        // instance j); else its lowest free slot takes e
+        const unsigned hit = __ballot_sync(kFull, spare && sv == e);
+        const unsigned freeb = __ballot_sync(kFull, spare && sv < 0);  // cold's free slots
         const int ej = e - cold * H;
         const bool home = (unsigned)ej < (unsigned)H;
+        const bool held = home || hit != 0u;
         const unsigned pick = held ? hit : freeb;
         if (!home && pick == 0u) {  // (never; keeps every index in range)
             status = EP_ERR_INVAL;
             break;
         }
-        const int dj = home ? ej : H + __ffs(pick) - 1;
+        // this lane is cold's instance: e's home, else the lowest lane of pick
+        const bool dst = home ? lane == ej : ((pick >> lane) & 1u) && (pick & lt) == 0u;
         const bool freed = release && src_j >= H && qsrc == mv;  // the source replica emptied
-        if (lane == 0) {
-            q[c * W + src_j] -= mv;
-            q[cold * W + dj] += mv;
-            if (!held) slot[cold * S + (dj - H)] = e;
-            if (freed) slot[c * S + (src_j - H)] = -1;
-            uint64_t h2 = held ? hm : (hm | (1ull << cold));
-            if (freed) h2 &= ~(1ull << c);
-            holder[e] = h2;
+        // owner-lane updates (c != cold, so no entry is written twice)
+        if (lane == src_j) {
+            q[c * W + lane] = qs - mv;
+            if (freed) slot[c * S + (lane - H)] = -1;
         }
+        if (dst) {
+            q[cold * W + lane] = qc + mv;
+            if (!held) slot[cold * S + (lane - H)] = e;
+        }
+        uint64_t h2 = held ? hm : (hm | (1ull << cold));
+        if (freed) h2 &= ~(1ull << c);
+        holder[e] = h2;  // every lane, the same value
         if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
         if (freed) freem |= 1ull << c;
         __syncwarp();  // the table, for every lane's next reads
