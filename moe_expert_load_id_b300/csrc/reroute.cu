@@ -434,14 +434,74 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
             for (int c2 = 0; c2 < cl; ++c2) lower += cluster.map_shared_rank(ctot, c2)[tid];
         cluster.sync();  // every read of a block's totals is done before any block moves on
     }
+    // phase B of the wide blocks, first half: for every (warp w, expert e) of
+    // the chunk, the rank of the warp's first slot of e (base[e] + the slots of
+    // e in warps below w).  The 32 lanes of a warp hold warps 0 .. 31 of one
+    // expert: an exclusive scan across them.  It needs only counts, so the
+    // first chunk's runs before the wait for the plan.
+    auto scan_b = [&]() {
+        constexpr int kEpp = kThreads / kWarps;  // experts per pass
+        const int wv = tid % kWarps, ei = tid / kWarps;
+        for (int eb = 0; eb < E; eb += kEpp) {  // same trip count in every lane
+            const int e = eb + ei;
+            const bool act = e < E;
+            const int c = act ? wx0[wv * Es + e] : 0;
+            const int b0 = act ? base[e] : 0;
+            int incl = c;
+#pragma unroll
+            for (int o = 1; o < kWarps; o <<= 1) {
+                const int y = __shfl_up_sync(kFull, incl, o, kWarps);
+                if (wv >= o) incl += y;
+            }
+            const int x0 = b0 + incl - c;
+            if (act) wx0[wv * Es + e] = x0;
+            __syncwarp();  // every lane of the group has read base[e]
+            if (act && wv == kWarps - 1) base[e] = x0 + c;
+        }
+    };
+    // ... second half (the plan): the row of that rank and how many ranks its
+    // instance holds from there, one independent search of e's list per lane
+    auto search_b = [&]() {
+        constexpr int kEpp = kThreads / kWarps;
+        const int wv = tid % kWarps, ei = tid / kWarps;
+        for (int eb = 0; eb < E; eb += kEpp) {
+            const int e = eb + ei;
+            if (e < E) {
+                const int x0 = wx0[wv * Es + e];
+                const int lo = ptr[e], end = ptr[e + 1];
+                const int m = upper_bound(bcum, lo, end, x0);
+                if (m < end) {
+                    wdb[wv * Es + e] = x0 + bdel[m];
+                    wlim[wv * El + e] = (uint16_t)min(bcum[m] - x0, 0xffff);
+                } else {
+                    wdb[wv * Es + e] = -1;
+                    wlim[wv * El + e] = 0;
+                }
+            }
+        }
+    };
+    constexpr bool kSplitB = kWarps == 32;
+    if constexpr (kSplitB) {
+        // want[] gets the prefix before base moves on; a block of a cluster
+        // starts at the slots of the blocks below it
+        __syncthreads();  // rank_prefix's adds and every warp's phase A
+        if (want != nullptr)
+            for (int e = tid; e < E; e += kThreads) want[e] += base[e];
+        if constexpr (kCl > 1) {
+            if (tid < E) base[tid] += lower;
+        }
+        __syncthreads();
+        if (s0 < s1) scan_b();
+    }
     if (early) pdl_wait();
     pdl_trigger();
 
-    // ---- prologue: plan tables (want[] gets the rank's whole count); a block
-    // of a cluster starts at the slots of the blocks below it
+    // ---- prologue: plan tables (want[] gets the rank's whole count, unless
+    // done above); a block of a cluster starts at the slots of the blocks
+    // below it
     plan_tables<kThreads>(E, P, M, inst, r, quota, inst_ptr, inst_id, inst_cum, inst_offset, off,
-                          ptr, bcum, bdel, base, want, warp_tot, cl == 0);
-    if constexpr (kCl > 1) {
+                          ptr, bcum, bdel, base, kSplitB ? nullptr : want, warp_tot, cl == 0);
+    if constexpr (kCl > 1 && !kSplitB) {
         if (tid < E) base[tid] += lower;  // (thread e alone touches base[e] here)
     }
     // (the barrier before phase B orders the writes above before any read of
@@ -459,46 +519,14 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
         }
         __syncthreads();
         if constexpr (kWarps == 32) {
-            // phase B: for every (warp w, expert e) of the chunk, the rank of the
-            // warp's first slot of e (base[e] + the slots of e in warps below w),
-            // the row of that rank and how many ranks its instance holds from
-            // there.  The 32 lanes of a warp hold warps 0 .. 31 of one expert:
-            // an exclusive scan across them, then one independent search of e's
-            // list per lane (measured 20.5 us per one-layer launch against 22.5
-            // for eight lanes per expert walking four warps each).  Narrow
-            // blocks, whose launches are issue-bound, keep the walk below (four
-            // times fewer searches: 379 us against 393 on a 94-layer batch).
-            {
-                constexpr int kEpp = kThreads / kWarps;  // experts per pass
-                const int wv = tid % kWarps, ei = tid / kWarps;
-                for (int eb = 0; eb < E; eb += kEpp) {  // same trip count in every lane
-                    const int e = eb + ei;
-                    const bool act = e < E;
-                    const int c = act ? wx0[wv * Es + e] : 0;
-                    const int b0 = act ? base[e] : 0;
-                    const int lo = act ? ptr[e] : 0, end = act ? ptr[e + 1] : 0;
-                    int incl = c;
-#pragma unroll
-                    for (int o = 1; o < kWarps; o <<= 1) {
-                        const int y = __shfl_up_sync(kFull, incl, o, kWarps);
-                        if (wv >= o) incl += y;
-                    }
-                    const int x0 = b0 + incl - c;
-                    if (act) {
-                        const int m = upper_bound(bcum, lo, end, x0);
-                        wx0[wv * Es + e] = x0;
-                        if (m < end) {
-                            wdb[wv * Es + e] = x0 + bdel[m];
-                            wlim[wv * El + e] = (uint16_t)min(bcum[m] - x0, 0xffff);
-                        } else {
-                            wdb[wv * Es + e] = -1;
-                            wlim[wv * El + e] = 0;
-                        }
-                    }
-                    __syncwarp();  // every lane of the group has read base[e]
-                    if (act && wv == kWarps - 1) base[e] = x0 + c;
-                }
-            }
+            // phase B (above): the scan over warps, then the search of each
+            // (warp, expert) entry (measured 20.5 us per one-layer launch
+            // against 22.5 for eight lanes per expert walking four warps each).
+            // Narrow blocks, whose launches are issue-bound, keep the walk
+            // below (four times fewer searches: 379 us against 393 on a
+            // 94-layer batch).  The first chunk's scan ran before the plan.
+            if (cs != s0) scan_b();
+            search_b();  // (each thread reads back the entries it scanned)
         } else {
             // experts per phase-B pass: G consecutive threads share one expert's warps
             int G = 1;
