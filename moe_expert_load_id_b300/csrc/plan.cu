@@ -60,8 +60,9 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
         int32_t* csum0 = reinterpret_cast<int32_t*>(smem + wbytes - align16((size_t)E * 4));
         const int g0 = blockIdx.x * kPlanWarps;
         const int nb = min(kPlanWarps, n_inst - g0);
+        const float invE = 1.0f / (float)E;
         for (int x = threadIdx.x; x < kPlanWarps * E; x += kPlanWarps * 32) {
-            const int w = x / E;
+            const int w = small_div(x, invE);
             csum0[w * (wbytes / 4) + (x - w * E)] = 0;
         }
         __syncthreads();
@@ -74,9 +75,10 @@ plan_kernel(const int32_t* __restrict__ counts, int n_inst, int R, int E, int S,
         if ((E & 3) == 0 && (reinterpret_cast<uintptr_t>(counts_src) & 15u) == 0) {
             const int Q = E >> 2;
             const int G = max(1, kThr / Q);
+            const float invQG = 1.0f / (float)(Q * G), invQ = 1.0f / (float)Q;
             for (int x = threadIdx.x; x < nb * Q * G; x += kThr) {
-                const int wi = x / (Q * G), rem = x - wi * Q * G;
-                const int rg = rem / Q, c = rem - rg * Q;
+                const int wi = small_div(x, invQG), rem = x - wi * Q * G;
+                const int rg = small_div(rem, invQ), c = rem - rg * Q;
                 const int4* cs =
                     reinterpret_cast<const int4*>(counts_src + (int64_t)(g0 + wi) * R * E) + c;
                 int4 t = make_int4(0, 0, 0, 0);

@@ -21,6 +21,17 @@ constexpr long long kQPackLimit = 1ll << 21; // ... and quotas fit a 10-bit-shif
 
 __host__ __device__ inline size_t align16(size_t x) { return (x + 15) & ~size_t(15); }
 
+// floor(x / d) for 0 <= x < 2^21 and d >= 1, given inv_d = 1.0f / d (rounded
+// to nearest, computed once by the caller).  (x + 1/2) / d lies at least
+// 1 / (2d) away from every integer, and the two roundings in (x + 1/2) * inv_d
+// change it by at most (x + 1/2) / d * 2^-22 < 1 / (2d), so truncation gives
+// the exact quotient.  The planner's indices (instances, experts, slots) are
+// far below 2^21; an integer division by a run-time value is a long
+// instruction sequence, and these sit on the per-layer critical path.
+__device__ __forceinline__ int small_div(int x, float inv_d) {
+    return (int)(((float)x + 0.5f) * inv_d);
+}
+
 // One warp's shared memory: q[P], slot[R*S], holder[E] (the table), the CSR
 // epilogue's scratch pos[E+1] and val[E+R*S], a copy of the loads Ls[64] (the
 // rule variants), and the instance's counts[E] when the planner sums them
@@ -453,12 +464,13 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
                                                  int32_t* Ls, int lane, int32_t* qo, int32_t* so,
                                                  int32_t* lo, int& iters, int& status) {
     const int H = E / R, W = H + S, P = R * W;
+    const float invW = 1.0f / (float)W, invH = 1.0f / (float)H;
     for (int p = lane; p < P; p += 32) {
-        const int r = p / W, j = p - r * W;
+        const int r = small_div(p, invW), j = p - r * W;
         q[p] = j < H ? cnt[r * H + j] : 0;
     }
     for (int x = lane; x < R * S; x += 32) slot[x] = -1;
-    for (int e = lane; e < E; e += 32) holder[e] = 1ull << (e / H);
+    for (int e = lane; e < E; e += 32) holder[e] = 1ull << small_div(e, invH);
     int loadA = -1, loadB = -1;
     if (lane < R) {
         unsigned sum = 0;
@@ -518,6 +530,7 @@ __device__ __forceinline__ void plan_csr_block(const int32_t* q, const int32_t* 
     constexpr int kWarps = kThreads / 32;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int H = E / R, W = H + S;
+    const float invH = 1.0f / (float)H, invS = 1.0f / (float)max(S, 1);
     // thread t: experts [t*per, (t+1)*per)
     const int per = (E + kThreads - 1) / kThreads;
     const int e0 = min(E, tid * per), e1 = min(E, e0 + per);
@@ -542,7 +555,7 @@ __device__ __forceinline__ void plan_csr_block(const int32_t* q, const int32_t* 
     for (int e = e0; e < e1; ++e) {
         pos[e] = run;
         po[e] = run;
-        const int home = e / H;
+        const int home = small_div(e, invH);
         const int hp = home * W + (e - home * H);  // the home instance heads the list
         io[run] = hp;
         val[run] = q[hp] | INT_MIN;  // a list's first entry
@@ -557,8 +570,8 @@ __device__ __forceinline__ void plan_csr_block(const int32_t* q, const int32_t* 
     for (int xs = tid; xs < R * S; xs += kThreads) {
         const int e = slot[xs];
         if (e < 0) continue;
-        const int c = xs / S, sl = xs - c * S;
-        const uint64_t lower = holder[e] & ~(1ull << (e / H)) & ((1ull << c) - 1ull);
+        const int c = small_div(xs, invS), sl = xs - c * S;
+        const uint64_t lower = holder[e] & ~(1ull << small_div(e, invH)) & ((1ull << c) - 1ull);
         const int m = pos[e] + 1 + __popcll(lower);
         const int p = c * W + H + sl;
         io[m] = p;
