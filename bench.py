@@ -933,7 +933,10 @@ def main():
     ap.add_argument("--layers", type=int, default=0, help="override the number of layers")
     ap.add_argument("--hidden", type=int, default=0,
                     help="override the hidden size (small cases for profiler captures)")
-    ap.add_argument("--e2e-steps", type=int, default=3)
+    # e2e timed steps: every step's inputs are copied in inside the timed
+    # region, and the first step's first half (~1.3 GB on the Qwen3-235B-like
+    # workload) cannot overlap anything, so the steps amortise that fill
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-layers", type=int, default=2)
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--stress-sweep", action="store_true",
