@@ -67,10 +67,15 @@ __host__ __device__ inline int count_cols(int E) {
     return C;
 }
 
-__host__ __device__ inline size_t count_smem_bytes(int E) {
+// the histogram table, reused by the last block's reduction as [G][E] partial
+// sums (G * E = 4 * threads with int4 columns)
+__host__ __device__ inline int count_hist_words(int E) {
     const int C = count_cols(E);
-    const int h = E * C > kCountThreads ? E * C : kCountThreads;
-    return sizeof(int32_t) * ((size_t)h + E);
+    return E * C > 4 * kCountThreads ? E * C : 4 * kCountThreads;
+}
+
+__host__ __device__ inline size_t count_smem_bytes(int E) {
+    return sizeof(int32_t) * ((size_t)count_hist_words(E) + E);
 }
 
 // 16-byte id load: streaming (evict-first), or (EP_COUNT_LOAD_HINT = 1)
@@ -105,8 +110,8 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     __shared__ int bad;
     __shared__ int is_last;
     const int C = count_cols(E);
-    int32_t* hist = sh;                                            // [E][C], later scratch
-    int32_t* blk = sh + (E * C > kCountThreads ? E * C : kCountThreads);  // [E] rank total
+    int32_t* hist = sh;                          // [E][C], later scratch
+    int32_t* blk = sh + count_hist_words(E);     // [E] rank total
 
     // A dependent planner (ep_balance) may launch now; it waits for this grid.
     pdl_trigger();
@@ -215,22 +220,54 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     __syncthreads();
     if (!is_last) return;
     const int32_t* cs = counts_src + (int64_t)inst * R * E;
-    if (E <= kCountThreads) {
-        // thread (g, e) sums rows g, g+G, ... of column e, G = threads / E;
-        // loads are issued eight at a time
+    constexpr int kU = 16;  // loads in flight per thread: 64 rows of E <= 256 in one round
+    if ((E & 3) == 0 && (E >> 2) <= kCountThreads && (reinterpret_cast<uintptr_t>(cs) & 15u) == 0) {
+        // thread (g, c) sums the int4 column c (experts 4c .. 4c+3) over rows
+        // g, g+G, ... (G = threads / (E/4)); the partials meet in hist[G][E]
+        const int Q = E >> 2;
+        const int G = kCountThreads / Q;
+        const int c = tid % Q, g = tid / Q;
+        if (g < G) {
+            const int4* col = reinterpret_cast<const int4*>(cs) + c;
+            int4 t = make_int4(0, 0, 0, 0);
+            for (int r0 = g; r0 < R; r0 += kU * G) {
+                int4 v[kU];
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int rr = r0 + u * G;
+                    v[u] = (rr < R) ? __ldcg(col + (int64_t)rr * Q) : make_int4(0, 0, 0, 0);
+                }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    t.x += v[u].x;
+                    t.y += v[u].y;
+                    t.z += v[u].z;
+                    t.w += v[u].w;
+                }
+            }
+            reinterpret_cast<int4*>(hist)[g * Q + c] = t;
+        }
+        __syncthreads();
+        for (int e = tid; e < E; e += kCountThreads) {
+            int sum = 0;
+            for (int gg = 0; gg < G; ++gg) sum += hist[gg * E + e];
+            counts[(int64_t)inst * E + e] = sum;
+        }
+    } else if (E <= kCountThreads) {
+        // thread (g, e) sums rows g, g+G, ... of column e, G = threads / E
         const int G = kCountThreads / E;
         const int e = tid % E, g = tid / E;
         int t = 0;
         if (g < G) {
-            for (int r0 = g; r0 < R; r0 += 8 * G) {
-                int v[8];
+            for (int r0 = g; r0 < R; r0 += kU * G) {
+                int v[kU];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) {
+                for (int u = 0; u < kU; ++u) {
                     const int rr = r0 + u * G;
                     v[u] = (rr < R) ? __ldcg(cs + (int64_t)rr * E + e) : 0;
                 }
 #pragma unroll
-                for (int u = 0; u < 8; ++u) t += v[u];
+                for (int u = 0; u < kU; ++u) t += v[u];
             }
             hist[g * E + e] = t;
         }
@@ -243,13 +280,13 @@ count_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, in
     } else {
         for (int e = tid; e < E; e += kCountThreads) {
             int t = 0;
-            for (int r0 = 0; r0 < R; r0 += 8) {
-                int v[8];
+            for (int r0 = 0; r0 < R; r0 += kU) {
+                int v[kU];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
+                for (int u = 0; u < kU; ++u)
                     v[u] = (r0 + u < R) ? __ldcg(cs + (int64_t)(r0 + u) * E + e) : 0;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) t += v[u];
+                for (int u = 0; u < kU; ++u) t += v[u];
             }
             counts[(int64_t)inst * E + e] = t;
         }
