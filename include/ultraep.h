@@ -249,9 +249,10 @@ ep_status_t ep_reroute(const ep_domain_t *dom, const int32_t *topk_ids, int64_t 
  * still running and waits on the device for its per-source-rank counts, which
  * it sums into counts itself (the count kernel stops at counts_src); the
  * reroute launches while the planner is still running, loads and ranks its
- * first chunk of ids (which depend on nothing the planner computes) and only
- * then waits for the plan.  Results are exactly those of the three separate
- * calls.
+ * first chunk of ids and reads counts_src (neither depends on anything the
+ * planner computes: the count grid completed before the planner let the
+ * reroute launch) and only then waits for the plan.  Results are exactly
+ * those of the three separate calls.
  *
  *   topk_ids, T, n_inst, max_iters, dev_status   as for ep_count / ep_plan
  *   workspace   as for ep_count (ep_count_workspace_bytes() bytes)
