@@ -129,14 +129,15 @@ __device__ __forceinline__ int upper_bound(const int32_t* a, int lo, int hi, int
 // base must be zero, and a block barrier passed, before the call.  With E a
 // multiple of 4 and the rows 16-byte aligned, thread (g, q) sums the int4
 // column q (experts 4q .. 4q+3) over rows g, g+G, ... < r (G = threads /
-// (E/4)), 2048 / threads loads in flight (every row of 64 ranks at E = 128 in
-// one round); otherwise thread (g, e) sums column e the same way (G =
-// threads / E).  The partial sums meet in base[] by atomics.
+// (E/4)), 2048 / threads loads in flight, at most 8 (every row of 64 ranks at
+// E = 128 in one round for 256 threads and more); otherwise thread (g, e)
+// sums column e the same way (G = threads / E).  The partial sums meet in
+// base[] by atomics.
 template <int kThreads>
 __device__ __forceinline__ void rank_prefix(int R, int E, int inst, int r,
                                             const int32_t* __restrict__ counts_src,
                                             int32_t* base, int32_t* want) {
-    constexpr int kU = 2048 / kThreads > 1 ? 2048 / kThreads : 1;
+    constexpr int kU = 2048 / kThreads > 8 ? 8 : (2048 / kThreads > 1 ? 2048 / kThreads : 1);
     const int tid = threadIdx.x;
     const int32_t* own = counts_src + ((int64_t)inst * R + r) * E;
     if (want != nullptr)
@@ -219,11 +220,19 @@ __device__ __forceinline__ void plan_tables(int E, int P, int M, int inst, int r
     // every load of the plan's outputs is independent of the others, so the
     // prologue waits for memory once: the list entries are loaded whole and
     // the used length applied afterwards
-    int qv[kIpt];
+    // the quotas: in registers (kIpt per thread) for wide blocks; narrow
+    // blocks, whose kIpt registers would spill, stage them in off[] and scan
+    // a contiguous run of them per thread
+    constexpr bool kQReg = kIpt <= 4;
+    int qv[kQReg ? kIpt : 1];
+    if constexpr (kQReg) {
 #pragma unroll
-    for (int u = 0; u < kIpt; ++u) {
-        const int p = tid * kIpt + u;
-        qv[u] = (p < P) ? qg[p] : 0;
+        for (int u = 0; u < kIpt; ++u) {
+            const int p = tid * kIpt + u;
+            qv[u] = (p < P) ? qg[p] : 0;
+        }
+    } else {
+        for (int p = tid; p < P; p += kThreads) off[p] = qg[p];
     }
     const int nM = min(max(pg[E], 0), M);
     const int xn = max(E + 1, M);
@@ -241,8 +250,17 @@ __device__ __forceinline__ void plan_tables(int E, int P, int M, int inst, int r
         }
     }
     int qlocal = 0;
+    int sb = 0, se = 0;  // (narrow blocks) this thread's run of quotas
+    if constexpr (kQReg) {
 #pragma unroll
-    for (int u = 0; u < kIpt; ++u) qlocal += qv[u];
+        for (int u = 0; u < kIpt; ++u) qlocal += qv[u];
+    } else {
+        __syncthreads();
+        const int seg = (P + kThreads - 1) / kThreads;
+        sb = min(P, tid * seg);
+        se = min(P, sb + seg);
+        for (int p = sb; p < se; ++p) qlocal += off[p];
+    }
     // inst_offset: exclusive prefix of quota over p
     int qx = qlocal;
 #pragma unroll
@@ -264,11 +282,19 @@ __device__ __forceinline__ void plan_tables(int E, int P, int M, int inst, int r
     __syncthreads();
     {
         int run = qx - qlocal + (warp > 0 ? warp_tot[warp - 1] : 0);
+        if constexpr (kQReg) {
 #pragma unroll
-        for (int u = 0; u < kIpt; ++u) {
-            const int p = tid * kIpt + u;
-            if (p < P) off[p] = run;
-            run += qv[u];
+            for (int u = 0; u < kIpt; ++u) {
+                const int p = tid * kIpt + u;
+                if (p < P) off[p] = run;
+                run += qv[u];
+            }
+        } else {
+            for (int p = sb; p < se; ++p) {  // (in place: each thread its own run)
+                const int v = off[p];
+                off[p] = run;
+                run += v;
+            }
         }
         if (tid == kThreads - 1) off[P] = warp_tot[kWarps - 1];
     }
@@ -666,7 +692,7 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 
 // ---------------------------------------------------------------- quad kernel
 // Batched launches with k a multiple of 4 and 16-byte aligned ids and rows:
-// one warp per (instance, source rank), eight consecutive source ranks of one
+// one warp per (instance, source rank), four consecutive source ranks of one
 // instance per block.  A warp walks its rank's slots in steps of 128: lane l
 // holds the 16-byte group of slots 4l .. 4l+3 of the step, four of one
 // token's top-k ids, which a top-k gate makes distinct.  So a lane adds at
@@ -693,7 +719,16 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 // discarded.  A step in which some lane's four valid ids are not distinct (no
 // top-k gate produces those) is ranked slot by slot instead: four sub-steps
 // of 32 consecutive slots on the same tables.
-constexpr int kQuadWarps = 8;
+// Four source ranks (warps) per block at eight blocks per SM: the SM's
+// shared-memory pipe is the bound, so a block's time grows with the blocks
+// sharing its SM, and the launch ends with the most loaded SM.  Smaller blocks
+// spread the ranks more evenly (measured on 94 / 58 / 89-layer batches: 244 /
+// 185 / 301 us against 252 / 196 / 334 with eight ranks per block at four
+// blocks per SM; two ranks per block at sixteen: 248 / 216 / 298).
+#ifndef EP_REROUTE_QUAD_WARPS
+#define EP_REROUTE_QUAD_WARPS 4  // build-time tunable
+#endif
+constexpr int kQuadWarps = EP_REROUTE_QUAD_WARPS;
 constexpr int kQuadThreads = kQuadWarps * 32;
 constexpr int kQuadAhead = 3;  // steps of ids loaded ahead of the one being ranked
 constexpr unsigned kCross = 0x80000000u;  // hot[e].y: e's ranks here may cross a boundary
@@ -702,7 +737,7 @@ constexpr unsigned kCross = 0x80000000u;  // hot[e].y: e's ranks here may cross 
                                         // quad kernel is used (build-time tunable)
 #endif
 #ifndef EP_REROUTE_QUAD_BLOCKS_PER_SM
-#define EP_REROUTE_QUAD_BLOCKS_PER_SM 4  // build-time tunable
+#define EP_REROUTE_QUAD_BLOCKS_PER_SM 8  // build-time tunable
 #endif
 
 struct QuadLayout {
