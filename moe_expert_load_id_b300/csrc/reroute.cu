@@ -33,6 +33,13 @@
 // launches; dst_row is written with coalesced streaming stores; the optional
 // src_slot inverse is a scattered store.
 //
+// Three kernels compute these rows and the launcher picks one by shape (see
+// launch_reroute): the quad kernel for batched launches (one warp per source
+// rank, four ranks per block, four slots per lane per step); the mask-table
+// kernel above in 1024-thread blocks for one-layer launches, a source rank
+// split over a thread-block cluster of two or four blocks when they fit; and
+// the same kernel in 256-thread blocks for everything else.
+//
 // (A design with lane-private counters, each lane owning a contiguous run of
 // slots, two shared-memory atomics per slot and one warp scan per expert
 // pair, was slower in every configuration measured, also with a path free of
