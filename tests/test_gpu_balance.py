@@ -46,6 +46,9 @@ CASES = [
     ("T_below_R",      8,  2, 1, 3,  5,     1,      False),
     ("R1",             1,  4, 1, 2,  500,   1,      False),
     ("W32",            8,  1, 31, 4, 3000,  2,      False),
+    ("empty_T",        8,  4, 1, 4,  0,     2,      False),   # no slots: home placement
+    ("k1",             8,  4, 1, 1,  777,   1,      False),
+    ("glm_like_layer", 40, 4, 1, 8,  163840, 1,     False),   # 32768 slots per rank, clusters of 2
 ]
 
 
