@@ -699,43 +699,54 @@ reroute_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, int E, 
 
 // ---------------------------------------------------------------- quad kernel
 // Batched launches with k a multiple of 4 and 16-byte aligned ids and rows:
-// one warp per (instance, source rank), four consecutive source ranks of one
-// instance per block.  A warp walks its rank's slots in steps of 128: lane l
-// holds the 16-byte group of slots 4l .. 4l+3 of the step, four of one
-// token's top-k ids, which a top-k gate makes distinct.  So a lane adds at
-// most one bit to any expert's lane mask, and one OR per slot, one warp
-// barrier and one 8-byte read per slot give every slot its place among the
-// step's slots of its expert (the lanes below holding the same expert); the
-// group's lowest lane then advances the expert's next row.
+// two warps per (instance, source rank), consecutive source ranks of one
+// instance per block.  A warp walks slots in steps of 128: lane l holds the
+// 16-byte group of slots 4l .. 4l+3 of the step, four of one token's top-k
+// ids, which a top-k gate makes distinct.  So a lane adds at most one bit to
+// any expert's lane mask, and one OR per slot, one warp barrier and one
+// 8-byte read per slot give every slot its place among the step's slots of
+// its expert (the lanes below, or above, holding the same expert); one lane
+// of the group then moves the expert's entry on.
 //
-// Each expert has two entries in the warp's tables:
-//   hot[e]  = {lane mask of the step, the row of e's next slot}
-//   cold[e] = {the row just past the current instance of e, row - rank there}
-// A slot's row is hot[e].row + (lanes below in its group).  Only a group that
-// runs past its instance (a replica boundary, or the expert's quotas used up)
-// takes the slow path: its slots search the expert's instance list and the
-// leader moves both entries on.  The top bit of hot[e].row marks the experts
-// whose ranks in this warp (by counts_src) reach a boundary at all; only their
-// leaders read cold[e] (rows are below 2^31, so the bit is free).  The rows start at the prefix of counts_src
-// over earlier source ranks (mapped through the plan), so no scan over warps
-// or chunks is needed; at the end the rank a warp reached must be that
-// prefix plus its own counts_src row, one compare per expert.
+// The two warps of a source rank split its steps and need nothing from each
+// other.  The forward warp walks the first half in slot order from the
+// prefix of counts_src over the earlier source ranks, the group's lowest lane
+// advancing the expert's next rank.  The backward warp walks the second half
+// in reverse from the prefix over the ranks up to and including this one: a
+// slot's rank is the expert's top rank still free minus one minus the lanes
+// above it in its group, and the group's highest lane lowers that top.  Each
+// rank thus goes to the slot the stable order gives it.  Where the two walks
+// meet, each expert's next forward rank must equal the lowest backward rank:
+// that one compare per expert is the check of counts_src.
+//
+// Each expert has two entries in a warp's tables:
+//   hot[e]  = {lane mask of the step, the row of e's next slot; backward, one
+//              past it}
+//   cold[e] = {the row just past e's current instance (backward: that
+//              instance's first row), row - rank there}
+// A slot's row is hot[e].row plus (forward) or minus one minus (backward) the
+// lanes before it in its group.  Only a group that runs past its instance (a
+// replica boundary, or the expert's quotas used up) takes the slow path: its
+// slots search the expert's instance list and the group's last lane moves both
+// entries on.  The top bit of hot[e].row marks the experts whose ranks on
+// this source rank (by counts_src) reach a boundary at all; only their groups
+// read cold[e] (rows are below 2^31, so the bit is free).
 //
 // Ids outside [0, E), and the slots past the end of a rank, use four spare
 // entries E .. E+3 (one per position in the lane's group), whose rows are
 // discarded.  A step in which some lane's four valid ids are not distinct (no
 // top-k gate produces those) is ranked slot by slot instead: four sub-steps
 // of 32 consecutive slots on the same tables.
-// Four source ranks (warps) per block at eight blocks per SM: the SM's
-// shared-memory pipe is the bound, so a block's time grows with the blocks
-// sharing its SM, and the launch ends with the most loaded SM.  Smaller blocks
-// spread the ranks more evenly (measured on 94 / 58 / 89-layer batches: 244 /
-// 185 / 301 us against 252 / 196 / 334 with eight ranks per block at four
-// blocks per SM; two ranks per block at sixteen: 248 / 216 / 298).
+// The SM's shared-memory pipe is the bound, so a block's time grows with the
+// blocks sharing its SM, and the launch ends with the most loaded SM: two
+// warps per source rank halve the unit of work, so the last wave of blocks
+// is a smaller part of the launch.
 #ifndef EP_REROUTE_QUAD_WARPS
-#define EP_REROUTE_QUAD_WARPS 4  // build-time tunable
+#define EP_REROUTE_QUAD_WARPS 4  // build-time tunable (even)
 #endif
 constexpr int kQuadWarps = EP_REROUTE_QUAD_WARPS;
+static_assert(kQuadWarps % 2 == 0, "two warps per source rank");
+constexpr int kQuadRanks = kQuadWarps / 2;
 constexpr int kQuadThreads = kQuadWarps * 32;
 constexpr int kQuadAhead = 3;  // steps of ids loaded ahead of the one being ranked
 constexpr unsigned kCross = 0x80000000u;  // hot[e].y: e's ranks here may cross a boundary
@@ -749,9 +760,9 @@ constexpr unsigned kCross = 0x80000000u;  // hot[e].y: e's ranks here may cross 
 
 struct QuadLayout {
     int P, M;
-    size_t pre_off;  // [kQuadWarps + 1][E] int32: prefix of counts_src for each warp's rank
+    size_t pre_off;  // [kQuadRanks + 1][E] int32: prefix of counts_src for each rank
     size_t hot_off;  // [kQuadWarps][E + 4] uint2 {mask, next row}
-    size_t cold_off; // [kQuadWarps][E + 4] int2 {end row, row - rank}
+    size_t cold_off; // [kQuadWarps][E + 4] int2 {instance bound row, row - rank}
     size_t bytes;
 };
 
@@ -761,10 +772,16 @@ __host__ __device__ inline QuadLayout quad_layout(int R, int E, int S) {
     l.M = E + R * S;
     // int32: off[P+1] ptr[E+1] bcum[M] bdel[M] base[E]
     l.pre_off = sizeof(int32_t) * ((size_t)(l.P + 1) + (E + 1) + 2 * (size_t)l.M + E);
-    l.hot_off = (l.pre_off + sizeof(int32_t) * (size_t)(kQuadWarps + 1) * E + 15) & ~(size_t)15;
+    l.hot_off = (l.pre_off + sizeof(int32_t) * (size_t)(kQuadRanks + 1) * E + 15) & ~(size_t)15;
     l.cold_off = l.hot_off + sizeof(uint2) * (size_t)kQuadWarps * (E + 4);
     l.bytes = l.cold_off + sizeof(int2) * (size_t)kQuadWarps * (E + 4);
     return l;
+}
+
+__device__ __forceinline__ unsigned lanemask_gt() {
+    unsigned m;
+    asm volatile("mov.u32 %0, %%lanemask_gt;" : "=r"(m));
+    return m;
 }
 
 __global__ void __launch_bounds__(kQuadThreads, EP_REROUTE_QUAD_BLOCKS_PER_SM)
@@ -789,12 +806,14 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
     int2* colds = reinterpret_cast<int2*>(reinterpret_cast<unsigned char*>(sm) + lay.cold_off);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int gpi = (R + kQuadWarps - 1) / kQuadWarps;  // blocks per instance
+    const int gpi = (R + kQuadRanks - 1) / kQuadRanks;  // blocks per instance
     const int inst = blockIdx.x / gpi;
-    const int r0 = (blockIdx.x - inst * gpi) * kQuadWarps;
-    const int r = r0 + warp;
+    const int r0 = (blockIdx.x - inst * gpi) * kQuadRanks;
+    const int j = warp >> 1;               // the warp's source rank within the block
+    const bool back = (warp & 1) != 0;     // the backward walk of that rank
+    const int r = r0 + j;
     const bool has_rank = r < R;
-    const int nr = min(kQuadWarps, R - r0);  // ranks of this block
+    const int nr = min(kQuadRanks, R - r0);  // ranks of this block
 
     // this warp's slots: source rank r (T*k < 2^31, so 32-bit offsets)
     const int Tr = ((int)T + R - 1) / R;
@@ -803,20 +822,24 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
     const int s1 = has_rank ? (int)min(T, (int64_t)(r + 1) * Tr) * k : 0;
     const int L = s1 - s0;  // a multiple of 4
     const int nsteps = (L + 127) >> 7;
+    const int half = (nsteps + 1) >> 1;  // steps [0, half) forward, [half, nsteps) backward
+    const int nmine = back ? nsteps - half : half;
     const int32_t* idw = ids + (int64_t)inst * N + s0;
     int32_t* dsw = dst_row + (int64_t)inst * N + s0;
     int32_t* srci = src_slot ? src_slot + (int64_t)inst * N : nullptr;
-    auto load_step = [&](int st) -> int4 {
-        const int sl = (st << 7) + (lane << 2);
-        return (st < nsteps && sl < L) ? __ldcs(reinterpret_cast<const int4*>(idw + sl))
-                                       : make_int4(-1, -1, -1, -1);
+    // the warp's i-th step, and its ids
+    auto step_of = [&](int i) { return back ? nsteps - 1 - i : i; };
+    auto load_step = [&](int i) -> int4 {
+        const int sl = (step_of(i) << 7) + (lane << 2);
+        return (i < nmine && sl < L) ? __ldcs(reinterpret_cast<const int4*>(idw + sl))
+                                     : make_int4(-1, -1, -1, -1);
     };
     // the first steps' ids depend only on the call's input: in ep_balance they
     // are in flight while the planner finishes
     if (!early) pdl_wait();
     int4 buf[kQuadAhead];
 #pragma unroll
-    for (int j = 0; j < kQuadAhead; ++j) buf[j] = load_step(j);
+    for (int a = 0; a < kQuadAhead; ++a) buf[a] = load_step(a);
     if (tid == 0) flags = 0;
     for (int e = tid; e < E; e += kQuadThreads) base[e] = 0;
     __syncthreads();
@@ -826,7 +849,7 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
     rank_prefix<kQuadThreads>(R, E, inst, r0, counts_src, base, nullptr);
     {
         const int32_t* cs = counts_src + ((int64_t)inst * R + r0) * E;
-        for (int x = tid; x < kQuadWarps * E; x += kQuadThreads) {
+        for (int x = tid; x < kQuadRanks * E; x += kQuadThreads) {
             const int w = x / E, e = x - w * E;
             pre[(w + 1) * E + e] = (w < nr) ? __ldg(cs + (int64_t)w * E + e) : 0;
         }
@@ -834,7 +857,7 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
     if (early) pdl_wait();
     pdl_trigger();
 
-    // ---- prologue: plan tables, then each warp's prefix over source ranks
+    // ---- prologue: plan tables, then each rank's prefix over source ranks
     plan_tables<kQuadThreads>(E, P, M, inst, r0, quota, inst_ptr, inst_id, inst_cum, inst_offset,
                               off, ptr, bcum, bdel, base, nullptr, warp_tot);
     __syncthreads();
@@ -842,180 +865,242 @@ reroute_quad_kernel(const int32_t* __restrict__ ids, int64_t T, int k, int R, in
         int run = base[e];
         pre[e] = run;
 #pragma unroll
-        for (int w = 1; w <= kQuadWarps; ++w) {
+        for (int w = 1; w <= kQuadRanks; ++w) {
             run += pre[w * E + e];
             pre[w * E + e] = run;
         }
     }
     __syncthreads();
+    uint2* hot = hots + (size_t)warp * (E + 4);
+    int2* cold = colds + (size_t)warp * (E + 4);
     int my_flags = 0;
+    // backward: the entries for "the next rank to give is x - 1": the row one
+    // past it and its instance's first row; with no such instance (x - 1 past
+    // the quotas, or x <= 0) every later slot of e searches.  Returns the
+    // instance's first rank (INT_MAX when none).
+    auto back_entry = [&](int e, int x, unsigned& y, int2& c) -> int {
+        const int b = ptr[e], end = ptr[e + 1];
+        if (x > 0) {
+            const int m = upper_bound(bcum, b, end, x - 1);
+            if (m < end) {
+                const int lo = (m > b) ? max(bcum[m - 1], 0) : 0;
+                const int nd = bdel[m];
+                y = (unsigned)(x + nd);
+                c = make_int2(lo + nd, nd);
+                return lo;
+            }
+        }
+        y = (unsigned)x;
+        c = make_int2(INT_MAX, 0);
+        return INT_MAX;
+    };
     if (has_rank) {
-        // ---- the warp's tables: each expert's next row (its prefix mapped
-        // through the plan) and the end of that row's instance
-        uint2* hot = hots + (size_t)warp * (E + 4);
-        int2* cold = colds + (size_t)warp * (E + 4);
-        const int32_t* mypre = pre + warp * E;
+        // ---- the warp's tables: each expert's first row (its prefix mapped
+        // through the plan) and the bound of that row's instance
+        const int32_t* lo_pre = pre + j * E;
+        const int32_t* hi_pre = pre + (j + 1) * E;
         for (int e = lane; e < E + 4; e += 32) {
             if (e < E) {
-                const int x = mypre[e];
-                const int end = ptr[e + 1];
-                const int m = upper_bound(bcum, ptr[e], end, x);
-                const int del = (m < end) ? bdel[m] : 0;  // quotas used up: every rank overflows
-                // the warp's ranks of e, by counts_src, all inside this
-                // instance: the leaders of e never look at cold[e]
-                const int own = mypre[E + e] - x;
-                const bool may_cross = m >= end || x + own > bcum[m];
-                hot[e] = make_uint2(0u, (unsigned)(x + del) | (may_cross ? kCross : 0u));
-                cold[e] = make_int2((m < end) ? bcum[m] + del : x, del);
+                const int lo = lo_pre[e], hi = hi_pre[e];
+                if (!back) {
+                    const int end = ptr[e + 1];
+                    const int m = upper_bound(bcum, ptr[e], end, lo);
+                    const int del = (m < end) ? bdel[m] : 0;  // quotas used up: every rank overflows
+                    // the rank's ranks of e, by counts_src, all inside this
+                    // instance: no group of e ever looks at cold[e]
+                    const bool may_cross = m >= end || hi > bcum[m];
+                    hot[e] = make_uint2(0u, (unsigned)(lo + del) | (may_cross ? kCross : 0u));
+                    cold[e] = make_int2((m < end) ? bcum[m] + del : lo, del);
+                } else {
+                    unsigned y;
+                    int2 c;
+                    const int first = back_entry(e, hi, y, c);
+                    hot[e] = make_uint2(0u, y | (first > lo ? kCross : 0u));
+                    cold[e] = c;
+                }
             } else {
                 hot[e] = make_uint2(0u, 0u);
-                cold[e] = make_int2(INT_MAX, 0);  // spare entries never cross
+                cold[e] = make_int2(back ? INT_MIN : INT_MAX, 0);  // spare entries never cross
             }
         }
         __syncwarp();
-        const unsigned lt = lanemask_lt(), bit = 1u << lane;
+        const unsigned bit = 1u << lane;
         uint32_t* hotw = reinterpret_cast<uint32_t*>(hot);
         // rank x of expert e past its entry: search e's instance list
         auto search = [&](int e, int x) -> int {
+            if (x < 0) return -1;  // (backward, counts_src short of the ids)
             const int end = ptr[e + 1];
             const int m = upper_bound(bcum, ptr[e], end, x);
             if (m < end) return x + bdel[m];
             my_flags |= EP_DEV_QUOTA_OVERFLOW;
             return -1;
         };
-        // the leader of a group that reached the end of its instance moves
-        // e's entries to the instance of its next row (rank = row - del)
-        auto advance = [&](int e, int next_row, int del) {
-            const int x = next_row - del;
-            const int end = ptr[e + 1];
-            const int m = upper_bound(bcum, ptr[e], end, x);
-            const int nd = (m < end) ? bdel[m] : 0;
-            hot[e].y = (unsigned)(x + nd) | kCross;
-            cold[e] = make_int2((m < end) ? bcum[m] + nd : x, nd);
-        };
-        // a step whose lanes hold a repeated id: four sub-steps of 32
-        // consecutive slots, one slot per lane, in slot order
-        auto step_by_slot = [&](int4 q, int st) {
-#pragma unroll 1
-            for (int a = 0; a < 4; ++a) {
-                const int srcl = (a << 3) + (lane >> 2), c = lane & 3;
-                const int qx = __shfl_sync(kFull, q.x, srcl), qy = __shfl_sync(kFull, q.y, srcl);
-                const int qz = __shfl_sync(kFull, q.z, srcl), qw = __shfl_sync(kFull, q.w, srcl);
-                const int id = c == 0 ? qx : c == 1 ? qy : c == 2 ? qz : qw;
-                const int sl = (st << 7) + (a << 5) + lane;
-                const bool v = (unsigned)id < (unsigned)E;
-                const int e = v ? id : E;
-                atomicOr(&hotw[2 * e], bit);
-                __syncwarp();
-                const uint2 h = hot[e];
-                const int2 cd = cold[e];
-                const unsigned below = h.x & lt;
-                int row = (int)(h.y & ~kCross) + __popc(below);
-                const int nr = (int)(h.y & ~kCross) + __popc(h.x);
-                const bool lead = below == 0u;
-                __syncwarp();
-                if (lead) hot[e] = make_uint2(0u, (unsigned)nr | (h.y & kCross));
-                if (v && row >= cd.x) row = search(e, row - cd.y);
-                __syncwarp();
-                if (lead && v && nr >= cd.x) advance(e, nr, cd.y);
-                __syncwarp();
-                row = v ? row : -1;
-                if ((unsigned)row >= (unsigned)N && v && row >= 0) my_flags |= EP_DEV_QUOTA_OVERFLOW;
-                row = ((unsigned)row < (unsigned)N) ? row : -1;
-                if (sl < L) {
-                    dsw[sl] = row;
-                    if (srci != nullptr && row >= 0) srci[row] = s0 + sl;
-                }
-            }
-        };
 
-        int ovf = 0, bad = 0;
+        auto walk = [&](auto dir) {
+            constexpr bool kB = decltype(dir)::value;
+            // the lanes whose slots of a group come before this lane's
+            const unsigned before = kB ? lanemask_gt() : lanemask_lt();
+            // a group that ran past its instance: its last lane moves e's
+            // entries to the instance of the next rank (rank = row - del)
+            auto advance = [&](int e, int next_row, int del) {
+                const int x = next_row - del;
+                if constexpr (!kB) {
+                    const int end = ptr[e + 1];
+                    const int m = upper_bound(bcum, ptr[e], end, x);
+                    const int nd = (m < end) ? bdel[m] : 0;
+                    hot[e].y = (unsigned)(x + nd) | kCross;
+                    cold[e] = make_int2((m < end) ? bcum[m] + nd : x, nd);
+                } else {
+                    unsigned y;
+                    int2 c;
+                    back_entry(e, x, y, c);
+                    hot[e].y = y | kCross;
+                    cold[e] = c;
+                }
+            };
+            // row of the slot with `nb` lanes before it in a group whose
+            // entry row is y, and the entry's next row after a group of n
+            auto row_at = [](int y, int nb) { return kB ? y - 1 - nb : y + nb; };
+            auto moved = [](int y, int n) { return kB ? y - n : y + n; };
+            auto past = [](int row, int bound) { return kB ? row < bound : row >= bound; };
+            auto done = [](int next, int bound) { return kB ? next <= bound : next >= bound; };
+            // a step whose lanes hold a repeated id: four sub-steps of 32
+            // consecutive slots, one slot per lane, in walk order
+            auto step_by_slot = [&](int4 q, int st) {
 #pragma unroll 1
-        for (int st = 0; st < nsteps; ++st) {
-            const int4 q = buf[0];
+                for (int aa = 0; aa < 4; ++aa) {
+                    const int a = kB ? 3 - aa : aa;
+                    const int srcl = (a << 3) + (lane >> 2), c = lane & 3;
+                    const int qx = __shfl_sync(kFull, q.x, srcl), qy = __shfl_sync(kFull, q.y, srcl);
+                    const int qz = __shfl_sync(kFull, q.z, srcl), qw = __shfl_sync(kFull, q.w, srcl);
+                    const int id = c == 0 ? qx : c == 1 ? qy : c == 2 ? qz : qw;
+                    const int sl = (st << 7) + (a << 5) + lane;
+                    const bool v = (unsigned)id < (unsigned)E;
+                    const int e = v ? id : E;
+                    atomicOr(&hotw[2 * e], bit);
+                    __syncwarp();
+                    const uint2 h = hot[e];
+                    const int2 cd = cold[e];
+                    const unsigned bef = h.x & before;
+                    const int y = (int)(h.y & ~kCross);
+                    int row = row_at(y, __popc(bef));
+                    const int nx = moved(y, __popc(h.x));
+                    const bool last = bef == 0u;
+                    __syncwarp();
+                    if (last) hot[e] = make_uint2(0u, (unsigned)nx | (h.y & kCross));
+                    if (v && past(row, cd.x)) row = search(e, row - cd.y);
+                    __syncwarp();
+                    if (last && v && done(nx, cd.x)) advance(e, nx, cd.y);
+                    __syncwarp();
+                    row = v ? row : -1;
+                    if ((unsigned)row >= (unsigned)N && v && row >= 0) my_flags |= EP_DEV_QUOTA_OVERFLOW;
+                    row = ((unsigned)row < (unsigned)N) ? row : -1;
+                    if (sl < L) {
+                        dsw[sl] = row;
+                        if (srci != nullptr && row >= 0) srci[row] = s0 + sl;
+                    }
+                }
+            };
+
+            int ovf = 0, bad = 0;
+#pragma unroll 1
+            for (int i = 0; i < nmine; ++i) {
+                const int st = kB ? nsteps - 1 - i : i;
+                const int4 q = buf[0];
 #pragma unroll
-            for (int j = 0; j + 1 < kQuadAhead; ++j) buf[j] = buf[j + 1];
-            buf[kQuadAhead - 1] = load_step(st + kQuadAhead);
-            const int sl = (st << 7) + (lane << 2);
-            // invalid ids and slots past the end: the spare entries E + a
-            const bool v0 = (unsigned)q.x < (unsigned)E, v1 = (unsigned)q.y < (unsigned)E;
-            const bool v2 = (unsigned)q.z < (unsigned)E, v3 = (unsigned)q.w < (unsigned)E;
-            const int e0 = v0 ? q.x : E, e1 = v1 ? q.y : E + 1;
-            const int e2 = v2 ? q.z : E + 2, e3 = v3 ? q.w : E + 3;
-            bad |= (sl < L) && !(v0 && v1 && v2 && v3);
-            const bool dup = (e0 == e1) || (e0 == e2) || (e0 == e3) || (e1 == e2) ||
-                             (e1 == e3) || (e2 == e3);
-            if (__any_sync(kFull, dup)) {
-                step_by_slot(q, st);
-                continue;
-            }
-            atomicOr(&hotw[2 * e0], bit);
-            atomicOr(&hotw[2 * e1], bit);
-            atomicOr(&hotw[2 * e2], bit);
-            atomicOr(&hotw[2 * e3], bit);
-            __syncwarp();
-            const uint2 h0 = hot[e0], h1 = hot[e1], h2 = hot[e2], h3 = hot[e3];
-            const unsigned b0 = h0.x & lt, b1 = h1.x & lt, b2 = h2.x & lt, b3 = h3.x & lt;
-            const int y0 = (int)(h0.y & ~kCross), y1 = (int)(h1.y & ~kCross);
-            const int y2 = (int)(h2.y & ~kCross), y3 = (int)(h3.y & ~kCross);
-            int4 rows = make_int4(y0 + __popc(b0), y1 + __popc(b1), y2 + __popc(b2), y3 + __popc(b3));
-            const int n0 = y0 + __popc(h0.x), n1 = y1 + __popc(h1.x);
-            const int n2 = y2 + __popc(h2.x), n3 = y3 + __popc(h3.x);
-            __syncwarp();
-            if (b0 == 0u) hot[e0] = make_uint2(0u, (unsigned)n0 | (h0.y & kCross));
-            if (b1 == 0u) hot[e1] = make_uint2(0u, (unsigned)n1 | (h1.y & kCross));
-            if (b2 == 0u) hot[e2] = make_uint2(0u, (unsigned)n2 | (h2.y & kCross));
-            if (b3 == 0u) hot[e3] = make_uint2(0u, (unsigned)n3 | (h3.y & kCross));
-            // a group reaching the end of its instance: its leader sees it
-            // (only experts whose ranks here may cross a boundary are checked)
-            const bool x0 = b0 == 0u && (h0.y & kCross) && n0 >= cold[e0].x;
-            const bool x1 = b1 == 0u && (h1.y & kCross) && n1 >= cold[e1].x;
-            const bool x2 = b2 == 0u && (h2.y & kCross) && n2 >= cold[e2].x;
-            const bool x3 = b3 == 0u && (h3.y & kCross) && n3 >= cold[e3].x;
-            if (__any_sync(kFull, x0 || x1 || x2 || x3)) {
-                // every slot past its entry's end searches; then the leaders
-                // move their entries on
-                const int2 c0 = cold[e0], c1 = cold[e1], c2 = cold[e2], c3 = cold[e3];
-                if (v0 && rows.x >= c0.x) rows.x = search(e0, rows.x - c0.y);
-                if (v1 && rows.y >= c1.x) rows.y = search(e1, rows.y - c1.y);
-                if (v2 && rows.z >= c2.x) rows.z = search(e2, rows.z - c2.y);
-                if (v3 && rows.w >= c3.x) rows.w = search(e3, rows.w - c3.y);
+                for (int a = 0; a + 1 < kQuadAhead; ++a) buf[a] = buf[a + 1];
+                buf[kQuadAhead - 1] = load_step(i + kQuadAhead);
+                const int sl = (st << 7) + (lane << 2);
+                // invalid ids and slots past the end: the spare entries E + a
+                const bool v0 = (unsigned)q.x < (unsigned)E, v1 = (unsigned)q.y < (unsigned)E;
+                const bool v2 = (unsigned)q.z < (unsigned)E, v3 = (unsigned)q.w < (unsigned)E;
+                const int e0 = v0 ? q.x : E, e1 = v1 ? q.y : E + 1;
+                const int e2 = v2 ? q.z : E + 2, e3 = v3 ? q.w : E + 3;
+                bad |= (sl < L) && !(v0 && v1 && v2 && v3);
+                const bool dup = (e0 == e1) || (e0 == e2) || (e0 == e3) || (e1 == e2) ||
+                                 (e1 == e3) || (e2 == e3);
+                if (__any_sync(kFull, dup)) {
+                    step_by_slot(q, st);
+                    continue;
+                }
+                atomicOr(&hotw[2 * e0], bit);
+                atomicOr(&hotw[2 * e1], bit);
+                atomicOr(&hotw[2 * e2], bit);
+                atomicOr(&hotw[2 * e3], bit);
                 __syncwarp();
-                if (x0 && v0) advance(e0, n0, c0.y);
-                if (x1 && v1) advance(e1, n1, c1.y);
-                if (x2 && v2) advance(e2, n2, c2.y);
-                if (x3 && v3) advance(e3, n3, c3.y);
-            }
-            __syncwarp();
-            rows.x = v0 ? rows.x : -1;
-            rows.y = v1 ? rows.y : -1;
-            rows.z = v2 ? rows.z : -1;
-            rows.w = v3 ? rows.w : -1;
-            ovf |= (rows.x >= (int)N) | (rows.y >= (int)N) | (rows.z >= (int)N) |
-                   (rows.w >= (int)N);
-            rows.x = ((unsigned)rows.x < (unsigned)N) ? rows.x : -1;
-            rows.y = ((unsigned)rows.y < (unsigned)N) ? rows.y : -1;
-            rows.z = ((unsigned)rows.z < (unsigned)N) ? rows.z : -1;
-            rows.w = ((unsigned)rows.w < (unsigned)N) ? rows.w : -1;
-            if (sl < L) {
-                __stcs(reinterpret_cast<int4*>(dsw + sl), rows);
-                if (srci != nullptr) {
-                    const int g = s0 + sl;
-                    if (rows.x >= 0) srci[rows.x] = g;
-                    if (rows.y >= 0) srci[rows.y] = g + 1;
-                    if (rows.z >= 0) srci[rows.z] = g + 2;
-                    if (rows.w >= 0) srci[rows.w] = g + 3;
+                const uint2 h0 = hot[e0], h1 = hot[e1], h2 = hot[e2], h3 = hot[e3];
+                const unsigned b0 = h0.x & before, b1 = h1.x & before;
+                const unsigned b2 = h2.x & before, b3 = h3.x & before;
+                const int y0 = (int)(h0.y & ~kCross), y1 = (int)(h1.y & ~kCross);
+                const int y2 = (int)(h2.y & ~kCross), y3 = (int)(h3.y & ~kCross);
+                int4 rows = make_int4(row_at(y0, __popc(b0)), row_at(y1, __popc(b1)),
+                                      row_at(y2, __popc(b2)), row_at(y3, __popc(b3)));
+                const int n0 = moved(y0, __popc(h0.x)), n1 = moved(y1, __popc(h1.x));
+                const int n2 = moved(y2, __popc(h2.x)), n3 = moved(y3, __popc(h3.x));
+                __syncwarp();
+                if (b0 == 0u) hot[e0] = make_uint2(0u, (unsigned)n0 | (h0.y & kCross));
+                if (b1 == 0u) hot[e1] = make_uint2(0u, (unsigned)n1 | (h1.y & kCross));
+                if (b2 == 0u) hot[e2] = make_uint2(0u, (unsigned)n2 | (h2.y & kCross));
+                if (b3 == 0u) hot[e3] = make_uint2(0u, (unsigned)n3 | (h3.y & kCross));
+                // a group reaching the bound of its instance: its last lane
+                // sees it (only experts whose ranks here may cross are checked)
+                const bool x0 = b0 == 0u && (h0.y & kCross) && done(n0, cold[e0].x);
+                const bool x1 = b1 == 0u && (h1.y & kCross) && done(n1, cold[e1].x);
+                const bool x2 = b2 == 0u && (h2.y & kCross) && done(n2, cold[e2].x);
+                const bool x3 = b3 == 0u && (h3.y & kCross) && done(n3, cold[e3].x);
+                if (__any_sync(kFull, x0 || x1 || x2 || x3)) {
+                    // every slot past its entry's bound searches; then the
+                    // groups' last lanes move their entries on
+                    const int2 c0 = cold[e0], c1 = cold[e1], c2 = cold[e2], c3 = cold[e3];
+                    if (v0 && past(rows.x, c0.x)) rows.x = search(e0, rows.x - c0.y);
+                    if (v1 && past(rows.y, c1.x)) rows.y = search(e1, rows.y - c1.y);
+                    if (v2 && past(rows.z, c2.x)) rows.z = search(e2, rows.z - c2.y);
+                    if (v3 && past(rows.w, c3.x)) rows.w = search(e3, rows.w - c3.y);
+                    __syncwarp();
+                    if (x0 && v0) advance(e0, n0, c0.y);
+                    if (x1 && v1) advance(e1, n1, c1.y);
+                    if (x2 && v2) advance(e2, n2, c2.y);
+                    if (x3 && v3) advance(e3, n3, c3.y);
+                }
+                __syncwarp();
+                rows.x = v0 ? rows.x : -1;
+                rows.y = v1 ? rows.y : -1;
+                rows.z = v2 ? rows.z : -1;
+                rows.w = v3 ? rows.w : -1;
+                ovf |= (rows.x >= (int)N) | (rows.y >= (int)N) | (rows.z >= (int)N) |
+                       (rows.w >= (int)N);
+                rows.x = ((unsigned)rows.x < (unsigned)N) ? rows.x : -1;
+                rows.y = ((unsigned)rows.y < (unsigned)N) ? rows.y : -1;
+                rows.z = ((unsigned)rows.z < (unsigned)N) ? rows.z : -1;
+                rows.w = ((unsigned)rows.w < (unsigned)N) ? rows.w : -1;
+                if (sl < L) {
+                    __stcs(reinterpret_cast<int4*>(dsw + sl), rows);
+                    if (srci != nullptr) {
+                        const int g = s0 + sl;
+                        if (rows.x >= 0) srci[rows.x] = g;
+                        if (rows.y >= 0) srci[rows.y] = g + 1;
+                        if (rows.z >= 0) srci[rows.z] = g + 2;
+                        if (rows.w >= 0) srci[rows.w] = g + 3;
+                    }
                 }
             }
-        }
-        if (ovf) my_flags |= EP_DEV_QUOTA_OVERFLOW;
-        if (bad) my_flags |= EP_DEV_BAD_ID;
-        // every slot of the rank is ranked: the rank each expert reached
-        // (next row - del) must be the prefix over the ranks up to and
-        // including this one
-        const int32_t* want = pre + (warp + 1) * E;
+            if (ovf) my_flags |= EP_DEV_QUOTA_OVERFLOW;
+            if (bad) my_flags |= EP_DEV_BAD_ID;
+        };
+        if (back)
+            walk(std::true_type{});
+        else
+            walk(std::false_type{});
+    }
+    __syncthreads();
+    // every slot of the rank is ranked: the forward walk's next rank of each
+    // expert (row - del) must be the backward walk's lowest
+    if (has_rank && !back) {
+        const uint2* hb = hot + (E + 4);
+        const int2* cb = cold + (E + 4);
         for (int e = lane; e < E; e += 32)
-            if ((int)(hot[e].y & ~kCross) - cold[e].y != want[e]) my_flags |= EP_DEV_COUNTS_MISMATCH;
+            if ((int)(hot[e].y & ~kCross) - cold[e].y != (int)(hb[e].y & ~kCross) - cb[e].y)
+                my_flags |= EP_DEV_COUNTS_MISMATCH;
     }
     if (my_flags) atomicOr(&flags, my_flags);
     __syncthreads();
@@ -1035,7 +1120,7 @@ cudaError_t launch_reroute_quad(const ep_domain_t& d, const int32_t* ids, int64_
                                                (int)lay.bytes);
         if (err != cudaSuccess) return err;
     }
-    const int gpi = (d.R + kQuadWarps - 1) / kQuadWarps;
+    const int gpi = (d.R + kQuadRanks - 1) / kQuadRanks;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)((int64_t)n_inst * gpi));
     cfg.blockDim = dim3(kQuadThreads);
