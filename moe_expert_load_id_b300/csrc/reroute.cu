@@ -748,7 +748,7 @@ constexpr int kQuadWarps = EP_REROUTE_QUAD_WARPS;
 static_assert(kQuadWarps % 2 == 0, "two warps per source rank");
 constexpr int kQuadRanks = kQuadWarps / 2;
 constexpr int kQuadThreads = kQuadWarps * 32;
-constexpr int kQuadAhead = 3;  // steps of ids loaded ahead of the one being ranked
+constexpr int kQuadAhead = 2;  // steps of ids loaded ahead of the one being ranked
 constexpr unsigned kCross = 0x80000000u;  // hot[e].y: e's ranks here may cross a boundary
 #ifndef EP_REROUTE_QUAD_MIN_RANKS
 #define EP_REROUTE_QUAD_MIN_RANKS 296  // (instance, source rank) units from which the

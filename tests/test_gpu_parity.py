@@ -156,6 +156,12 @@ CASES = [
     ("cluster4_ragged",    8,  4, 1, 8,  30001, 1,      8,   "bad"),
     ("cluster2_ragged",    16, 4, 2, 4,  50001, 1,      8,   "zipf"),
     ("quad_E320",          16, 20, 2, 8, 3000,  19,     8,   "bad"),
+    # the quad kernel over many instances (several waves of blocks): even R,
+    # an odd R (the last block of each instance holds one source rank),
+    # invalid ids
+    ("quad_tail_R64",      64, 2, 1, 8,  1500,  40,     8,   "bad"),
+    ("quad_tail_R36",      36, 4, 1, 4,  999,   70,     8,   "zipf"),
+    ("quad_tail_R37_odd",  37, 2, 1, 4,  500,   70,     8,   "zipf"),
 ]
 
 
