@@ -34,8 +34,9 @@
 // src_slot inverse is a scattered store.
 //
 // Three kernels compute these rows and the launcher picks one by shape (see
-// launch_reroute): the quad kernel for batched launches (one warp per source
-// rank, four ranks per block, four slots per lane per step); the mask-table
+// launch_reroute): the quad kernel for batched launches (two warps per source
+// rank, one walking its first half forward and one its second half backward,
+// two ranks per block, four slots per lane per step); the mask-table
 // kernel above in 1024-thread blocks for one-layer launches, a source rank
 // split over a thread-block cluster of two or four blocks when they fit; and
 // the same kernel in 256-thread blocks for everything else.
