@@ -437,6 +437,277 @@ __device__ __forceinline__ void plan_moves_table_flags(int32_t* q, int32_t* slot
     }
 }
 
+// EP_PLAN_SKIP (with or without EP_PLAN_RELEASE) when a rank has kW <=
+// kCachedW instances (W, a template parameter so that the loops over a
+// rank's instances are exact): the same moves as plan_moves_table_flags, with each
+// lane's own ranks' instances kept in registers: the expert of every
+// instance (-1: a free spare slot), its quota and its expert's holder mask.
+// A rank's best movable instance is then a pass over registers instead of
+// dependent shared-memory reads (slot, quota, holder) on every move.  A move
+// changes two quotas (on the lanes of c and of the receiving rank), maybe one
+// spare slot on each of those ranks, and the holder mask of the moved expert,
+// which every lane copies into each of its instances of that expert.  The
+// shared-memory table is written back from the caches when the loop ends.
+constexpr int kCachedW = 8;
+
+template <int kN>
+struct RankCache {
+    int x[kN];       // expert of instance j (-1: a free spare slot)
+    int q[kN];       // quota of instance j
+    uint64_t h[kN];  // holder mask of that expert
+};
+
+template <bool kTwo, bool kPacked, int kW>
+__device__ __forceinline__ void plan_moves_skip_cached(int32_t* q, int32_t* slot,
+                                                       uint64_t* holder, int32_t* Ls,
+                                                       int& loadA, int& loadB, int lane, int H,
+                                                       int S, int R, int max_iters, int flags,
+                                                       int& iters, int& status) {
+    constexpr int W = kW;
+    const bool release = (flags & EP_PLAN_RELEASE) != 0;
+    const bool hasA = loadA >= 0, hasB = kTwo && loadB >= 0;
+    const int ra = lane, rb = lane + 32;
+    const uint64_t exist = (R >= 64) ? ~0ull : ((1ull << R) - 1ull);
+    uint64_t freem = S > 0 ? exist : 0ull;  // ranks with a free spare slot (warp-uniform)
+    // the caches of my ranks' instances
+    RankCache<kW> A, B;
+    auto fill = [&](RankCache<kW>& C, bool has, int r) {
+#pragma unroll
+        for (int j = 0; j < kW; ++j) {
+            int x = -1, qq = 0;
+            uint64_t hh = 0ull;
+            if (has) {
+                x = j < H ? r * H + j : slot[r * S + (j - H)];
+                qq = q[r * W + j];
+                hh = x >= 0 ? holder[x] : 0ull;
+            }
+            C.x[j] = x;
+            C.q[j] = qq;
+            C.h[j] = hh;
+        }
+    };
+    fill(A, hasA, ra);
+    if (kTwo) fill(B, hasB, rb);
+    // my ranks' masks of the ranks at least 2 below them, as halves
+    Ls[ra] = hasA ? loadA : INT_MAX;
+    Ls[rb] = hasB ? loadB : INT_MAX;
+    __syncwarp();
+    unsigned loA = 0u, hiA = 0u, loB = 0u, hiB = 0u;
+    {
+        const int tA = loadA - 2, tB = loadB - 2;
+#pragma unroll 4
+        for (int d = 0; d < 32; d += 4) {
+            const int4 v = *reinterpret_cast<const int4*>(Ls + d);
+            const int4 w = *reinterpret_cast<const int4*>(Ls + 32 + d);
+            loA |= ((unsigned)(v.x <= tA) | (unsigned)(v.y <= tA) << 1 |
+                    (unsigned)(v.z <= tA) << 2 | (unsigned)(v.w <= tA) << 3) << d;
+            hiA |= ((unsigned)(w.x <= tA) | (unsigned)(w.y <= tA) << 1 |
+                    (unsigned)(w.z <= tA) << 2 | (unsigned)(w.w <= tA) << 3) << d;
+            if (kTwo) {
+                loB |= ((unsigned)(v.x <= tB) | (unsigned)(v.y <= tB) << 1 |
+                        (unsigned)(v.z <= tB) << 2 | (unsigned)(v.w <= tB) << 3) << d;
+                hiB |= ((unsigned)(w.x <= tB) | (unsigned)(w.y <= tB) << 1 |
+                        (unsigned)(w.z <= tB) << 2 | (unsigned)(w.w <= tB) << 3) << d;
+            }
+        }
+    }
+    // a rank's best instance (largest quota >= 1, lowest expert) whose expert
+    // has an eligible rank in the rank's low mask, as the key
+    // quota << 32 | (2047 - expert) << 5 | j (0: none).  The instances are
+    // tested independently and the keys meet in a max (experts are below
+    // 2048 and distinct within a rank).
+    auto best = [&](const RankCache<kW>& C, bool has, uint64_t low) -> uint64_t {
+        uint64_t k = 0ull;
+#pragma unroll
+        for (int j = 0; j < kW; ++j) {
+            const int x = C.x[j], qq = C.q[j];
+            const bool ok = has && x >= 0 && qq >= 1 && ((C.h[j] | freem) & low) != 0ull;
+            const uint64_t kj = ok ? ((uint64_t)(unsigned)qq << 32) |
+                                         ((unsigned)(2047 - x) << 5) | (unsigned)j
+                                   : 0ull;
+            k = kj > k ? kj : k;
+        }
+        return k;
+    };
+    while (true) {
+        const uint64_t kA = best(A, hasA, ((uint64_t)hiA << 32) | loA);
+        const uint64_t kB = kTwo ? best(B, hasB, ((uint64_t)hiB << 32) | loB) : 0ull;
+        // the first rank in (load desc, index asc) order with a movable instance
+        const bool mA = kA != 0ull, mB = kTwo && kB != 0ull;
+        int c, Lc;
+        if (kPacked) {
+            const unsigned ka = mA ? ((unsigned)loadA << 6) | (unsigned)(63 - ra) : 0u;
+            const unsigned kb = mB ? ((unsigned)loadB << 6) | (unsigned)(31 - lane) : 0u;
+            const unsigned k = __reduce_max_sync(kFull, kTwo ? max(ka, kb) : ka);
+            if (k == 0u) break;  // no candidate can move
+            c = 63 - (int)(k & 63u);
+            Lc = (int)(k >> 6);
+        } else {
+            const int la = mA ? loadA : -1, lb = mB ? loadB : -1;
+            Lc = __reduce_max_sync(kFull, kTwo ? max(la, lb) : la);
+            if (Lc < 0) break;
+            const unsigned b0 = __ballot_sync(kFull, mA && la == Lc);
+            const unsigned b1 = kTwo ? __ballot_sync(kFull, mB && lb == Lc) : 0u;
+            c = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+        }
+        const bool cB = c >= 32;
+        const int cl = c & 31;
+        // c's best instance and its expert's holder mask, from c's lane
+        const uint64_t kc = cB ? kB : kA;
+        const int jc = (int)(kc & 31u);
+        uint64_t bh = 0ull;
+#pragma unroll
+        for (int j = 0; j < kW; ++j) bh = j == jc ? (cB ? B.h[j] : A.h[j]) : bh;
+        const int qsrc = (int)__shfl_sync(kFull, (unsigned)(kc >> 32), cl);
+        const unsigned lo_key = __shfl_sync(kFull, (unsigned)kc, cl);
+        const int e = 2047 - (int)(lo_key >> 5);
+        const int src_j = (int)(lo_key & 31u);
+        const uint64_t hm = ((uint64_t)__shfl_sync(kFull, (unsigned)(bh >> 32), cl) << 32) |
+                            (uint64_t)__shfl_sync(kFull, (unsigned)bh, cl);
+        // the coldest eligible rank (lowest index on ties)
+        const uint64_t el = (hm | freem) & exist & ~(1ull << c);
+        const bool elA = hasA && (((unsigned)el >> lane) & 1u);
+        const bool elB = hasB && (((unsigned)(el >> 32) >> lane) & 1u);
+        int cold, Lmin;
+        if (kPacked) {
+            const unsigned ca = elA ? ((unsigned)loadA << 6) | (unsigned)ra : 0xffffffffu;
+            const unsigned cb = elB ? ((unsigned)loadB << 6) | (unsigned)rb : 0xffffffffu;
+            const unsigned kk = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            cold = (int)(kk & 63u);
+            Lmin = (int)(kk >> 6);
+        } else {
+            const int ca = elA ? loadA : INT_MAX;
+            const int cb = elB ? loadB : INT_MAX;
+            Lmin = __reduce_min_sync(kFull, kTwo ? min(ca, cb) : ca);
+            const unsigned b0 = __ballot_sync(kFull, elA && ca == Lmin);
+            const unsigned b1 = kTwo ? __ballot_sync(kFull, elB && cb == Lmin) : 0u;
+            cold = b0 ? __ffs(b0) - 1 : 32 + __ffs(b1) - 1;
+        }
+        // the receiving rank's spare slots holding e, and its free ones (bit
+        // j: instance j), from the lane that caches that rank
+        unsigned hitA = 0u, freeA = 0u, hitB = 0u, freeB = 0u;
+#pragma unroll
+        for (int j = 0; j < kW; ++j) {
+            if (j >= H) {
+                hitA |= (A.x[j] == e ? 1u : 0u) << j;
+                freeA |= (A.x[j] < 0 ? 1u : 0u) << j;
+                if (kTwo) {
+                    hitB |= (B.x[j] == e ? 1u : 0u) << j;
+                    freeB |= (B.x[j] < 0 ? 1u : 0u) << j;
+                }
+            }
+        }
+        const bool dB = cold >= 32;
+        const int dl = cold & 31;
+        const unsigned hit = __shfl_sync(kFull, dB ? hitB : hitA, dl);
+        const unsigned freeb = __shfl_sync(kFull, dB ? freeB : freeA, dl);
+        const int mv = min(qsrc, (Lc - Lmin) >> 1);
+        if (mv <= 0) break;  // (never: a movable candidate has a rank 2 below it)
+        if (iters == max_iters) {
+            status = EP_ERR_ITER_LIMIT;
+            break;
+        }
+        // the move: loads, then the masks (c and cold from ballots over the new
+        // loads; every other rank re-tests bits c and cold)
+        loadA += (ra == cold ? mv : 0) - (ra == c ? mv : 0);
+        if (kTwo) loadB += (rb == cold ? mv : 0) - (rb == c ? mv : 0);
+        {
+            const int nLc = Lc - mv, nLd = Lmin + mv;
+            const unsigned cLo = __ballot_sync(kFull, hasA && loadA <= nLc - 2);
+            const unsigned cHi = kTwo ? __ballot_sync(kFull, hasB && loadB <= nLc - 2) : 0u;
+            const unsigned dLo = __ballot_sync(kFull, hasA && loadA <= nLd - 2);
+            const unsigned dHi = kTwo ? __ballot_sync(kFull, hasB && loadB <= nLd - 2) : 0u;
+            const unsigned bc = 1u << (c & 31), bd = 1u << (cold & 31);
+            const bool cLoHalf = c < 32, dLoHalf = cold < 32;
+            // (selects, no divergent branches: every lane takes the same path)
+            const unsigned mcLo = cLoHalf ? bc : 0u, mcHi = cLoHalf ? 0u : bc;
+            const unsigned mdLo = dLoHalf ? bd : 0u, mdHi = dLoHalf ? 0u : bd;
+            auto retest = [&](int r, int L, unsigned& lo, unsigned& hi) {
+                const bool sc = nLc <= L - 2, sd = nLd <= L - 2;
+                const unsigned nlo = (lo & ~(mcLo | mdLo)) | (sc ? mcLo : 0u) | (sd ? mdLo : 0u);
+                const unsigned nhi = (hi & ~(mcHi | mdHi)) | (sc ? mcHi : 0u) | (sd ? mdHi : 0u);
+                lo = r == c ? cLo : (r == cold ? dLo : nlo);
+                hi = r == c ? cHi : (r == cold ? dHi : nhi);
+            };
+            if (hasA) retest(ra, loadA, loA, hiA);
+            if (hasB) retest(rb, loadB, loB, hiB);
+        }
+        // cold's instance of e: its home, a spare slot holding e, else its
+        // lowest free slot
+        const int ej = e - cold * H;
+        const bool home = (unsigned)ej < (unsigned)H;
+        const bool held = home || hit != 0u;
+        const unsigned pick = held ? hit : freeb;
+        if (!home && pick == 0u) {  // (never; keeps every index in range)
+            status = EP_ERR_INVAL;
+            break;
+        }
+        const int dst_j = home ? ej : __ffs(pick) - 1;
+        const bool freed = release && src_j >= H && qsrc == mv;  // the source replica emptied
+        uint64_t h2 = held ? hm : (hm | (1ull << cold));
+        if (freed) h2 &= ~(1ull << c);
+        // the caches (selects only): c's instance src_j and cold's instance
+        // dst_j, then the holder mask of every cached instance of e
+        auto apply = [&](RankCache<kW>& C, int r) {
+            const bool isc = r == c, isd = r == cold;
+#pragma unroll
+            for (int j = 0; j < kW; ++j) {
+                const bool js = isc && j == src_j, jd = isd && j == dst_j;
+                C.q[j] = js ? C.q[j] - mv : (jd ? C.q[j] + mv : C.q[j]);
+                C.x[j] = (js && freed) ? -1 : ((jd && !held) ? e : C.x[j]);
+                C.h[j] = C.x[j] == e ? h2 : (C.x[j] < 0 ? 0ull : C.h[j]);
+            }
+        };
+        apply(A, ra);
+        if (kTwo) apply(B, rb);
+        if (!held && (freeb & (freeb - 1u)) == 0u) freem &= ~(1ull << cold);  // its last free slot
+        if (freed) freem |= 1ull << c;
+        ++iters;
+    }
+    // the table from the caches: each lane its ranks' quotas and spare slots,
+    // and the holder mask of each of their home experts (every expert has
+    // one home rank, whose cache holds its current mask)
+    auto write_back = [&](const RankCache<kW>& C, bool has, int r) {
+        if (!has) return;
+#pragma unroll
+        for (int j = 0; j < kW; ++j) {
+            q[r * W + j] = C.q[j];
+            if (j >= H) slot[r * S + (j - H)] = C.x[j];
+            else holder[C.x[j]] = C.h[j];
+        }
+    };
+    write_back(A, hasA, ra);
+    if (kTwo) write_back(B, hasB, rb);
+    __syncwarp();
+}
+
+// The skip rule on the cached loop when W <= kCachedW; false: not handled.
+template <bool kTwo, bool kPacked>
+__device__ __forceinline__ bool plan_moves_skip_cached_w(int32_t* q, int32_t* slot,
+                                                         uint64_t* holder, int32_t* Ls,
+                                                         int& loadA, int& loadB, int lane, int H,
+                                                         int S, int W, int R, int max_iters,
+                                                         int flags, int& iters, int& status) {
+#define EP_SKIP_CACHED_CASE(w)                                                                    \
+    case w:                                                                                       \
+        plan_moves_skip_cached<kTwo, kPacked, w>(q, slot, holder, Ls, loadA, loadB, lane, H, S, R, \
+                                                 max_iters, flags, iters, status);                \
+        return true;
+    switch (W) {
+        EP_SKIP_CACHED_CASE(1)
+        EP_SKIP_CACHED_CASE(2)
+        EP_SKIP_CACHED_CASE(3)
+        EP_SKIP_CACHED_CASE(4)
+        EP_SKIP_CACHED_CASE(5)
+        EP_SKIP_CACHED_CASE(6)
+        EP_SKIP_CACHED_CASE(7)
+        EP_SKIP_CACHED_CASE(8)
+        default:
+            return false;
+    }
+#undef EP_SKIP_CACHED_CASE
+}
+
 // Counts must be >= 0 with a total below 2^31; otherwise the instance is
 // rejected (EP_ERR_INVAL).  tot: the warp-uniform total.
 __device__ __forceinline__ int plan_check_counts(const int32_t* cnt, int E, int lane,
@@ -484,7 +755,16 @@ __device__ __forceinline__ void plan_table_solve(const int32_t* cnt, int R, int 
     }
     __syncwarp();
     if (kFlags) {
-        if (status == EP_OK) {
+        bool done = false;
+        if (status == EP_OK && (flags & EP_PLAN_SKIP) && W <= kCachedW)
+            done = tot < kPackLimit
+                       ? plan_moves_skip_cached_w<kTwo, true>(q, slot, holder, Ls, loadA, loadB,
+                                                              lane, H, S, W, R, max_iters, flags,
+                                                              iters, status)
+                       : plan_moves_skip_cached_w<kTwo, false>(q, slot, holder, Ls, loadA, loadB,
+                                                               lane, H, S, W, R, max_iters, flags,
+                                                               iters, status);
+        if (!done && status == EP_OK) {
             if (tot < kPackLimit)
                 plan_moves_table_flags<kTwo, true>(q, slot, holder, Ls, loadA, loadB, lane, H, S,
                                                    W, R, max_iters, flags, iters, status);

@@ -162,3 +162,41 @@ def test_base_rule_table_loop_wide_keys():
     got = _gpu_plan(R, E, S, c, 0)
     for g in range(c.shape[0]):
         _same(got, g, oracle.plan(c[g], R, E, S))
+
+
+# The skip variants keep each lane's ranks' instances in registers when a rank
+# has at most 8 (W = H + S); wider ranks take the shared-memory table loop.
+# These shapes pin both against the oracle: W = 1 (no spare slot), 8 (the
+# widest cached), 9, 10 and 32 (the table loop), one and two ranks per lane,
+# and totals past 2^25 (the unpacked reductions) on the cached loop.
+SKIP_SHAPES = [(5, 1, 0), (16, 2, 6), (64, 4, 4), (8, 8, 1), (33, 4, 6), (20, 16, 16)]
+
+
+@pytest.mark.parametrize("variant", ["skip", "skip+release"])
+@pytest.mark.parametrize("shape", SKIP_SHAPES, ids=[f"R{r}H{h}S{s}" for r, h, s in SKIP_SHAPES])
+def test_skip_instance_widths(shape, variant):
+    R, H, S = shape
+    E = R * H
+    rng = np.random.default_rng(R * 1000 + H * 10 + S)
+    c = np.stack([(500.0 / (1 + rng.permutation(E)) ** rng.uniform(0.5, 1.6)).astype(np.int32)
+                  for _ in range(12)])
+    got = _gpu_plan(R, E, S, c, FLAGS[variant])
+    for g in range(c.shape[0]):
+        _same(got, g, oracle.plan(c[g], R, E, S, variant=variant))
+    cap = max(1, min(int(oracle.plan(c[g], R, E, S, variant=variant)["n_iter"])
+                     for g in range(c.shape[0])) // 2)
+    got = _gpu_plan(R, E, S, c, FLAGS[variant], cap)
+    for g in range(c.shape[0]):
+        _same(got, g, oracle.plan(c[g], R, E, S, max_iters=cap, variant=variant))
+
+
+def test_skip_wide_keys():
+    # totals of 2^25 and more: the cached skip loop's unpacked reductions
+    R, H, S = 64, 2, 1
+    E = R * H
+    rng = np.random.default_rng(9)
+    c = (rng.random((3, E)) ** 3 * 4.0e6).astype(np.int32)
+    assert (c.sum(1) >= (1 << 25)).all()
+    got = _gpu_plan(R, E, S, c, FLAGS["skip"], 3000)
+    for g in range(c.shape[0]):
+        _same(got, g, oracle.plan(c[g], R, E, S, max_iters=3000, variant="skip"))
