@@ -598,9 +598,9 @@ __device__ __forceinline__ void plan_moves_skip_cached(int32_t* q, int32_t* slot
             }
         }
         const bool dB = cold >= 32;
-        const int dl = cold & 31;
-        const unsigned hit = __shfl_sync(kFull, dB ? hitB : hitA, dl);
-        const unsigned freeb = __shfl_sync(kFull, dB ? freeB : freeA, dl);
+        const unsigned hf = __shfl_sync(kFull, dB ? (hitB | freeB << 16) : (hitA | freeA << 16),
+                                        cold & 31);
+        const unsigned hit = hf & 0xffffu, freeb = hf >> 16;
         const int mv = min(qsrc, (Lc - Lmin) >> 1);
         if (mv <= 0) break;  // (never: a movable candidate has a rank 2 below it)
         if (iters == max_iters) {
@@ -655,7 +655,7 @@ __device__ __forceinline__ void plan_moves_skip_cached(int32_t* q, int32_t* slot
                 const bool js = isc && j == src_j, jd = isd && j == dst_j;
                 C.q[j] = js ? C.q[j] - mv : (jd ? C.q[j] + mv : C.q[j]);
                 C.x[j] = (js && freed) ? -1 : ((jd && !held) ? e : C.x[j]);
-                C.h[j] = C.x[j] == e ? h2 : (C.x[j] < 0 ? 0ull : C.h[j]);
+                C.h[j] = C.x[j] == e ? h2 : C.h[j];  // (a free slot's is never read)
             }
         };
         apply(A, ra);
