@@ -515,13 +515,14 @@ __device__ __forceinline__ void plan_moves_skip_cached(int32_t* q, int32_t* slot
     // has an eligible rank in the rank's low mask, as the key
     // quota << 32 | (2047 - expert) << 5 | j (0: none).  The instances are
     // tested independently and the keys meet in a max (experts are below
-    // 2048 and distinct within a rank).
-    auto best = [&](const RankCache<kW>& C, bool has, uint64_t low) -> uint64_t {
+    // 2048 and distinct within a rank).  A quota >= 1 implies an expert (a
+    // free slot has quota 0), and a lane without the rank caches free slots.
+    auto best = [&](const RankCache<kW>& C, uint64_t low) -> uint64_t {
         uint64_t k = 0ull;
 #pragma unroll
         for (int j = 0; j < kW; ++j) {
             const int x = C.x[j], qq = C.q[j];
-            const bool ok = has && x >= 0 && qq >= 1 && ((C.h[j] | freem) & low) != 0ull;
+            const bool ok = qq >= 1 && ((C.h[j] | freem) & low) != 0ull;
             const uint64_t kj = ok ? ((uint64_t)(unsigned)qq << 32) |
                                          ((unsigned)(2047 - x) << 5) | (unsigned)j
                                    : 0ull;
@@ -530,8 +531,8 @@ __device__ __forceinline__ void plan_moves_skip_cached(int32_t* q, int32_t* slot
         return k;
     };
     while (true) {
-        const uint64_t kA = best(A, hasA, ((uint64_t)hiA << 32) | loA);
-        const uint64_t kB = kTwo ? best(B, hasB, ((uint64_t)hiB << 32) | loB) : 0ull;
+        const uint64_t kA = best(A, ((uint64_t)hiA << 32) | loA);
+        const uint64_t kB = kTwo ? best(B, ((uint64_t)hiB << 32) | loB) : 0ull;
         // the first rank in (load desc, index asc) order with a movable instance
         const bool mA = kA != 0ull, mB = kTwo && kB != 0ull;
         int c, Lc;
@@ -649,10 +650,10 @@ __device__ __forceinline__ void plan_moves_skip_cached(int32_t* q, int32_t* slot
         // the caches (selects only): c's instance src_j and cold's instance
         // dst_j, then the holder mask of every cached instance of e
         auto apply = [&](RankCache<kW>& C, int r) {
-            const bool isc = r == c, isd = r == cold;
+            const int sj = r == c ? src_j : -1, dj = r == cold ? dst_j : -1;
 #pragma unroll
             for (int j = 0; j < kW; ++j) {
-                const bool js = isc && j == src_j, jd = isd && j == dst_j;
+                const bool js = j == sj, jd = j == dj;
                 C.q[j] = js ? C.q[j] - mv : (jd ? C.q[j] + mv : C.q[j]);
                 C.x[j] = (js && freed) ? -1 : ((jd && !held) ? e : C.x[j]);
                 C.h[j] = C.x[j] == e ? h2 : C.h[j];  // (a free slot's is never read)
