@@ -1,5 +1,6 @@
 // Device code of the planner: the count checks, the shared-memory table move
-// loops of the flag-free rule and of the rule variants, and the
+// loops of the flag-free rule and of the rule variants, the register-cached
+// loop of the skip variants (ranks of at most eight instances), and the
 // logical->physical CSR epilogue.
 //
 // UltraEP article (m.youleyou.com), "key design" section, control-plane
