@@ -304,6 +304,59 @@ def test_reroute_flags_counts_of_other_ids(case):
     b.guard.check()
 
 
+@pytest.mark.parametrize("case", [(64, 2, 1, 8, 8192, 5), (16, 4, 2, 4, 12000, 20)])
+def test_quad_reroute_past_the_quotas(case):
+    # a plan whose last replicas hold less than their experts' counts (every
+    # source rank walked by two warps, the backward one starting above the
+    # quotas): the overflowing slots get no row and the flag, every other row
+    # is the oracle's, bit for bit
+    R, H, S, k, T, n_inst = case
+    E = R * H
+    dom = G().dom_of(R, E, S, k)
+    ids_np = _make_ids(R, E, k, T, n_inst, "zipf", 77)
+    ids = torch.from_numpy(ids_np).cuda()
+    b = G().guarded_buffers(dom, T, n_inst, src_slot=True)
+    b.count(ids)
+    b.plan()
+    quota = b.quota.cpu().numpy().copy()
+    ptr = b.inst_ptr.cpu().numpy()
+    iid = b.inst_id.cpu().numpy()
+    cum = b.inst_cum.cpu().numpy().copy()
+    short = 0
+    for g in range(n_inst):
+        for e in range(E):
+            lo, hi = int(ptr[g, e]), int(ptr[g, e + 1])
+            if hi - lo >= 2:                  # trim the last replica of a replicated expert
+                p_last = int(iid[g, hi - 1])
+                cut = (int(quota[g, p_last]) + 2) // 3
+                quota[g, p_last] -= cut
+                short += cut
+                run = 0
+                for m in range(lo, hi):
+                    run += int(quota[g, int(iid[g, m])])
+                    cum[g, m] = run
+    assert short > 0
+    b.quota.copy_(torch.from_numpy(quota))
+    b.inst_cum.copy_(torch.from_numpy(cum))
+    b.dev_status.zero_()
+    b.reroute(ids)
+    torch.cuda.synchronize()
+    assert int(b.dev_status.item()) & U.EP_DEV_QUOTA_OVERFLOW
+    dst = b.dst_row.cpu().numpy()
+    src = b.src_slot.cpu().numpy()
+    off = b.inst_offset.cpu().numpy()
+    n_none = 0
+    for g in range(n_inst):
+        pl = dict(quota=quota[g], inst_ptr=ptr[g], inst_id=iid[g], inst_cum=cum[g])
+        d_o, s_o, o_o = oracle.reroute(ids_np[g], R, E, S, pl)
+        assert np.array_equal(dst[g], d_o), g
+        assert np.array_equal(src[g], s_o), g
+        assert np.array_equal(off[g], o_o), g
+        n_none += int((d_o < 0).sum())
+    assert n_none == short
+    b.guard.check()
+
+
 def test_workspace_reused_across_calls():
     w, ids, _ = _tiny_inputs([0, 1])
     dom = G().dom_of(w.R, w.E, w.S, w.k)
