@@ -270,7 +270,7 @@ def test_device_status_flags():
 
 
 @pytest.mark.parametrize("case", [(8, 4, 1, 4, 4096, 2), (64, 2, 1, 8, 131072, 1),
-                                  (64, 2, 1, 8, 4096, 5)])
+                                  (64, 2, 1, 8, 4096, 5), (64, 2, 1, 8, 2048, 40)])
 def test_reroute_flags_counts_of_other_ids(case):
     # counts_src taken from other ids (another layer's buffer): every block
     # compares what it ranked with its own counts_src row and flags the
@@ -295,16 +295,21 @@ def test_reroute_flags_counts_of_other_ids(case):
     assert int(b.dev_status.item()) & U.EP_DEV_COUNTS_MISMATCH
     # only the block of source rank 0 of an instance starts at prefix zero; a
     # counts_src differing in one entry still raises the flag
-    b.dev_status.zero_()
-    b.count(ids_b)
-    b.counts_src[0, R - 1, int(ids_b[0, -1, 0].item())] += 1
-    b.reroute(ids_b)
-    torch.cuda.synchronize()
-    assert int(b.dev_status.item()) & U.EP_DEV_COUNTS_MISMATCH
+    for g in sorted({0, n_inst - 1}):     # the first and the last instance of the batch
+        b.dev_status.zero_()
+        b.count(ids_b)
+        b.reroute(ids_b)
+        torch.cuda.synchronize()
+        assert int(b.dev_status.item()) == 0
+        b.counts_src[g, R - 1, int(ids_b[g, -1, 0].item())] += 1
+        b.reroute(ids_b)
+        torch.cuda.synchronize()
+        assert int(b.dev_status.item()) & U.EP_DEV_COUNTS_MISMATCH
     b.guard.check()
 
 
-@pytest.mark.parametrize("case", [(64, 2, 1, 8, 8192, 5), (16, 4, 2, 4, 12000, 20)])
+@pytest.mark.parametrize("case", [(64, 2, 1, 8, 8192, 5), (16, 4, 2, 4, 12000, 20),
+                                  (64, 2, 1, 8, 4096, 40)])
 def test_quad_reroute_past_the_quotas(case):
     # a plan whose last replicas hold less than their experts' counts (every
     # source rank walked by two warps, the backward one starting above the
