@@ -64,9 +64,8 @@ constexpr int kMaxChunksPerRank = 8;            // portable cluster size
 #endif
 
 // columns of the lane-column histogram: 16 (lanes l and l+16 share a column,
-// at most a 2-way same-address collision) while E*16 ints fit 32 KB.  Four
-// blocks per SM with two 16-byte loads per thread measured faster than three
-// blocks with four loads and 32 columns.
+// at most a 2-way same-address collision) while E*16 ints fit 32 KB.  (32
+// columns, whose table leaves room for three blocks per SM, measured slower.)
 #ifndef EP_COUNT_COLS
 #define EP_COUNT_COLS 16                        // lane columns at most (build-time tunable)
 #endif
